@@ -1,1 +1,13 @@
-"""Packed linear-attention pass for GB300 (sm_103a)."""
+"""Packed linear-attention pass for GB300 (sm_103a).
+
+The compute path is ``libspanla.so`` (hand-written CUDA kernels behind the C
+ABI in ``include/spanla.h``); :mod:`.spanla` is its thin Python binding and
+:mod:`.workloads` the seeded synthetic inputs.
+"""
+from .spanla import (  # noqa: F401
+    SpanLAError,
+    load_library,
+    span_la_branches_from_state,
+    span_la_check,
+    span_la_pass,
+)

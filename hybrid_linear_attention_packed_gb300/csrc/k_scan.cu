@@ -1,0 +1,68 @@
+// Segmented scan kernel: one exclusive prefix scan of chunk states across
+// every segment of the pass, in a single launch.
+//
+// "Serving 0.88M TPS from Two RTXs and Mac Minis", section "Kernels": one scan
+// covers every view in a pass instead of one scan per view (the second of the
+// three launches).  For segment s with state slots c0 .. c0+n-1 it replaces
+// slot c by  sum_{c' < c} dS_{c'}  (the state entering chunk c) and writes the
+// segment total (the view's final state) to final_out[final_idx] when
+// final_idx >= 0.  An empty view (n = 0) gets the zero state.
+//
+// fp32 adds on CUDA cores; the kernel is bound by memory traffic.  One CTA of
+// 256 threads owns a 1,024-float quarter of one (segment, head) state and
+// walks the segment's chunks in order, keeping the running sum in registers
+// and loading eight chunks ahead so the loads stay in flight while the
+// stores drain.
+#include "spanla_internal.h"
+
+namespace spanla {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kSlices = kStateFloats / (kThreads * 4);   // 4 CTAs per (segment, head)
+constexpr int kAhead = 8;
+
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+__global__ void __launch_bounds__(kThreads)
+segmented_scan_kernel(const ScanDesc* __restrict__ scan, int H, float* __restrict__ ws,
+                      float* __restrict__ final_out) {
+  const ScanDesc sd = scan[blockIdx.x];
+  const int h = blockIdx.y;
+  const int off = (blockIdx.z * kThreads + threadIdx.x) * 4;
+  const int64_t stride = static_cast<int64_t>(H) * kStateFloats;
+  float* p = ws + (static_cast<int64_t>(sd.chunk0) * H + h) * kStateFloats + off;
+
+  float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < sd.nchunks; c0 += kAhead) {
+    float4 x[kAhead];
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j)
+      if (c0 + j < sd.nchunks) x[j] = *reinterpret_cast<const float4*>(p + (c0 + j) * stride);
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) {
+      if (c0 + j < sd.nchunks) {
+        *reinterpret_cast<float4*>(p + (c0 + j) * stride) = run;
+        run = add4(run, x[j]);
+      }
+    }
+  }
+  if (sd.final_idx >= 0) {
+    float* f = final_out + (static_cast<int64_t>(sd.final_idx) * H + h) * kStateFloats + off;
+    *reinterpret_cast<float4*>(f) = run;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_scan(const ScanDesc* scan, int n_scan, int H, float* ws, float* final_out,
+                        cudaStream_t stream) {
+  if (n_scan <= 0) return cudaSuccess;
+  const dim3 grid(n_scan, H, kSlices);
+  segmented_scan_kernel<<<grid, kThreads, 0, stream>>>(scan, H, ws, final_out);
+  return cudaGetLastError();
+}
+
+}  // namespace spanla

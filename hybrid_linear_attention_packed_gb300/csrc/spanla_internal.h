@@ -1,0 +1,76 @@
+// Internal interface between the host side of libspanla (validation,
+// descriptor build, workspace, launches) and its CUDA kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace spanla {
+
+constexpr int kHeadDim = 64;     // d_k = d_v
+constexpr int kChunk = 64;       // rows per chunk of the state scan
+constexpr int kTileRows = 128;   // rows per output tile (two chunks)
+constexpr int kStateFloats = kHeadDim * kHeadDim;
+
+// One 64-row chunk whose local state K_c^T V_c the chunk-state kernel
+// computes.  Chunk i of the table owns state slot i of the workspace.
+struct ChunkDesc {
+  int32_t row0;   // first row of the chunk in the packed buffer
+  int32_t len;    // valid rows, 1..64
+};
+
+// One segment's run of chunk-state slots for the segmented scan.
+struct ScanDesc {
+  int32_t chunk0;     // first state slot
+  int32_t nchunks;    // slots in the run (0 for an empty view)
+  int32_t final_idx;  // index into the final-state output, or -1
+  int32_t pad;
+};
+
+// One output tile of up to 128 rows, for one head (the grid's y index).
+// Rows [row0, row0 + nrows) are contiguous; they hold one view's rows, one
+// long branch's rows, or several whole short branches of the same parent.
+// bounds[bound0 .. bound0 + nbound) are the ascending row offsets (relative to
+// row0, first one 0) at which a segment starts inside the tile.  The tile's
+// start state is  stateA[a] + stateB[b]  (a missing term is -1).
+struct TileDesc {
+  int32_t row0;
+  int32_t nrows;
+  int32_t stateA;   // parent view final state (pass) / cached state index
+  int32_t stateB;   // exclusive chunk-prefix slot of the tile's first chunk
+  int32_t bound0;
+  int32_t nbound;
+  int32_t pad0;
+  int32_t pad1;
+};
+
+struct DeviceOperands {
+  // TMA descriptors; [0] = bf16 value (or high part), [1] = low part (fp32 inputs).
+  CUtensorMap q[2], k[2], v[2];
+};
+
+// Kernel launchers (each returns the launch error, if any).
+cudaError_t launch_split_f32(const float* q, const float* k, const float* v, int64_t n,
+                             void* hi_lo_base, cudaStream_t stream);
+
+cudaError_t launch_chunk_state(bool split, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                               const ChunkDesc* chunks, int n_chunks, int H, float* ws,
+                               unsigned* err, cudaStream_t stream);
+
+cudaError_t launch_scan(const ScanDesc* scan, int n_scan, int H, float* ws, float* final_out,
+                        cudaStream_t stream);
+
+cudaError_t launch_tile_output(bool split, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                               const CUtensorMap* tm_v, const TileDesc* tiles, int n_tiles,
+                               const uint8_t* bounds, const float* stateA, const float* stateB,
+                               void* out, int H, unsigned* err, cudaStream_t stream);
+
+cudaError_t launch_wait_timeout_probe(unsigned limit_us, unsigned* err, cudaStream_t stream);
+
+// Box sizes of the TMA descriptors each kernel expects.
+constexpr int kChunkBoxRows = kChunk;     // chunk-state kernel: 64 rows x 2 heads
+constexpr int kChunkBoxHeads = 2;
+constexpr int kTileBoxRows = kTileRows;   // tile-output kernel: 128 rows x 1 head
+
+}  // namespace spanla

@@ -1,0 +1,199 @@
+"""Thin Python binding of ``libspanla.so`` (argument marshalling only).
+
+Every step of the pass runs in the library's CUDA kernels; this module only
+checks tensor dtypes, shapes, devices and contiguity, converts host metadata to
+int32 arrays and passes raw pointers and the current CUDA stream through the C
+ABI declared in ``include/spanla.h``.  PyTorch is used for device memory and
+streams only.  There is no fallback: if the library is missing or cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.environ.get("SPANLA_LIB", os.path.join(_PKG, "libspanla.so"))
+
+SPAN_LA_BF16 = 0
+SPAN_LA_F32 = 1
+
+STATUS = {0: "SPAN_LA_OK", 1: "SPAN_LA_ERR_INVALID", 2: "SPAN_LA_ERR_UNSUPPORTED",
+          3: "SPAN_LA_ERR_CUDA", 4: "SPAN_LA_ERR_NOMEM", 5: "SPAN_LA_ERR_TIMEOUT"}
+
+EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
+            "span_la_status_string", "span_la_last_error_detail", "span_la_version",
+            "span_la_selftest_wait_timeout")
+
+
+class SpanLAError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__("%s: %s (%s)" % (where, STATUS.get(status, status), detail))
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("total_rows", ctypes.c_int64), ("num_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: Optional[str] = None):
+    """Load the CUDA library (raises if it is missing: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError("libspanla.so not found at %s: build it with "
+                               "hybrid_linear_attention_packed_gb300.build.build()" % p)
+        lib = ctypes.CDLL(p)
+        vp, i32p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)
+        lib.span_la_pass.argtypes = [vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
+                                     ctypes.c_int32, i32p, vp, vp, vp]
+        lib.span_la_pass.restype = ctypes.c_int
+        lib.span_la_branches_from_state.argtypes = [vp, ctypes.c_int32, vp, vp, vp, Dims, i32p,
+                                                    ctypes.c_int32, i32p, vp, vp]
+        lib.span_la_branches_from_state.restype = ctypes.c_int
+        lib.span_la_check.argtypes = [vp]
+        lib.span_la_check.restype = ctypes.c_int
+        lib.span_la_status_string.argtypes = [ctypes.c_int]
+        lib.span_la_status_string.restype = ctypes.c_char_p
+        lib.span_la_last_error_detail.argtypes = []
+        lib.span_la_last_error_detail.restype = ctypes.c_char_p
+        lib.span_la_version.argtypes = []
+        lib.span_la_version.restype = ctypes.c_int32
+        lib.span_la_selftest_wait_timeout.argtypes = [ctypes.c_int32, vp]
+        lib.span_la_selftest_wait_timeout.restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _raise(lib, status: int, where: str):
+    if status != 0:
+        raise SpanLAError(status, where, lib.span_la_last_error_detail().decode())
+
+
+def _i32(a) -> np.ndarray:
+    if a is None:
+        return np.zeros(0, dtype=np.int32)
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int64).reshape(-1).astype(np.int32))
+
+
+def _iptr(a: np.ndarray):
+    if a.size == 0:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dims_of(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> Dims:
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if t.dim() != 3 or t.shape[2] != 64:
+            raise ValueError("%s must be [T, H, 64], got %s" % (name, tuple(t.shape)))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if q.shape != k.shape or q.shape != v.shape or q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k and v must share shape and dtype")
+    if q.dtype == torch.bfloat16:
+        dt = SPAN_LA_BF16
+    elif q.dtype == torch.float32:
+        dt = SPAN_LA_F32
+    else:
+        raise ValueError("dtype %s not supported (bf16 or fp32)" % q.dtype)
+    return Dims(q.shape[0], q.shape[1], q.shape[2], dt)
+
+
+def span_la_pass(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                 view_cu_seqlens: Sequence[int], branch_cu_seqlens: Optional[Sequence[int]],
+                 branch_parent: Optional[Sequence[int]],
+                 out: Optional[torch.Tensor] = None,
+                 view_state_out: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """One packed pass (see ``span_la_pass`` in ``include/spanla.h``).
+
+    Returns ``(out [T,H,64], view_state_out [V,H,64,64] fp32)``.  ``out`` is
+    allocated with ``torch.empty`` when not given: rows in no segment then
+    hold whatever the allocator returned.
+    """
+    lib = load_library()
+    dims = _dims_of(q, k, v)
+    vcu, bcu, par = _i32(view_cu_seqlens), _i32(branch_cu_seqlens), _i32(branch_parent)
+    V = max(len(vcu) - 1, 0)
+    B = max(len(bcu) - 1, 0)
+    H = q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if view_state_out is None:
+        view_state_out = torch.empty((V, H, 64, 64), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor like q")
+    if (view_state_out.dtype != torch.float32 or not view_state_out.is_contiguous()
+            or view_state_out.numel() < V * H * 4096):
+        raise ValueError("view_state_out must be contiguous fp32 [V, H, 64, 64]")
+    st = lib.span_la_pass(q.data_ptr(), k.data_ptr(), v.data_ptr(), dims,
+                          _iptr(vcu), V, _iptr(bcu), B, _iptr(par),
+                          out.data_ptr(), view_state_out.data_ptr(), _stream_handle(stream))
+    _raise(lib, st, "span_la_pass")
+    return out, view_state_out
+
+
+def span_la_branches_from_state(cached_state: torch.Tensor, q: torch.Tensor, k: torch.Tensor,
+                                v: torch.Tensor, branch_cu_seqlens: Sequence[int],
+                                branch_parent: Sequence[int],
+                                out: Optional[torch.Tensor] = None,
+                                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Branches forking from cached view states (``span_la_branches_from_state``)."""
+    lib = load_library()
+    dims = _dims_of(q, k, v)
+    bcu, par = _i32(branch_cu_seqlens), _i32(branch_parent)
+    B = max(len(bcu) - 1, 0)
+    if (cached_state.dtype != torch.float32 or not cached_state.is_contiguous()
+            or not cached_state.is_cuda or cached_state.dim() != 4
+            or tuple(cached_state.shape[1:]) != (q.shape[1], 64, 64)):
+        raise ValueError("cached_state must be contiguous fp32 CUDA [P, H, 64, 64]")
+    if out is None:
+        out = torch.empty_like(q)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor like q")
+    st = lib.span_la_branches_from_state(cached_state.data_ptr(), cached_state.shape[0],
+                                         q.data_ptr(), k.data_ptr(), v.data_ptr(), dims,
+                                         _iptr(bcu), B, _iptr(par), out.data_ptr(),
+                                         _stream_handle(stream))
+    _raise(lib, st, "span_la_branches_from_state")
+    return out
+
+
+def span_la_check(stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Synchronise the stream and raise on a CUDA error or a device wait timeout."""
+    lib = load_library()
+    _raise(lib, lib.span_la_check(_stream_handle(stream)), "span_la_check")
+
+
+def span_la_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    lib = load_library()
+    _raise(lib, lib.span_la_selftest_wait_timeout(int(limit_us), _stream_handle(stream)),
+           "span_la_selftest_wait_timeout")
+
+
+def version() -> int:
+    return int(load_library().span_la_version())

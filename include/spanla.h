@@ -1,0 +1,166 @@
+/*
+ * spanla.h -- C ABI of libspanla, the packed linear-attention pass for GB300
+ * (sm_103a).
+ *
+ * What a call computes ("Serving 0.88M TPS from Two RTXs and Mac Minis",
+ * sections "The Workload", "Kernels" and "Long Requests"): unnormalised causal
+ * linear attention, independently per head,
+ *
+ *     S_t = S_{t-1} + k_t v_t^T        o_t = S_t^T q_t      (inclusive diagonal)
+ *
+ * over a *packed pass*: one buffer of rows that holds many variable-length
+ * views and many short branches.  Each view starts from S = 0.  Each branch
+ * starts from the final state of its parent view (the state after the view's
+ * last row) and runs over its own rows only; branches never see one another
+ * (section "The Workload": branches attend to the view but not to each other).
+ * The work is done in 64-token chunks as the "Kernels" section describes
+ * (each chunk a few 64x64 matrix products; one scan of chunk states covers
+ * every view of the pass, in three launches): per-chunk local state K^T V,
+ * one segmented prefix scan over every view of the pass, and the chunk/branch
+ * output (masked Q K^T V inside a tile plus Q S_prev).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.  q, k, v and out are contiguous row-major [T][H][64] arrays in
+ *   device memory (T = dims.total_rows, H = dims.num_heads), element type
+ *   dims.dtype, base address 16-byte aligned.  States are contiguous fp32
+ *   [n][H][64][64] arrays in device memory with S[i][j] at i*64 + j (i = key
+ *   dimension, j = value dimension), 16-byte aligned.
+ * Segments.  view_cu_seqlens (num_views + 1 entries) and branch_cu_seqlens
+ *   (num_branches + 1 entries) are HOST int32 arrays of non-decreasing
+ *   absolute row offsets into the same [T] buffer: segment s covers rows
+ *   [cu[s], cu[s+1]).  Zero-length segments are allowed; a count of 0 is
+ *   allowed (the array may then be NULL).  No two non-empty segments may
+ *   overlap.  Rows in no segment are never read into a result and never
+ *   written.  branch_parent (num_branches entries, HOST int32) names the
+ *   parent of every branch.
+ * Ownership.  The caller owns every buffer.  Host arrays are read only during
+ *   the call.  The library allocates its workspace stream-ordered
+ *   (cudaMallocAsync / cudaFreeAsync on `stream`) and frees it before the
+ *   work completes on the stream.
+ * Asynchrony.  A call only enqueues work on `stream` (a cudaStream_t on the
+ *   current device; 0 = legacy default stream).  Outputs are valid once the
+ *   stream has reached the call; inputs must stay unchanged until then.
+ * Precision.  bf16 or fp32 inputs; the state and every accumulation are fp32.
+ *   fp32 operands (and the fp32 state and P tiles fed to the tensor cores) are
+ *   split into two bf16 parts whose cross products are summed.  Outputs are
+ *   rounded to the input type (round to nearest even).  Results are
+ *   deterministic run to run (no floating-point atomics).
+ * Errors.  Metadata, shape, pointer and alignment problems are detected on the
+ *   host before anything is enqueued; the call then returns an error code and
+ *   writes nothing.  Device-side waits are bounded: a wait that runs out sets
+ *   a device error word, the kernel returns without trapping, and
+ *   span_la_check() reports SPAN_LA_ERR_TIMEOUT.  span_la_last_error_detail()
+ *   describes the last failure on the calling thread.
+ * Supported.  head_dim == 64, num_heads >= 1, total_rows < 2^31,
+ *   dtype SPAN_LA_BF16 or SPAN_LA_F32, one GPU of compute capability 10.3.
+ */
+#ifndef SPANLA_H
+#define SPANLA_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPAN_LA_BF16 = 0,
+    SPAN_LA_F32 = 1
+} span_la_dtype;
+
+typedef enum {
+    SPAN_LA_OK = 0,
+    SPAN_LA_ERR_INVALID = 1,      /* bad metadata, pointer, alignment or size */
+    SPAN_LA_ERR_UNSUPPORTED = 2,  /* head_dim != 64, unknown dtype, wrong GPU */
+    SPAN_LA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed */
+    SPAN_LA_ERR_NOMEM = 4,        /* workspace allocation failed */
+    SPAN_LA_ERR_TIMEOUT = 5       /* a bounded device wait ran out */
+} span_la_status;
+
+typedef struct {
+    int64_t total_rows;  /* T: rows of q, k, v and out */
+    int32_t num_heads;   /* H */
+    int32_t head_dim;    /* must be 64 */
+    int32_t dtype;       /* span_la_dtype of q, k, v and out */
+} span_la_dims;
+
+/*
+ * span_la_pass -- one packed pass over views and branches.
+ *
+ * Section "Kernels" (one scan per pass in three launches; shared branch
+ * passes) and section "The Workload".  Computes o for every view row and every
+ * branch row and writes each view's final state to view_state_out.
+ *
+ *   q, k, v          device [T][H][64], dims.dtype
+ *   view_cu_seqlens  host int32 [num_views + 1]
+ *   branch_cu_seqlens host int32 [num_branches + 1]
+ *   branch_parent    host int32 [num_branches], each in [0, num_views)
+ *   out              device [T][H][64], dims.dtype; only segment rows written
+ *   view_state_out   device fp32 [num_views][H][64][64]; required when
+ *                    num_views > 0 (an empty view gets the zero state)
+ *   stream           stream to enqueue on
+ */
+span_la_status span_la_pass(const void *q, const void *k, const void *v,
+                            span_la_dims dims,
+                            const int32_t *view_cu_seqlens, int32_t num_views,
+                            const int32_t *branch_cu_seqlens, int32_t num_branches,
+                            const int32_t *branch_parent,
+                            void *out, float *view_state_out,
+                            cudaStream_t stream);
+
+/*
+ * span_la_branches_from_state -- branches only, each forking from a cached
+ * view state.
+ *
+ * Section "Long Requests": branches only attend to their own view, so they can
+ * be split into shards that each reuse the view's cached linear-attention
+ * state instead of recomputing the view.  Equivalent to the branch rows of
+ * span_la_pass when cached_state holds that pass's view_state_out.
+ *
+ *   cached_state     device fp32 [num_states][H][64][64]
+ *   branch_parent    host int32 [num_branches], each in [0, num_states)
+ *   out              device [T][H][64]; only branch rows written
+ *   other arguments  as for span_la_pass
+ */
+span_la_status span_la_branches_from_state(const float *cached_state, int32_t num_states,
+                                           const void *q, const void *k, const void *v,
+                                           span_la_dims dims,
+                                           const int32_t *branch_cu_seqlens,
+                                           int32_t num_branches,
+                                           const int32_t *branch_parent,
+                                           void *out, cudaStream_t stream);
+
+/*
+ * span_la_check -- synchronise `stream`, then report (and clear) the device
+ * error word of the current device.  Returns SPAN_LA_ERR_CUDA if the stream
+ * reports a CUDA error, SPAN_LA_ERR_TIMEOUT if a kernel's bounded wait ran
+ * out, SPAN_LA_OK otherwise.
+ */
+span_la_status span_la_check(cudaStream_t stream);
+
+/* Static text for a status code. */
+const char *span_la_status_string(span_la_status status);
+
+/* Text describing the last failure of a call made on this host thread. */
+const char *span_la_last_error_detail(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t span_la_version(void);
+
+/*
+ * span_la_selftest_wait_timeout -- failure-detection hook: enqueue one tiny
+ * kernel whose bounded wait is on an mbarrier that nothing ever completes,
+ * with a wait limit of `limit_us` microseconds (1 .. 1,000,000).  The kernel
+ * gives up, sets the device error word and returns; span_la_check() then
+ * reports SPAN_LA_ERR_TIMEOUT.  Used by the tests to show that a wait that
+ * runs out neither traps nor hangs.
+ */
+span_la_status span_la_selftest_wait_timeout(int32_t limit_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPANLA_H */

@@ -1,0 +1,188 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on the
+same seeded inputs, element by element.
+
+Tolerance (written here, applied per call): max|o_gpu - o_ref| / max|o_ref|
+<= 1e-3 for fp32 inputs and <= 1e-2 for bf16 inputs; the same bound holds for
+the view states against max|S_ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL, f64, rel_err, segment_rows, sub_pass, to_device
+from hybrid_linear_attention_packed_gb300 import (span_la_branches_from_state, span_la_check,
+                                                  span_la_pass, workloads)
+from oracle import oracle_branches_from_state, oracle_pass
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_gpu(w, dev, poison=True):
+    q, k, v = to_device(w, dev)
+    out = torch.full_like(q, float("nan")) if poison else torch.zeros_like(q)
+    out, state = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, out=out)
+    span_la_check()
+    return out, state
+
+
+def _oracle(w):
+    return oracle_pass(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu, w.branch_parent)
+
+
+def _check_full(w, dev):
+    out, state = _run_gpu(w, dev)
+    ref, ref_state = _oracle(w)
+    got = f64(out)
+    seg = segment_rows(w)
+    assert not np.any(np.isnan(got[seg])), "a segment row was not written"
+    assert np.all(np.isnan(got[~seg])), "a row outside every segment was written"
+    tol = TOL[w.dtype]
+    e_all = rel_err(got[seg], ref[seg])
+    vrows = np.zeros(w.T, bool)
+    vrows[w.view_cu[0]:w.view_cu[-1]] = True
+    e_view = rel_err(got[vrows & seg], ref[vrows & seg])
+    e_br = rel_err(got[~vrows & seg], ref[~vrows & seg])
+    e_state = rel_err(f64(state), ref_state)
+    print("%s: out %.2e (views %.2e, branches %.2e) state %.2e"
+          % (w.name, e_all, e_view, e_br, e_state))
+    assert e_all <= tol and e_state <= tol
+    return out, state
+
+
+def test_tiny_oracle_case(cuda_device):
+    _check_full(workloads.tiny_oracle_case(0), cuda_device)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_single_request_7400(cuda_device, seed):
+    _check_full(workloads.single_request(seed), cuda_device)
+
+
+def test_packed_four_requests(cuda_device):
+    _check_full(workloads.packed_four(0), cuda_device)
+
+
+@pytest.mark.parametrize("n_views", [1, 4])
+def test_sweep_small(cuda_device, n_views):
+    _check_full(workloads.sweep(n_views, 0), cuda_device)
+
+
+@pytest.mark.parametrize("n_views", [16, 32])
+def test_sweep_large_sampled(cuda_device, n_views):
+    """Full-size sweep passes, launched exactly as the benchmark launches them;
+    the oracle checks a sample of requests (each view with all its branches)."""
+    w = workloads.sweep(n_views, 0)
+    out, state = _run_gpu(w, cuda_device)
+    got, got_state = f64(out), f64(state)
+    seg = segment_rows(w)
+    assert not np.any(np.isnan(got[seg]))
+    assert np.all(np.isnan(got[~seg]))
+    rng = np.random.default_rng(5)
+    sample = sorted(rng.choice(w.V, size=3, replace=False).tolist())
+    idx, vcu, bcu, par = sub_pass(w, sample)
+    ref, ref_state = oracle_pass(f64(w.q[idx]), f64(w.k[idx]), f64(w.v[idx]), vcu, bcu, par)
+    e = rel_err(got[idx], ref)
+    es = rel_err(got_state[sample], ref_state)
+    print("sweep %d views, sample %s: out %.2e state %.2e" % (n_views, sample, e, es))
+    assert e <= TOL["bf16"] and es <= TOL["bf16"]
+
+
+def test_cached_long_request_shards(cuda_device):
+    """18,000-token view -> cached state -> 256 branches in 4 shards of 64."""
+    w = workloads.cached_long(0)
+    q, k, v = to_device(w, cuda_device)
+    view_out = torch.full_like(q, float("nan"))
+    _, state = span_la_pass(q, k, v, w.view_cu, None, None, out=view_out)
+    out = torch.full_like(q, float("nan"))
+    for cu in workloads.shards(w, 4):
+        span_la_branches_from_state(state, q, k, v, cu, np.zeros(len(cu) - 1, np.int32), out=out)
+    span_la_check()
+    ref, ref_state = _oracle(w)
+    e_state = rel_err(f64(state), ref_state)
+    br = np.zeros(w.T, bool)
+    br[w.branch_cu[0]:w.branch_cu[-1]] = True
+    got = f64(out)
+    assert np.all(np.isnan(got[~br]))
+    e_br = rel_err(got[br], ref[br])
+    e_view = rel_err(f64(view_out)[~br], ref[~br])
+    # the branches from the GPU's own cached state, checked against the oracle
+    # run from that same state
+    ref_from = oracle_branches_from_state(f64(state), f64(w.q), f64(w.k), f64(w.v),
+                                          w.branch_cu, w.branch_parent)
+    e_from = rel_err(got[br], ref_from[br])
+    print("cached long: state %.2e view %.2e branches %.2e (from gpu state %.2e)"
+          % (e_state, e_view, e_br, e_from))
+    assert max(e_state, e_br, e_view, e_from) <= TOL["bf16"]
+    # four shards equal one 256-branch call bit for bit
+    out1 = torch.full_like(q, float("nan"))
+    span_la_branches_from_state(state, q, k, v, w.branch_cu, w.branch_parent, out=out1)
+    span_la_check()
+    assert torch.equal(out1[br], out[br])
+
+
+EDGE = [0, 1, 63, 64, 65, 127, 128, 129, 255, 256, 257]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_edge_lengths(cuda_device, dtype):
+    views = EDGE
+    branches = EDGE + [300, 2, 3]
+    parent = [i % len(views) for i in range(len(branches))]
+    w = workloads.make_pass(views, branches, parent, H=3, dtype=dtype, seed=21,
+                            lead_rows=5, mid_rows=70, tail_rows=130)
+    _check_full(w, cuda_device)
+
+
+def test_gap_rows_with_nan_inputs_do_not_leak(cuda_device):
+    """Rows outside every segment hold NaN in q, k and v; no result may see them
+    and they are never written."""
+    w = workloads.make_pass([100, 64, 1], [20, 44, 7, 200], [0, 0, 1, 2], H=2, dtype="bf16",
+                            seed=22, lead_rows=3, mid_rows=9, tail_rows=64)
+    seg = segment_rows(w)
+    for t in (w.q, w.k, w.v):
+        t[torch.from_numpy(~seg)] = float("nan")
+    _check_full(w, cuda_device)
+
+
+def test_branches_block_before_views(cuda_device):
+    """Segments may sit anywhere in the buffer: branches first, then views."""
+    base = workloads.make_pass([150, 90], [30, 40, 12], [1, 0, 1], H=2, dtype="bf16", seed=23)
+    nb = int(base.branch_lens.sum())
+    nv = int(base.view_lens.sum())
+    w = base
+    perm = np.concatenate([np.arange(nv, nv + nb), np.arange(0, nv)])
+    w.q, w.k, w.v = w.q[perm].contiguous(), w.k[perm].contiguous(), w.v[perm].contiguous()
+    w.branch_cu = (w.branch_cu - nv).astype(np.int32)
+    w.view_cu = (w.view_cu + nb).astype(np.int32)
+    _check_full(w, cuda_device)
+
+
+def test_one_hot_counts_are_exact(cuda_device):
+    """One-hot k, v, q: every output is an integer count < 256, exact in bf16."""
+    w = workloads.one_hot_pass([300, 129], [40, 100, 5], [0, 1, 0], H=2, D=64, dtype="bf16",
+                               seed=24)
+    out, state = _run_gpu(w, cuda_device)
+    ref, ref_state = _oracle(w)
+    seg = segment_rows(w)
+    assert np.array_equal(f64(out)[seg], ref[seg])
+    assert np.array_equal(f64(state), ref_state)
+
+
+def test_empty_and_degenerate_passes(cuda_device):
+    dev = cuda_device
+    q = torch.zeros((10, 2, 64), dtype=torch.bfloat16, device=dev)
+    # no segments at all
+    out = torch.full_like(q, 7.0)
+    span_la_pass(q, q, q, [0], None, None, out=out)
+    span_la_check()
+    assert torch.all(out == 7.0)
+    # empty views only, with branches of an empty view (start from zero state)
+    w = workloads.make_pass([0, 0], [5, 0, 3], [1, 0, 0], H=2, dtype="bf16", seed=25,
+                            lead_rows=2)
+    out, state = _check_full(w, dev)
+    assert torch.all(state == 0)
+    # zero rows in total
+    z = torch.zeros((0, 2, 64), dtype=torch.bfloat16, device=dev)
+    out, state = span_la_pass(z, z, z, [0, 0], [0, 0], [0])
+    span_la_check()
+    assert state.shape == (1, 2, 64, 64) and torch.all(state == 0)

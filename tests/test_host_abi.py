@@ -1,0 +1,108 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+symbol ``include/spanla.h`` declares; host-side validation rejects bad
+metadata before any CUDA call; the binding fails loudly when the library is
+missing.  No compute call runs here (there is no GPU on this side)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from hybrid_linear_attention_packed_gb300 import build as spanla_build
+from hybrid_linear_attention_packed_gb300 import spanla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = spanla_build.build()
+    return spanla.load_library(path)
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "spanla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(span_la_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_symbols()
+    assert set(declared) >= {"span_la_pass", "span_la_branches_from_state", "span_la_check"}
+    for name in declared:
+        assert hasattr(lib, name), "missing export %s" % name
+    assert set(declared) == set(spanla.EXPORTED)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.span_la_version() == 100
+    for code in range(6):
+        assert lib.span_la_status_string(code)
+
+
+def _dims(T=100, H=2, D=64, dtype=0):
+    return spanla.Dims(T, H, D, dtype)
+
+
+def _arr(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+FAKE = 1 << 20   # a 16-byte-aligned non-NULL address; never dereferenced on the host
+
+
+def _pass(lib, vcu, bcu, par, dims=None, q=FAKE, out=FAKE, state=FAKE):
+    dims = dims or _dims()
+    (va, vp), (ba, bp), (pa, pp) = _arr(vcu), _arr(bcu), _arr(par)
+    V, B = max(len(va) - 1, 0), max(len(ba) - 1, 0)
+    st = lib.span_la_pass(q, q, q, dims, vp if V else None, V, bp if B else None, B,
+                          pp if B else None, out, state, None)
+    return st, lib.span_la_last_error_detail().decode()
+
+
+@pytest.mark.parametrize("vcu,bcu,par,what", [
+    ([0, 50, 40], [], [], "non-decreasing"),
+    ([0, 101], [], [], "non-decreasing"),
+    ([-1, 10], [], [], "non-decreasing"),
+    ([0, 50], [40, 60], [0], "overlap"),
+    ([0, 50], [50, 60], [1], "branch_parent"),
+    ([0, 50], [50, 60], [-1], "branch_parent"),
+])
+def test_bad_metadata_is_rejected_before_any_launch(lib, vcu, bcu, par, what):
+    st, detail = _pass(lib, vcu, bcu, par)
+    assert st == 1 and what in detail
+
+
+def test_unsupported_shapes_and_pointers(lib):
+    st, detail = _pass(lib, [0, 10], [], [], dims=_dims(D=128))
+    assert st == 2 and "head_dim" in detail
+    st, detail = _pass(lib, [0, 10], [], [], dims=_dims(dtype=7))
+    assert st == 2
+    st, detail = _pass(lib, [0, 10], [], [], dims=_dims(H=0))
+    assert st == 1
+    st, detail = _pass(lib, [0, 10], [], [], q=FAKE + 8)
+    assert st == 1 and "aligned" in detail
+    st, detail = _pass(lib, [0, 10], [], [], state=0)
+    assert st == 1 and "view_state_out" in detail
+    st, detail = _pass(lib, [0, 10], [], [], q=0)
+    assert st == 1
+
+
+def test_from_state_validation(lib):
+    (ba, bp), (pa, pp) = _arr([0, 10, 20]), _arr([0, 1])
+    st = lib.span_la_branches_from_state(FAKE, 1, FAKE, FAKE, FAKE, _dims(), bp, 2, pp, FAKE, None)
+    assert st == 1 and "branch_parent" in lib.span_la_last_error_detail().decode()
+    st = lib.span_la_branches_from_state(0, 2, FAKE, FAKE, FAKE, _dims(), bp, 2, pp, FAKE, None)
+    assert st == 1 and "cached_state" in lib.span_la_last_error_detail().decode()
+
+
+def test_empty_call_is_a_no_op(lib):
+    st, _ = _pass(lib, [0], [], [], q=0, out=0, state=0)
+    assert st == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not found"):
+        spanla.load_library(str(tmp_path / "nope.so"))
