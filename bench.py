@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Benchmark of the packed linear-attention pass (one layer) on one GB300.
+
+A step is one ``span_la_pass`` call over the whole pass (chunk state, segmented
+scan, tile output with the branch fork) on inputs already resident in HBM.
+The default workload is the single request of the pages' 7,400-token figure
+("Serving 0.88M TPS from Two RTXs and Mac Minis", section "Kernels"): 16 heads,
+d = 64, bf16 inputs with fp32 state, one 7,400-token view plus 8 branches of
+U[32, 96] rows, synthetic and seeded.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle on the host cores instead (the only other place this script runs it).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "packed-pass tokens/s per layer"
+UNIT = "tokens/s"
+STATE_BYTES = 64 * 64 * 4
+# ms per layer the page reports for one scan per pass at 7,400 tokens (section
+# "Kernels"), measured on an older RTX GPU: context for vs_baseline only.
+PAGE_MS_PER_LAYER_7400 = 1.50
+PAGE_TOKENS_7400 = 7400
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="single",
+                    help="single | packed4 | cached_long | sweepN (N views) | tiny")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running (SM clock, throttle reasons)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append(parts)
+        return rows
+
+
+def summarize_clocks(rows, t0: float, t1: float):
+    """Median SM clock and the throttle reasons seen between wall times t0 and t1."""
+    import datetime
+    sel = []
+    for r in rows:
+        try:
+            ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            ts = None
+        if ts is None or (t0 - 0.25) <= ts <= (t1 + 0.25):
+            sel.append(r)
+    if not sel:
+        sel = rows[-3:]
+    if not sel:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                "samples": 0}
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = set()
+    for r in sel:
+        for n, val in zip(names, r[6:10]):
+            if val.strip().lower() in ("active", "0x1", "1"):
+                reasons.add(n)
+
+    def num(x):
+        try:
+            return float(x)
+        except ValueError:
+            return None
+    sm = [num(r[2]) for r in sel if num(r[2]) is not None]
+    mx = [num(r[3]) for r in sel if num(r[3]) is not None]
+    pw = [num(r[4]) for r in sel if num(r[4]) is not None]
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "power_w_max": max(pw) if pw else None,
+            "reasons": sorted(reasons), "samples": len(sel)}
+
+
+def gpu_id_for_smi(torch, dev_index: int) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[dev_index]
+    return str(dev_index)
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+def algorithmic_bytes(plan: dict, H: int, esize: int, T: int) -> dict:
+    """Bytes each kernel must move at least once per launch, from the library's
+    own plan: operand rows read, states written/read, outputs written."""
+    row = 64 * esize
+    state_k = plan["state_rows"] * H * 2 * row + plan["state_slots"] * H * STATE_BYTES
+    out_k = plan["tile_rows"] * H * 4 * row + plan["start_state_reads"] * H * STATE_BYTES
+    return {
+        "chunk_state": state_k, "span_state": state_k,
+        "segmented_scan": (2 * plan["state_slots"] + plan["final_states"]) * H * STATE_BYTES,
+        "tile_output": out_k, "span_output": out_k,
+        "split_f32": T * H * 64 * (3 * 4 + 6 * 2),
+    }
+
+
+def io_bytes(w, esize: int) -> int:
+    """Bytes of the call's inputs and outputs alone: q, k, v read and o written
+    once per segment row, view states written once."""
+    return w.rows * w.H * 64 * esize * 4 + w.V * w.H * STATE_BYTES
+
+
+def kernel_sha(name: str) -> str:
+    files = {"tile_output": "k_tile_output.cu", "chunk_state": "k_chunk_state.cu",
+             "segmented_scan": "k_scan.cu", "split_f32": "k_misc.cu",
+             "span_state": "k_span_state.cu", "span_output": "k_span_output.cu"}
+    p = os.path.join(ROOT, "hybrid_linear_attention_packed_gb300", "csrc", files[name])
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when there is none or the kernel source changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(p):
+        return None
+    pat = re.compile(r"^\|\s*%s\s*\|\s*%s\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9.eE+]+)\s*\|"
+                     % (re.escape(kernel), re.escape(workload)))
+    with open(p) as f:
+        for line in f:
+            m = pat.match(line.strip())
+            if m and m.group(1) == kernel_sha(kernel):
+                return float(m.group(2))
+    return None
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_time(w, budget_s: float = 8.0, max_reps: int = 50):
+    """Time the float64 oracle on the whole workload, repeated within ~budget_s."""
+    from oracle import oracle_max_threads, oracle_pass
+    q, k, v = (t.double().numpy() for t in (w.q, w.k, w.v))
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < max_reps and (time.perf_counter() - t_all) < budget_s:
+        t0 = time.perf_counter()
+        oracle_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+        times.append(time.perf_counter() - t0)
+    return statistics.median(times), len(times), oracle_max_threads()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from hybrid_linear_attention_packed_gb300 import workloads
+    from oracle import oracle_max_threads, oracle_pass
+    w = workloads.by_name(args.workload, args.seed)
+    q, k, v = (t.double().numpy() for t in (w.q, w.k, w.v))
+    for _ in range(max(0, min(args.warmup, 3))):
+        oracle_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+    # bounded: at most ~60 s of timed oracle work whatever --steps asks for
+    times = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all > 60.0:
+            break
+    ms = statistics.mean(times) * 1e3
+    value = w.rows / (ms / 1e3)
+    cores = oracle_max_threads()
+    sample = ("the whole workload (%d rows x %d heads) per step, %d timed steps"
+              % (w.rows, w.H, len(times)))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, args.workload),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w, name: str) -> dict:
+    return {"workload": w.name, "key": name, "heads": w.H, "head_dim": w.D, "views": w.V,
+            "branches": w.B, "rows": w.rows, "view_rows": int(w.view_lens.sum()),
+            "branch_rows": int(w.branch_lens.sum()),
+            "l2": "flushed before every timed step (512 MiB write)"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    rank, world, local = dist_env()
+    import numpy as np
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    from hybrid_linear_attention_packed_gb300 import build as libbuild
+    if rank == 0:
+        libbuild.build()
+    if pg:
+        pg.barrier()
+    from hybrid_linear_attention_packed_gb300 import spanla, workloads
+
+    # Weak scaling: every rank runs its own pass (independent requests).
+    w = workloads.by_name(args.workload, args.seed + rank)
+    esize = 2 if w.dtype == "bf16" else 4
+    q, k, v = (t.to(dev).contiguous() for t in (w.q, w.k, w.v))
+    out = torch.zeros_like(q)
+    state = torch.zeros((w.V, w.H, 64, 64), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        spanla.span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, out=out,
+                            view_state_out=state)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    spanla.span_la_check()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_id_for_smi(torch, local))
+    time.sleep(0.5)
+    spanla.profile_reset()        # launch counters only; no per-kernel events here
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if pg:
+        pg.barrier()
+    launches = spanla.profile_read()
+    spanla.span_la_check()
+    clock_rows = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(step_ms)
+    ms_max = ms
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_max = float(t.item())
+    rows_total = w.rows * world
+    value = rows_total / (ms_max / 1e3)
+
+    # Per-kernel durations: the same steps again with CUDA events recorded
+    # around every launch on the call's stream (the events keep consecutive
+    # kernels from overlapping, so these add up to more than a step).
+    KP = min(K, 500)
+    spanla.profile_reset()
+    spanla.profile_enable(True)
+    for i in range(KP):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    spanla.profile_enable(False)
+    prof = spanla.profile_read()
+    spanla.span_la_check()
+
+    # Roofline of the dominant kernel, from live event timings.
+    plan = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H, w.dtype)
+    alg = algorithmic_bytes(plan, w.H, esize, w.T)
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        with open(pk) as f:
+            peaks = json.load(f)
+    hbm_peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if hbm_peak else "fallback"
+    hbm_peak = hbm_peak or 6800.0
+    kernels = {}
+    for name, p in prof.items():
+        if p["timed"]:
+            avg_ms = p["ms"] / p["timed"]
+            kernels[name] = {"avg_us": avg_ms * 1e3, "launches": p["launches"],
+                             "share": None, "alg_bytes": alg.get(name, 0),
+                             "gbs": alg.get(name, 0) / (avg_ms / 1e3) / 1e9 if avg_ms > 0 else None}
+    tot = sum(kk["avg_us"] for kk in kernels.values()) or 1.0
+    profiled_step_us = tot
+    for kk in kernels.values():
+        kk["share"] = kk["avg_us"] / tot
+    dom = max(kernels, key=lambda n: kernels[n]["avg_us"])
+    dk = kernels[dom]
+    traffic = recorded_traffic(dom, args.workload)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": dk["gbs"], "peak": hbm_peak,
+                "unit": "GB/s", "frac": dk["gbs"] / hbm_peak, "traffic": traffic,
+                "peak_source": peak_src,
+                "alg_bytes_per_launch": dk["alg_bytes"]}
+    step_bytes = sum(alg[n] for n in kernels)
+    pass_roofline = {"method_bytes": step_bytes,
+                     "method_frac": step_bytes / (ms / 1e3) / 1e9 / hbm_peak,
+                     "io_bytes": io_bytes(w, esize),
+                     "io_frac": io_bytes(w, esize) / (ms / 1e3) / 1e9 / hbm_peak}
+
+    # End to end through the public API with host buffers: pinned H2D of
+    # q, k, v, the call, D2H of out and the view states, every step.
+    hq, hk, hv = (t.pin_memory() for t in (w.q, w.k, w.v))
+    hout = torch.empty_like(hq).pin_memory()
+    hstate = torch.empty((w.V, w.H, 64, 64), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        hstate.copy_(state, non_blocking=True)
+
+    for _ in range(3):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    KE = max(1, args.e2e_steps)
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    for i in range(KE):
+        flush.zero_()
+        es[i].record(stream)
+        e2e_step()
+        ee[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(es, ee))
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = 3 * w.T * w.H * 64 * esize
+    d2h = w.T * w.H * 64 * esize + w.V * w.H * STATE_BYTES
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        med, reps, cores = oracle_time(w)
+        cpu = {"value": w.rows / med, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "the whole workload (%d rows x %d heads), median of %d passes"
+                         % (w.rows, w.H, reps)}
+
+    vs = None
+    if args.workload == "single":
+        vs = value / (PAGE_TOKENS_7400 / (PAGE_MS_PER_LAYER_7400 / 1e3))
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": vs, "dtype": w.dtype, "data": "synthetic",
+                "config": dict(workload_config(w, args.workload), parallelism="dp%d" % world),
+                "roofline": roofline, "pass_roofline": pass_roofline,
+                "kernels": kernels, "plan": plan,
+                "cpu_baseline": cpu,
+                "e2e": {"value": rows_total / (e2e_ms / 1e3), "unit": UNIT,
+                        "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h},
+                "gpu_launches": int(sum(p["launches"] for p in launches.values())),
+                "clocks": summarize_clocks(clock_rows, t0, t1),
+                "step_ms_p50": statistics.median(step_ms),
+                "profiled_kernel_us_sum": profiled_step_us,
+                "step_ms_min": min(step_ms)}
+        print(json.dumps(line))
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -14,6 +14,7 @@
 // and loading eight chunks ahead so the loads stay in flight while the
 // stores drain.
 #include "spanla_internal.h"
+#include "tc_ptx.cuh"
 
 namespace spanla {
 namespace {
@@ -29,6 +30,7 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) {
 __global__ void __launch_bounds__(kThreads)
 segmented_scan_kernel(const ScanDesc* __restrict__ scan, int H, float* __restrict__ ws,
                       float* __restrict__ final_out) {
+  griddep_wait();   // chunk states from the previous kernel
   const ScanDesc sd = scan[blockIdx.x];
   const int h = blockIdx.y;
   const int off = (blockIdx.z * kThreads + threadIdx.x) * 4;
@@ -49,6 +51,7 @@ segmented_scan_kernel(const ScanDesc* __restrict__ scan, int H, float* __restric
       }
     }
   }
+  griddep_launch_dependents();
   if (sd.final_idx >= 0) {
     float* f = final_out + (static_cast<int64_t>(sd.final_idx) * H + h) * kStateFloats + off;
     *reinterpret_cast<float4*>(f) = run;
@@ -58,11 +61,18 @@ segmented_scan_kernel(const ScanDesc* __restrict__ scan, int H, float* __restric
 }  // namespace
 
 cudaError_t launch_scan(const ScanDesc* scan, int n_scan, int H, float* ws, float* final_out,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool pdl) {
   if (n_scan <= 0) return cudaSuccess;
-  const dim3 grid(n_scan, H, kSlices);
-  segmented_scan_kernel<<<grid, kThreads, 0, stream>>>(scan, H, ws, final_out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_scan, H, kSlices);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, segmented_scan_kernel, scan, H, ws, final_out);
 }
 
 }  // namespace spanla

@@ -7,10 +7,12 @@
 // over descriptor tables built here from the host metadata, so that each step
 // is one launch for the whole pass however many views and branches it holds.
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -46,6 +48,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;
   bool supported = false;
+  int num_sms = 1;
   unsigned* err = nullptr;   // device error word
 };
 
@@ -71,6 +74,8 @@ span_la_status device_state(DeviceState** out) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     d.supported = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || d.num_sms < 1)
+      d.num_sms = 1;
     if (!d.supported) {
       d.ready = true;
       return fail(SPAN_LA_ERR_UNSUPPORTED,
@@ -100,6 +105,78 @@ span_la_status device_state(DeviceState** out) {
   if (!d.supported) return fail(SPAN_LA_ERR_UNSUPPORTED, "device %d is not sm_103", dev);
   *out = &d;
   return SPAN_LA_OK;
+}
+
+// ------------------------------------------------------------------ profiling
+constexpr int kKernelSplit = 0, kKernelChunk = 1, kKernelScan = 2, kKernelTile = 3,
+              kKernelSpanState = 4, kKernelSpanOutput = 5;
+const char* const kKernelNames[SPAN_LA_NUM_KERNELS] = {"split_f32", "chunk_state", "segmented_scan",
+                                                       "tile_output", "span_state", "span_output"};
+
+std::atomic<int64_t> g_launches[SPAN_LA_NUM_KERNELS];
+std::atomic<bool> g_profiling{false};
+
+struct EventRecord {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+
+std::mutex g_prof_mu;
+std::vector<EventRecord> g_pending;
+std::vector<cudaEvent_t> g_spare_events;
+double g_ms[SPAN_LA_NUM_KERNELS];
+int64_t g_timed[SPAN_LA_NUM_KERNELS];
+
+cudaEvent_t take_event() {
+  if (!g_spare_events.empty()) {
+    cudaEvent_t e = g_spare_events.back();
+    g_spare_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Launch through `fn`, counting it and (when profiling) timing it with events.
+template <typename Fn>
+cudaError_t counted_launch(int kernel, cudaStream_t stream, Fn&& fn) {
+  EventRecord rec{kernel, nullptr, nullptr};
+  const bool timing = g_profiling.load(std::memory_order_relaxed);
+  if (timing) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    rec.start = take_event();
+    rec.stop = take_event();
+  }
+  if (rec.start) cudaEventRecord(rec.start, stream);
+  cudaError_t e = fn();
+  if (e == cudaSuccess) g_launches[kernel].fetch_add(1, std::memory_order_relaxed);
+  if (rec.start && rec.stop) {
+    cudaEventRecord(rec.stop, stream);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_pending.push_back(rec);
+  }
+  return e;
+}
+
+// Fold every pending event pair into the totals (caller holds g_prof_mu).
+cudaError_t drain_events() {
+  cudaError_t first = cudaSuccess;
+  for (const EventRecord& r : g_pending) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e == cudaSuccess) {
+      g_ms[r.kernel] += ms;
+      g_timed[r.kernel] += 1;
+    } else if (first == cudaSuccess) {
+      first = e;
+    }
+    g_spare_events.push_back(r.start);
+    g_spare_events.push_back(r.stop);
+  }
+  g_pending.clear();
+  return first;
 }
 
 // ------------------------------------------------------------------ validation
@@ -156,98 +233,212 @@ span_la_status check_parents(const int32_t* parent, int32_t B, int32_t n_parents
 }
 
 // ------------------------------------------------------------------ descriptor build
+// Two plans share one builder.
+//  * span mode (bf16 inputs): every view and every branch longer than one
+//    tile is cut into spans of up to G 128-row tiles.  span_state sums K^T V
+//    per span, the scan turns span states into exclusive prefixes, and
+//    span_output walks each span's tiles carrying the state.  Short branches
+//    are packed (adjacent, contiguous, same parent) into single-tile items.
+//  * chunk mode (fp32 inputs, split in bf16 parts): one state per 64-row
+//    chunk (chunk_state), the scan over chunks, and one CTA per 128-row tile
+//    (tile_output) starting from its first chunk's prefix.
 struct Plan {
-  std::vector<ChunkDesc> chunks;
-  std::vector<ScanDesc> scan;
-  std::vector<TileDesc> tiles;
+  bool span_mode = true;
+  int G = 1;   // tiles per span (span mode)
+  std::vector<ChunkDesc> chunks;     // chunk mode: 64-row chunks
+  std::vector<SpanDesc> spans;       // span mode
+  std::vector<ScanDesc> scan;        // over chunk or span state slots
+  std::vector<TileDesc> tiles;       // chunk mode: self-contained tiles
+  std::vector<ItemDesc> items;       // span mode
+  std::vector<OutTileDesc> otiles;   // span mode
   std::vector<uint8_t> bounds;
 
-  // Chunk a segment for the scan; returns its first state slot.
-  int add_chunks(int64_t start, int64_t len, int final_idx) {
-    const int chunk0 = static_cast<int>(chunks.size());
-    const int n = static_cast<int>((len + kChunk - 1) / kChunk);
-    for (int c = 0; c < n; ++c) {
-      const int64_t r = start + static_cast<int64_t>(c) * kChunk;
-      chunks.push_back({static_cast<int32_t>(r), static_cast<int32_t>(std::min<int64_t>(kChunk, start + len - r))});
-    }
-    scan.push_back({chunk0, n, final_idx, 0});
-    return chunk0;
+  int state_slots() const { return static_cast<int>(span_mode ? spans.size() : chunks.size()); }
+  size_t n_out_tiles() const { return span_mode ? otiles.size() : tiles.size(); }
+
+  void push_bound(int32_t& bound0, int32_t& nbound) {
+    bound0 = static_cast<int32_t>(bounds.size());
+    nbound = 1;
+    bounds.push_back(0);
   }
 
-  // One segment cut into 128-row tiles; tile j starts from stateA[a] plus
-  // the prefix slot of its first chunk (none for j = 0).
-  void add_segment_tiles(int64_t start, int64_t len, int stateA, int chunk0) {
-    for (int64_t r = 0; r < len; r += kTileRows) {
-      const int j = static_cast<int>(r / kTileRows);
-      TileDesc t{};
-      t.row0 = static_cast<int32_t>(start + r);
-      t.nrows = static_cast<int32_t>(std::min<int64_t>(kTileRows, len - r));
-      t.stateA = stateA;
-      t.stateB = j == 0 ? -1 : chunk0 + 2 * j;
-      t.bound0 = static_cast<int32_t>(bounds.size());
-      t.nbound = 1;
-      bounds.push_back(0);
-      tiles.push_back(t);
+  // A segment (view: final_idx >= 0; long branch: stateA = parent).
+  void add_segment(int64_t start, int64_t len, int final_idx, int stateA) {
+    if (span_mode) {
+      const int64_t span_rows = static_cast<int64_t>(G) * kTileRows;
+      const int span0 = static_cast<int>(spans.size());
+      const int n_sp = static_cast<int>((len + span_rows - 1) / span_rows);
+      for (int sp = 0; sp < n_sp; ++sp) {
+        const int64_t r0 = start + sp * span_rows;
+        const int64_t r1 = std::min<int64_t>(start + len, r0 + span_rows);
+        spans.push_back({static_cast<int32_t>(r0), static_cast<int32_t>(r1 - r0)});
+        ItemDesc it{};
+        it.tile0 = static_cast<int32_t>(otiles.size());
+        it.ntiles = static_cast<int32_t>((r1 - r0 + kTileRows - 1) / kTileRows);
+        it.stateA = stateA;
+        it.stateB = sp == 0 ? -1 : span0 + sp;
+        items.push_back(it);
+        for (int64_t r = r0; r < r1; r += kTileRows) {
+          OutTileDesc t{};
+          t.row0 = static_cast<int32_t>(r);
+          t.nrows = static_cast<int32_t>(std::min<int64_t>(kTileRows, r1 - r));
+          push_bound(t.bound0, t.nbound);
+          otiles.push_back(t);
+        }
+      }
+      scan.push_back({span0, n_sp, final_idx, 0});
+    } else {
+      const int chunk0 = static_cast<int>(chunks.size());
+      const int n = static_cast<int>((len + kChunk - 1) / kChunk);
+      for (int c = 0; c < n; ++c) {
+        const int64_t r = start + static_cast<int64_t>(c) * kChunk;
+        chunks.push_back({static_cast<int32_t>(r), static_cast<int32_t>(std::min<int64_t>(kChunk, start + len - r))});
+      }
+      scan.push_back({chunk0, n, final_idx, 0});
+      for (int64_t r = 0; r < len; r += kTileRows) {
+        const int j = static_cast<int>(r / kTileRows);
+        TileDesc t{};
+        t.row0 = static_cast<int32_t>(start + r);
+        t.nrows = static_cast<int32_t>(std::min<int64_t>(kTileRows, len - r));
+        t.stateA = stateA;
+        t.stateB = j == 0 ? -1 : chunk0 + 2 * j;
+        push_bound(t.bound0, t.nbound);
+        tiles.push_back(t);
+      }
     }
   }
 
   // Branches: short ones (<= 128 rows) are packed greedily with adjacent,
-  // contiguous branches of the same parent; longer ones are chunked and
-  // scanned like views and start every tile from parent + prefix.
+  // contiguous branches of the same parent into one tile; longer ones are
+  // handled like views, starting from the parent's state.
   void add_branches(const int32_t* cu, int32_t B, const int32_t* parent) {
-    int open = -1;   // index of the short-branch tile being filled
+    int open = -1;   // short-branch tile being filled
     for (int32_t b = 0; b < B; ++b) {
       const int64_t start = cu[b], len = cu[b + 1] - cu[b];
       if (len == 0) continue;
       if (len > kTileRows) {
         open = -1;
-        const int chunk0 = add_chunks(start, len, -1);
-        add_segment_tiles(start, len, parent[b], chunk0);
+        add_segment(start, len, -1, parent[b]);
         continue;
       }
       if (open >= 0) {
-        TileDesc& t = tiles[open];
-        if (t.stateA == parent[b] && t.row0 + t.nrows == start && t.nrows + len <= kTileRows) {
-          bounds.push_back(static_cast<uint8_t>(t.nrows));
-          t.nbound += 1;
-          t.nrows += static_cast<int32_t>(len);
+        int32_t& row0 = span_mode ? otiles[open].row0 : tiles[open].row0;
+        int32_t& nrows = span_mode ? otiles[open].nrows : tiles[open].nrows;
+        int32_t& nbound = span_mode ? otiles[open].nbound : tiles[open].nbound;
+        const int32_t par = span_mode ? items.back().stateA : tiles[open].stateA;
+        if (par == parent[b] && row0 + nrows == start && nrows + len <= kTileRows) {
+          bounds.push_back(static_cast<uint8_t>(nrows));
+          nbound += 1;
+          nrows += static_cast<int32_t>(len);
           continue;
         }
       }
-      TileDesc t{};
-      t.row0 = static_cast<int32_t>(start);
-      t.nrows = static_cast<int32_t>(len);
-      t.stateA = parent[b];
-      t.stateB = -1;
-      t.bound0 = static_cast<int32_t>(bounds.size());
-      t.nbound = 1;
-      bounds.push_back(0);
-      open = static_cast<int>(tiles.size());
-      tiles.push_back(t);
+      if (span_mode) {
+        ItemDesc it{static_cast<int32_t>(otiles.size()), 1, parent[b], -1};
+        items.push_back(it);
+        OutTileDesc t{};
+        t.row0 = static_cast<int32_t>(start);
+        t.nrows = static_cast<int32_t>(len);
+        push_bound(t.bound0, t.nbound);
+        open = static_cast<int>(otiles.size());
+        otiles.push_back(t);
+      } else {
+        TileDesc t{};
+        t.row0 = static_cast<int32_t>(start);
+        t.nrows = static_cast<int32_t>(len);
+        t.stateA = parent[b];
+        t.stateB = -1;
+        push_bound(t.bound0, t.nbound);
+        open = static_cast<int>(tiles.size());
+        tiles.push_back(t);
+      }
     }
   }
 };
 
+// Span length G: enough (item, head) work for the GPU, long spans otherwise
+// (fewer states through the scan).  Depends on the metadata and H only.
+int choose_span_tiles(const int32_t* view_cu, int32_t V, const int32_t* branch_cu, int32_t B, int H) {
+  int64_t tiles = 0;
+  for (int32_t s = 0; s < V; ++s) tiles += (view_cu[s + 1] - view_cu[s] + kTileRows - 1) / kTileRows;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t len = branch_cu[b + 1] - branch_cu[b];
+    if (len > kTileRows) tiles += (len + kTileRows - 1) / kTileRows;
+  }
+  const int64_t g = (tiles * H + kTargetItems - 1) / kTargetItems;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxSpanTiles, g)));
+}
+
+Plan make_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu, int32_t B,
+               const int32_t* parent, int H, bool span_mode) {
+  Plan plan;
+  plan.span_mode = span_mode;
+  plan.G = span_mode ? choose_span_tiles(view_cu, V, branch_cu, B, H) : 1;
+  for (int32_t s = 0; s < V; ++s)
+    plan.add_segment(view_cu[s], view_cu[s + 1] - view_cu[s], s, -1);
+  if (B > 0) plan.add_branches(branch_cu, B, parent);
+  return plan;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-struct Workspace {
-  size_t off_tiles = 0, off_chunks = 0, off_scan = 0, off_bounds = 0, desc_bytes = 0;
-  size_t off_states = 0, off_parts = 0, total = 0;
-};
+// Span mode: deal the (item, head) work units to `grid` persistent CTAs,
+// longest first onto the least-loaded CTA, and list each CTA's tiles in
+// order.  Returns the grid size actually used.
+int build_schedule(const Plan& plan, int H, int max_ctas, std::vector<WorkTile>* work,
+                   std::vector<int32_t>* cta_begin) {
+  const int64_t n_units = static_cast<int64_t>(plan.items.size()) * H;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(n_units, max_ctas)));
+  std::vector<int64_t> order(n_units);
+  for (int64_t u = 0; u < n_units; ++u) order[u] = u;
+  std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
+    return plan.items[a / H].ntiles > plan.items[b / H].ntiles;
+  });
+  using Slot = std::pair<int64_t, int>;   // (tiles assigned, cta)
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < grid; ++c) heap.push({0, c});
+  std::vector<std::vector<int64_t>> per_cta(grid);
+  for (int64_t u : order) {
+    Slot sl = heap.top();
+    heap.pop();
+    per_cta[sl.second].push_back(u);
+    sl.first += plan.items[u / H].ntiles;
+    heap.push(sl);
+  }
+  work->clear();
+  cta_begin->assign(grid + 1, 0);
+  for (int c = 0; c < grid; ++c) {
+    (*cta_begin)[c] = static_cast<int32_t>(work->size());
+    for (int64_t u : per_cta[c]) {
+      const ItemDesc& it = plan.items[u / H];
+      const int head = static_cast<int>(u % H);
+      for (int j = 0; j < it.ntiles; ++j) {
+        const OutTileDesc& t = plan.otiles[it.tile0 + j];
+        WorkTile w{};
+        w.row0 = t.row0;
+        w.nrows = t.nrows;
+        w.head = head;
+        w.flags = (j == 0 ? kTileFirst : 0) | (j + 1 == it.ntiles ? kTileLast : 0) |
+                  ((it.stateA >= 0 || it.stateB >= 0) ? kTileHasInit : 0);
+        w.stateA = it.stateA;
+        w.stateB = it.stateB;
+        w.bound0 = t.bound0;
+        w.nbound = t.nbound;
+        for (int q = 0; q < kInlineBounds && q < t.nbound; ++q) w.inl[q] = plan.bounds[t.bound0 + q];
+        work->push_back(w);
+      }
+    }
+  }
+  (*cta_begin)[grid] = static_cast<int32_t>(work->size());
+  return grid;
+}
 
-Workspace layout(const Plan& p, int H, int64_t T, bool split) {
-  Workspace w;
-  size_t o = 0;
-  w.off_tiles = o;  o = align256(o + p.tiles.size() * sizeof(TileDesc));
-  w.off_chunks = o; o = align256(o + p.chunks.size() * sizeof(ChunkDesc));
-  w.off_scan = o;   o = align256(o + p.scan.size() * sizeof(ScanDesc));
-  w.off_bounds = o; o = align256(o + p.bounds.size());
-  w.desc_bytes = o;
-  w.off_states = o; o = align256(o + p.chunks.size() * static_cast<size_t>(H) * kStateFloats * sizeof(float));
-  w.off_parts = o;
-  if (split) o = align256(o + 6 * static_cast<size_t>(T) * H * kHeadDim * 2);
-  w.total = o;
-  return w;
+template <typename T>
+size_t put(std::vector<uint8_t>& host, const std::vector<T>& v) {
+  const size_t off = host.size();
+  host.resize(align256(off + v.size() * sizeof(T)), 0);
+  if (!v.empty()) std::memcpy(host.data() + off, v.data(), v.size() * sizeof(T));
+  return off;
 }
 
 // 3-D view (d, token, head) of a [T][H][64] bf16 array; box = {64, rows, heads}.
@@ -274,36 +465,55 @@ span_la_status run_plan(const Plan& plan, const void* q, const void* k, const vo
   const int H = dims.num_heads;
   const int64_t T = dims.total_rows;
   const bool split = dims.dtype == SPAN_LA_F32;
-  if (plan.tiles.empty() && plan.scan.empty()) return SPAN_LA_OK;
+  if (plan.n_out_tiles() == 0 && plan.scan.empty()) return SPAN_LA_OK;
 
-  const Workspace w = layout(plan, H, T, split);
-  std::vector<uint8_t> host(w.desc_bytes, 0);
-  if (!plan.tiles.empty()) std::memcpy(host.data() + w.off_tiles, plan.tiles.data(), plan.tiles.size() * sizeof(TileDesc));
-  if (!plan.chunks.empty()) std::memcpy(host.data() + w.off_chunks, plan.chunks.data(), plan.chunks.size() * sizeof(ChunkDesc));
-  if (!plan.scan.empty()) std::memcpy(host.data() + w.off_scan, plan.scan.data(), plan.scan.size() * sizeof(ScanDesc));
-  if (!plan.bounds.empty()) std::memcpy(host.data() + w.off_bounds, plan.bounds.data(), plan.bounds.size());
+  // Descriptor block (uploaded with one copy), then the state slots and, for
+  // fp32 inputs, the six bf16 part arrays.
+  std::vector<uint8_t> host;
+  const size_t off_scan = put(host, plan.scan);
+  const size_t off_bounds = put(host, plan.bounds);
+  size_t off_a = 0, off_b = 0, off_c = 0;
+  int grid = 0;
+  if (plan.span_mode) {
+    std::vector<WorkTile> work;
+    std::vector<int32_t> cta_begin;
+    if (!plan.items.empty()) grid = build_schedule(plan, H, dev->num_sms, &work, &cta_begin);
+    off_a = put(host, plan.spans);
+    off_b = put(host, work);
+    off_c = put(host, cta_begin);
+  } else {
+    off_a = put(host, plan.chunks);
+    off_b = put(host, plan.tiles);
+  }
+  const size_t desc_bytes = host.size();
+  const size_t off_states = desc_bytes;
+  const size_t state_bytes = static_cast<size_t>(plan.state_slots()) * H * kStateFloats * sizeof(float);
+  const size_t off_parts = align256(off_states + state_bytes);
+  const size_t part_bytes = static_cast<size_t>(T) * H * kHeadDim * 2;
+  const size_t total = off_parts + (split ? 6 * part_bytes : 0);
 
   uint8_t* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), w.total, stream);
-  if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): %s", w.total, cudaGetErrorString(e));
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), total, stream);
+  if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): %s", total, cudaGetErrorString(e));
   span_la_status st = SPAN_LA_OK;
   do {
-    e = cudaMemcpyAsync(ws, host.data(), w.desc_bytes, cudaMemcpyHostToDevice, stream);
+    e = cudaMemcpyAsync(ws, host.data(), desc_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) { st = cuda_fail(e, "cudaMemcpyAsync(descriptors)"); break; }
 
     // bf16 operand arrays the kernels read through TMA: the inputs themselves,
     // or, for fp32 inputs, their bf16 high / low parts made by the split kernel.
     const void* parts[3][2] = {{q, nullptr}, {k, nullptr}, {v, nullptr}};
     if (split) {
-      const size_t part_bytes = static_cast<size_t>(T) * H * kHeadDim * 2;
       for (int t = 0; t < 3; ++t)
-        for (int p = 0; p < 2; ++p) parts[t][p] = ws + w.off_parts + (2 * t + p) * part_bytes;
-      e = launch_split_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                           static_cast<const float*>(v), T * H * kHeadDim, ws + w.off_parts, stream);
+        for (int p = 0; p < 2; ++p) parts[t][p] = ws + off_parts + (2 * t + p) * part_bytes;
+      e = counted_launch(kKernelSplit, stream, [&] {
+        return launch_split_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                static_cast<const float*>(v), T * H * kHeadDim, ws + off_parts, stream);
+      });
       if (e != cudaSuccess) { st = cuda_fail(e, "split kernel launch"); break; }
     }
     DeviceOperands tile_ops{}, chunk_ops{};
-    const bool need_maps = !plan.tiles.empty() || !plan.chunks.empty();   // implies T > 0
+    const bool need_maps = plan.n_out_tiles() > 0 || plan.state_slots() > 0;   // implies T > 0
     for (int t = 0; t < 3 && st == SPAN_LA_OK && need_maps; ++t) {
       for (int p = 0; p < (split ? 2 : 1) && st == SPAN_LA_OK; ++p) {
         CUtensorMap* tm = t == 0 ? &tile_ops.q[p] : t == 1 ? &tile_ops.k[p] : &tile_ops.v[p];
@@ -314,17 +524,51 @@ span_la_status run_plan(const Plan& plan, const void* q, const void* k, const vo
     }
     if (st != SPAN_LA_OK) break;
 
-    float* states = reinterpret_cast<float*>(ws + w.off_states);
-    e = launch_chunk_state(split, chunk_ops.k, chunk_ops.v, reinterpret_cast<const ChunkDesc*>(ws + w.off_chunks),
-                           static_cast<int>(plan.chunks.size()), H, states, dev->err, stream);
-    if (e != cudaSuccess) { st = cuda_fail(e, "chunk-state launch"); break; }
-    e = launch_scan(reinterpret_cast<const ScanDesc*>(ws + w.off_scan), static_cast<int>(plan.scan.size()), H,
-                    states, final_out, stream);
-    if (e != cudaSuccess) { st = cuda_fail(e, "scan launch"); break; }
-    e = launch_tile_output(split, tile_ops.q, tile_ops.k, tile_ops.v,
-                           reinterpret_cast<const TileDesc*>(ws + w.off_tiles), static_cast<int>(plan.tiles.size()),
-                           ws + w.off_bounds, stateA, states, out, H, dev->err, stream);
-    if (e != cudaSuccess) { st = cuda_fail(e, "tile-output launch"); break; }
+    float* states = reinterpret_cast<float*>(ws + off_states);
+    bool kernel_before = split;   // a kernel precedes the next launch in the stream
+    if (plan.state_slots() > 0) {
+      e = plan.span_mode
+              ? counted_launch(kKernelSpanState, stream, [&] {
+                  return launch_span_state(chunk_ops.k, chunk_ops.v,
+                                           reinterpret_cast<const SpanDesc*>(ws + off_a),
+                                           static_cast<int>(plan.spans.size()), H, states, dev->err, stream);
+                })
+              : counted_launch(kKernelChunk, stream, [&] {
+                  return launch_chunk_state(split, chunk_ops.k, chunk_ops.v,
+                                            reinterpret_cast<const ChunkDesc*>(ws + off_a),
+                                            static_cast<int>(plan.chunks.size()), H, states, dev->err, stream);
+                });
+      if (e != cudaSuccess) { st = cuda_fail(e, "chunk/span-state launch"); break; }
+      kernel_before = true;
+    }
+    if (!plan.scan.empty()) {
+      const bool pdl = kernel_before;
+      e = counted_launch(kKernelScan, stream, [&] {
+        return launch_scan(reinterpret_cast<const ScanDesc*>(ws + off_scan),
+                           static_cast<int>(plan.scan.size()), H, states, final_out, stream, pdl);
+      });
+      if (e != cudaSuccess) { st = cuda_fail(e, "scan launch"); break; }
+      kernel_before = true;
+    }
+    if (plan.n_out_tiles() > 0) {
+      if (plan.span_mode) {
+        const bool pdl = kernel_before;
+        e = counted_launch(kKernelSpanOutput, stream, [&] {
+          return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v,
+                                    reinterpret_cast<const WorkTile*>(ws + off_b),
+                                    reinterpret_cast<const int32_t*>(ws + off_c), grid,
+                                    ws + off_bounds, stateA, states, out, H, dev->err, stream, pdl);
+        });
+      } else {
+        e = counted_launch(kKernelTile, stream, [&] {
+          return launch_tile_output(split, tile_ops.q, tile_ops.k, tile_ops.v,
+                                    reinterpret_cast<const TileDesc*>(ws + off_b),
+                                    static_cast<int>(plan.tiles.size()), ws + off_bounds, stateA,
+                                    states, out, H, dev->err, stream);
+        });
+      }
+      if (e != cudaSuccess) { st = cuda_fail(e, "output launch"); break; }
+    }
   } while (false);
   cudaError_t ef = cudaFreeAsync(ws, stream);
   if (st == SPAN_LA_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync");
@@ -365,13 +609,8 @@ span_la_status span_la_pass(const void* q, const void* k, const void* v, span_la
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != SPAN_LA_OK) return st;
 
-  Plan plan;
-  for (int32_t s = 0; s < num_views; ++s) {
-    const int64_t start = view_cu_seqlens[s], len = view_cu_seqlens[s + 1] - view_cu_seqlens[s];
-    const int chunk0 = plan.add_chunks(start, len, s);
-    plan.add_segment_tiles(start, len, -1, chunk0);
-  }
-  if (num_branches > 0) plan.add_branches(branch_cu_seqlens, num_branches, branch_parent);
+  const Plan plan = make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
+                              branch_parent, dims.num_heads, dims.dtype == SPAN_LA_BF16);
   return run_plan(plan, q, k, v, dims, view_state_out, view_state_out, out, stream, dev);
 }
 
@@ -396,8 +635,8 @@ span_la_status span_la_branches_from_state(const float* cached_state, int32_t nu
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != SPAN_LA_OK) return st;
 
-  Plan plan;
-  plan.add_branches(branch_cu_seqlens, num_branches, branch_parent);
+  const Plan plan = make_plan(nullptr, 0, branch_cu_seqlens, num_branches, branch_parent,
+                              dims.num_heads, dims.dtype == SPAN_LA_BF16);
   return run_plan(plan, q, k, v, dims, cached_state, nullptr, out, stream, dev);
 }
 
@@ -433,6 +672,83 @@ const char* span_la_status_string(span_la_status s) {
 const char* span_la_last_error_detail(void) { return g_detail.c_str(); }
 
 int32_t span_la_version(void) { return 100; }
+
+span_la_status span_la_plan_stats(const int32_t* view_cu_seqlens, int32_t num_views,
+                                  const int32_t* branch_cu_seqlens, int32_t num_branches,
+                                  const int32_t* branch_parent, int32_t num_parents,
+                                  int32_t from_state, int32_t num_heads, int32_t dtype,
+                                  int64_t* stats) {
+  g_detail.clear();
+  if (stats == nullptr) return fail(SPAN_LA_ERR_INVALID, "stats is NULL");
+  if (num_heads < 1) return fail(SPAN_LA_ERR_INVALID, "num_heads %d < 1", num_heads);
+  if (dtype != SPAN_LA_BF16 && dtype != SPAN_LA_F32) return fail(SPAN_LA_ERR_UNSUPPORTED, "dtype %d", dtype);
+  const int64_t T = INT32_MAX;
+  std::vector<Segment> segs;
+  span_la_status st = SPAN_LA_OK;
+  if (from_state) num_views = 0;
+  if ((st = check_cu(view_cu_seqlens, num_views, T, "view_cu_seqlens", &segs, true)) != SPAN_LA_OK) return st;
+  if ((st = check_cu(branch_cu_seqlens, num_branches, T, "branch_cu_seqlens", &segs, false)) != SPAN_LA_OK) return st;
+  if ((st = check_overlap(segs)) != SPAN_LA_OK) return st;
+  if ((st = check_parents(branch_parent, num_branches, from_state ? num_parents : num_views)) != SPAN_LA_OK) return st;
+  const Plan plan = make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
+                              branch_parent, num_heads, dtype == SPAN_LA_BF16);
+  int64_t state_rows = 0, finals = 0, tile_rows = 0, state_reads = 0;
+  for (const ChunkDesc& c : plan.chunks) state_rows += c.len;
+  for (const SpanDesc& c : plan.spans) state_rows += c.len;
+  for (const ScanDesc& s : plan.scan) finals += s.final_idx >= 0;
+  for (const TileDesc& t : plan.tiles) {
+    tile_rows += t.nrows;
+    state_reads += (t.stateA >= 0) + (t.stateB >= 0);
+  }
+  for (const OutTileDesc& t : plan.otiles) tile_rows += t.nrows;
+  for (const ItemDesc& it : plan.items) state_reads += (it.stateA >= 0) + (it.stateB >= 0);
+  stats[0] = plan.state_slots();
+  stats[1] = state_rows;
+  stats[2] = static_cast<int64_t>(plan.scan.size());
+  stats[3] = finals;
+  stats[4] = static_cast<int64_t>(plan.n_out_tiles());
+  stats[5] = tile_rows;
+  stats[6] = state_reads;
+  stats[7] = static_cast<int64_t>(plan.span_mode ? plan.items.size() : plan.tiles.size());
+  stats[8] = plan.G;
+  return SPAN_LA_OK;
+}
+
+span_la_status span_la_profile_enable(int32_t enable) {
+  g_profiling.store(enable != 0);
+  return SPAN_LA_OK;
+}
+
+span_la_status span_la_profile_read(double* ms_total, int64_t* timed, int64_t* launches, int32_t n) {
+  g_detail.clear();
+  if (n < 0 || n > SPAN_LA_NUM_KERNELS) return fail(SPAN_LA_ERR_INVALID, "n %d not in [0, %d]", n, SPAN_LA_NUM_KERNELS);
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  cudaError_t e = drain_events();
+  for (int k = 0; k < n; ++k) {
+    if (ms_total) ms_total[k] = g_ms[k];
+    if (timed) timed[k] = g_timed[k];
+    if (launches) launches[k] = g_launches[k].load();
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "profiling events");
+  return SPAN_LA_OK;
+}
+
+span_la_status span_la_profile_reset(void) {
+  g_detail.clear();
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  cudaError_t e = drain_events();
+  for (int k = 0; k < SPAN_LA_NUM_KERNELS; ++k) {
+    g_ms[k] = 0.0;
+    g_timed[k] = 0;
+    g_launches[k].store(0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "profiling events");
+  return SPAN_LA_OK;
+}
+
+const char* span_la_kernel_name(int32_t k) {
+  return (k >= 0 && k < SPAN_LA_NUM_KERNELS) ? kKernelNames[k] : nullptr;
+}
 
 span_la_status span_la_selftest_wait_timeout(int32_t limit_us, cudaStream_t stream) {
   g_detail.clear();

@@ -45,6 +45,53 @@ struct TileDesc {
   int32_t pad1;
 };
 
+// bf16 path.  A span is a run of up to G consecutive 128-row tiles of one
+// segment (a view or a branch longer than one tile).  The span-state kernel
+// computes the span's local state sum K^T V (span i owns state slot i); the
+// scan turns the slots of each segment into exclusive prefixes; the
+// span-output kernel walks the span's tiles carrying the state.
+struct SpanDesc {
+  int32_t row0;   // first row of the span
+  int32_t len;    // rows in the span, 1 .. G*128
+};
+
+// One work item of the span-output kernel (for every head): a span, or one
+// tile of packed short branches.  Its start state is stateA[a] + stateB[b]
+// (a missing term is -1), as for TileDesc.
+struct ItemDesc {
+  int32_t tile0;    // first entry of the item's tiles in the tile table
+  int32_t ntiles;   // 1 .. G
+  int32_t stateA;
+  int32_t stateB;
+};
+
+struct OutTileDesc {
+  int32_t row0;
+  int32_t nrows;    // 1 .. 128
+  int32_t bound0;   // segment starts inside the tile, as for TileDesc
+  int32_t nbound;
+};
+
+// One tile of the span-output kernel's per-CTA schedule (48 bytes).  The
+// host deals the (item, head) work units to CTAs and lists each CTA's tiles
+// in processing order; CTA c runs records [cta_begin[c], cta_begin[c+1]).
+constexpr int kInlineBounds = 16;
+constexpr int32_t kTileFirst = 1;      // first tile of its item: load the start state
+constexpr int32_t kTileLast = 2;       // last tile of its item: no state update
+constexpr int32_t kTileHasInit = 4;    // the item has a start state (stateA and/or stateB)
+struct WorkTile {
+  int32_t row0;
+  int32_t nrows;
+  int32_t head;
+  int32_t flags;
+  int32_t stateA;    // start state terms (first tile of an item), -1 if absent
+  int32_t stateB;
+  int32_t bound0;    // segment starts in the global bounds table
+  int32_t nbound;    // the first kInlineBounds are also inline below
+  uint8_t inl[kInlineBounds];
+};
+static_assert(sizeof(WorkTile) == 48, "WorkTile layout");
+
 struct DeviceOperands {
   // TMA descriptors; [0] = bf16 value (or high part), [1] = low part (fp32 inputs).
   CUtensorMap q[2], k[2], v[2];
@@ -59,7 +106,21 @@ cudaError_t launch_chunk_state(bool split, const CUtensorMap* tm_k, const CUtens
                                unsigned* err, cudaStream_t stream);
 
 cudaError_t launch_scan(const ScanDesc* scan, int n_scan, int H, float* ws, float* final_out,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool pdl);
+
+cudaError_t launch_span_state(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                              const SpanDesc* spans, int n_spans, int H, float* ws,
+                              unsigned* err, cudaStream_t stream);
+
+cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                               const CUtensorMap* tm_v, const WorkTile* work,
+                               const int32_t* cta_begin, int grid, const uint8_t* bounds,
+                               const float* stateA, const float* stateB, void* out, int H,
+                               unsigned* err, cudaStream_t stream, bool pdl);
+
+// Work items the planner aims for when it picks the span length G.
+constexpr int kTargetItems = 4 * 152;
+constexpr int kMaxSpanTiles = 8;
 
 cudaError_t launch_tile_output(bool split, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                const CUtensorMap* tm_v, const TileDesc* tiles, int n_tiles,

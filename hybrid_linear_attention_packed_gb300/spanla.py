@@ -28,7 +28,9 @@ STATUS = {0: "SPAN_LA_OK", 1: "SPAN_LA_ERR_INVALID", 2: "SPAN_LA_ERR_UNSUPPORTED
 
 EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
             "span_la_status_string", "span_la_last_error_detail", "span_la_version",
-            "span_la_selftest_wait_timeout")
+            "span_la_selftest_wait_timeout", "span_la_profile_enable", "span_la_profile_read",
+            "span_la_profile_reset", "span_la_kernel_name", "span_la_plan_stats")
+NUM_KERNELS = 6
 
 
 class SpanLAError(RuntimeError):
@@ -74,6 +76,20 @@ def load_library(path: Optional[str] = None):
         lib.span_la_version.restype = ctypes.c_int32
         lib.span_la_selftest_wait_timeout.argtypes = [ctypes.c_int32, vp]
         lib.span_la_selftest_wait_timeout.restype = ctypes.c_int
+        lib.span_la_profile_enable.argtypes = [ctypes.c_int32]
+        lib.span_la_profile_enable.restype = ctypes.c_int
+        lib.span_la_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                             ctypes.POINTER(ctypes.c_int64),
+                                             ctypes.POINTER(ctypes.c_int64), ctypes.c_int32]
+        lib.span_la_profile_read.restype = ctypes.c_int
+        lib.span_la_profile_reset.argtypes = []
+        lib.span_la_profile_reset.restype = ctypes.c_int
+        lib.span_la_kernel_name.argtypes = [ctypes.c_int32]
+        lib.span_la_kernel_name.restype = ctypes.c_char_p
+        lib.span_la_plan_stats.argtypes = [i32p, ctypes.c_int32, i32p, ctypes.c_int32, i32p,
+                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)]
+        lib.span_la_plan_stats.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -193,6 +209,49 @@ def span_la_selftest_wait_timeout(limit_us: int, stream=None) -> None:
     lib = load_library()
     _raise(lib, lib.span_la_selftest_wait_timeout(int(limit_us), _stream_handle(stream)),
            "span_la_selftest_wait_timeout")
+
+
+PLAN_FIELDS = ("state_slots", "state_rows", "scan_segments", "final_states", "tiles",
+               "tile_rows", "start_state_reads", "out_items", "span_tiles")
+
+
+def plan_stats(view_cu_seqlens, branch_cu_seqlens, branch_parent, num_heads: int,
+               dtype: str = "bf16", num_parents: int = 0, from_state: bool = False) -> dict:
+    """Work units the library would launch for this metadata (host only)."""
+    lib = load_library()
+    vcu, bcu, par = _i32(view_cu_seqlens), _i32(branch_cu_seqlens), _i32(branch_parent)
+    V = max(len(vcu) - 1, 0)
+    B = max(len(bcu) - 1, 0)
+    stats = (ctypes.c_int64 * len(PLAN_FIELDS))()
+    dt = SPAN_LA_BF16 if dtype == "bf16" else SPAN_LA_F32
+    _raise(lib, lib.span_la_plan_stats(_iptr(vcu), V, _iptr(bcu), B, _iptr(par), int(num_parents),
+                                       1 if from_state else 0, int(num_heads), dt, stats),
+           "span_la_plan_stats")
+    return dict(zip(PLAN_FIELDS, (int(x) for x in stats)))
+
+
+def profile_enable(on: bool = True) -> None:
+    """Time every kernel launch with CUDA events on its stream (tracing hook)."""
+    lib = load_library()
+    _raise(lib, lib.span_la_profile_enable(1 if on else 0), "span_la_profile_enable")
+
+
+def profile_reset() -> None:
+    lib = load_library()
+    _raise(lib, lib.span_la_profile_reset(), "span_la_profile_reset")
+
+
+def profile_read() -> dict:
+    """Per kernel name: {"ms": summed event time, "timed": launches timed,
+    "launches": launches counted} since the last reset."""
+    lib = load_library()
+    ms = (ctypes.c_double * NUM_KERNELS)()
+    timed = (ctypes.c_int64 * NUM_KERNELS)()
+    launches = (ctypes.c_int64 * NUM_KERNELS)()
+    _raise(lib, lib.span_la_profile_read(ms, timed, launches, NUM_KERNELS), "span_la_profile_read")
+    return {lib.span_la_kernel_name(k).decode(): {"ms": ms[k], "timed": timed[k],
+                                                  "launches": launches[k]}
+            for k in range(NUM_KERNELS)}
 
 
 def version() -> int:

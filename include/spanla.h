@@ -159,6 +159,58 @@ int32_t span_la_version(void);
  */
 span_la_status span_la_selftest_wait_timeout(int32_t limit_us, cudaStream_t stream);
 
+/*
+ * span_la_plan_stats -- host only, no CUDA call: the work units a call with
+ * this metadata, head count and dtype would launch (used to count the
+ * algorithmic bytes of each kernel).
+ *   stats[0] state slots: 64-row chunks (fp32) or spans of up to G tiles (bf16)
+ *   stats[1] rows those slots cover (rows whose K and V the state kernel reads)
+ *   stats[2] segments of the segmented scan
+ *   stats[3] scan segments that write a final view state
+ *   stats[4] output tiles (<= 128 rows each)
+ *   stats[5] rows those tiles cover
+ *   stats[6] fp32 64x64 start-state reads of the output kernel (per head)
+ *   stats[7] output work items per head (tiles for fp32, items for bf16)
+ *   stats[8] G, the tiles per span (1 for fp32)
+ * from_state != 0 plans span_la_branches_from_state (views ignored).
+ * Returns SPAN_LA_ERR_INVALID on bad metadata, like the entry points.
+ */
+span_la_status span_la_plan_stats(const int32_t *view_cu_seqlens, int32_t num_views,
+                                  const int32_t *branch_cu_seqlens, int32_t num_branches,
+                                  const int32_t *branch_parent, int32_t num_parents,
+                                  int32_t from_state, int32_t num_heads, int32_t dtype,
+                                  int64_t *stats);
+
+/*
+ * Kernel profiling (tracing hook).  Kernels are numbered
+ *   0 split_f32, 1 chunk_state, 3 tile_output (fp32 inputs),
+ *   2 segmented_scan (both), 4 span_state, 5 span_output (bf16 inputs).
+ * Launches of every kernel are always counted.  While profiling is enabled,
+ * every launch is also bracketed by two CUDA events recorded on the call's
+ * stream (one device only); span_la_profile_read() waits for the pending
+ * events and adds their elapsed times up.  Enabling adds two event records per
+ * launch and nothing else to the work on the stream.
+ */
+#define SPAN_LA_NUM_KERNELS 6
+
+/* Turn event timing on (non-zero) or off. */
+span_la_status span_la_profile_enable(int32_t enable);
+
+/*
+ * Per kernel id k < n (n <= SPAN_LA_NUM_KERNELS): ms_total[k] = summed event
+ * time of its timed launches, timed[k] = launches timed, launches[k] = all
+ * launches since the last reset.  Any of the three arrays may be NULL.
+ * Synchronises on the pending events.
+ */
+span_la_status span_la_profile_read(double *ms_total, int64_t *timed, int64_t *launches,
+                                    int32_t n);
+
+/* Clear the counters and timings (waits for pending events first). */
+span_la_status span_la_profile_reset(void);
+
+/* Static name of kernel id k, or NULL. */
+const char *span_la_kernel_name(int32_t k);
+
 #ifdef __cplusplus
 }
 #endif

@@ -77,12 +77,14 @@ static int check_cu(const int32_t *cu, int32_t n, int64_t T)
     return 0;
 }
 
-static void set_threads(int nthreads)
+/* Threads of one call: nthreads if positive, else the OpenMP default. */
+static int threads_for(int nthreads)
 {
 #ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
+    return nthreads > 0 ? nthreads : omp_get_max_threads();
 #else
     (void)nthreads;
+    return 1;
 #endif
 }
 
@@ -94,13 +96,13 @@ static int run_branches(const double *init_states, int32_t num_states,
                         const double *q, const double *k, const double *v,
                         int64_t H, int64_t D,
                         const int32_t *branch_cu, int32_t B, const int32_t *parent,
-                        double *out)
+                        double *out, int nt)
 {
     for (int32_t b = 0; b < B; ++b)
         if (parent[b] < 0 || parent[b] >= num_states) return 1;
     const int64_t items = (int64_t)B * H;
     int err = 0;
-#pragma omp parallel
+#pragma omp parallel num_threads(nt)
     {
         double *S = (double *)malloc(sizeof(double) * D * D);
         if (S == NULL) {
@@ -135,10 +137,10 @@ int oracle_pass(const double *q, const double *k, const double *v,
     if (H < 1 || D < 1 || T < 0) return 1;
     if (check_cu(view_cu, V, T) || check_cu(branch_cu, B, T)) return 1;
     if (B > 0 && (parent == NULL || V < 1)) return 1;
-    set_threads(nthreads);
+    const int nt = threads_for(nthreads);
 
     const int64_t items = (int64_t)V * H;
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
     for (int64_t it = 0; it < items; ++it) {
         const int64_t vi = it / H, h = it % H;
         double *S = state_out + (vi * H + h) * D * D;
@@ -146,7 +148,7 @@ int oracle_pass(const double *q, const double *k, const double *v,
         run_rows(q, k, v, H, D, h, view_cu[vi], view_cu[vi + 1], S, out);
     }
     if (B == 0) return 0;
-    return run_branches(state_out, V, q, k, v, H, D, branch_cu, B, parent, out);
+    return run_branches(state_out, V, q, k, v, H, D, branch_cu, B, parent, out, nt);
 }
 
 /*
@@ -162,9 +164,8 @@ int oracle_branches_from_state(const double *states, int32_t P,
     if (H < 1 || D < 1 || T < 0 || P < 0) return 1;
     if (check_cu(branch_cu, B, T)) return 1;
     if (B > 0 && (parent == NULL || states == NULL)) return 1;
-    set_threads(nthreads);
     if (B == 0) return 0;
-    return run_branches(states, P, q, k, v, H, D, branch_cu, B, parent, out);
+    return run_branches(states, P, q, k, v, H, D, branch_cu, B, parent, out, threads_for(nthreads));
 }
 
 int oracle_max_threads(void)

@@ -106,3 +106,27 @@ def test_empty_call_is_a_no_op(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not found"):
         spanla.load_library(str(tmp_path / "nope.so"))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("name", ["tiny", "single", "packed4", "cached_long", "sweep4"])
+def test_plan_covers_every_row_once(lib, dtype, name):
+    """The planner's output tiles cover every segment row, and its state slots
+    cover exactly the rows of views and of branches longer than one tile."""
+    from hybrid_linear_attention_packed_gb300 import workloads
+    w = workloads.by_name(name)
+    st = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H, dtype)
+    assert st["tile_rows"] == w.rows
+    long_rows = int(sum(L for L in w.branch_lens if L > 128))
+    assert st["state_rows"] == int(w.view_lens.sum()) + long_rows
+    assert st["scan_segments"] == w.V + sum(1 for L in w.branch_lens if L > 128)
+    assert st["final_states"] == w.V
+    if dtype == "f32":
+        assert st["span_tiles"] == 1
+        assert st["state_slots"] == sum(-(-int(L) // 64) for L in list(w.view_lens)
+                                        + [L for L in w.branch_lens if L > 128])
+    else:
+        G = st["span_tiles"]
+        assert 1 <= G <= 8
+        assert st["state_slots"] == sum(-(-int(L) // (128 * G)) for L in list(w.view_lens)
+                                        + [L for L in w.branch_lens if L > 128])
