@@ -1,0 +1,63 @@
+// Fixed device scratch for span_la_pass_noalloc.
+//
+// Some callers cannot allocate device memory while they run a pass: a process
+// that hands all of the GPU's memory to its own pool up front, or code that
+// runs where an allocation could block or fail at the wrong moment.  For them
+// the library keeps one workspace for the whole process in a file-scope device
+// array of fixed size.  Every GPU that loads this module holds it until the
+// process exits.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "spanla_internal.h"
+
+namespace spanla {
+namespace {
+
+// Largest workspace a no-allocation pass may use: descriptors plus one fp32
+// 64x64 state per span and head (16 KiB each), i.e. about a thousand
+// span-heads -- a 7,400-token or four-request 16-head pass fits.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+// Error word of the no-allocation path's kernels (bounded waits that ran out).
+static __device__ unsigned g_noalloc_err;
+
+struct Slot {
+  bool ready = false;
+  uint8_t* scratch = nullptr;
+  unsigned* err = nullptr;
+};
+
+std::mutex g_mu;
+Slot g_slots[64];
+
+}  // namespace
+
+// Device addresses of the scratch array and error word on the current device.
+// The first call on a device looks them up with cudaGetSymbolAddress (with
+// that device current) and caches them; later calls only read the cache.
+cudaError_t noalloc_scratch(uint8_t** scratch, unsigned** err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  Slot& s = g_slots[dev];
+  if (!s.ready) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    void* q = nullptr;
+    e = cudaGetSymbolAddress(&q, g_noalloc_err);
+    if (e != cudaSuccess) return e;
+    s.scratch = static_cast<uint8_t*>(p);
+    s.err = static_cast<unsigned*>(q);
+    s.ready = true;
+  }
+  *scratch = s.scratch;
+  *err = s.err;
+  return cudaSuccess;
+}
+
+}  // namespace spanla

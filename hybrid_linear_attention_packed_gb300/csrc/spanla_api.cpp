@@ -750,6 +750,119 @@ const char* span_la_kernel_name(int32_t k) {
   return (k >= 0 && k < SPAN_LA_NUM_KERNELS) ? kKernelNames[k] : nullptr;
 }
 
+span_la_status span_la_pass_noalloc(const void* q, const void* k, const void* v, span_la_dims dims,
+                                    const int32_t* view_cu_seqlens, int32_t num_views,
+                                    const int32_t* branch_cu_seqlens, int32_t num_branches,
+                                    const int32_t* branch_parent, void* out, float* view_state_out,
+                                    cudaStream_t stream) {
+  g_detail.clear();
+  span_la_status st = check_dims(dims);
+  if (st != SPAN_LA_OK) return st;
+  if (dims.dtype != SPAN_LA_BF16)
+    return fail(SPAN_LA_ERR_UNSUPPORTED,
+                "span_la_pass_noalloc takes bf16 inputs only (fp32 inputs need per-call scratch "
+                "for their bf16 parts; use span_la_pass)");
+  std::vector<Segment> segs;
+  if ((st = check_cu(view_cu_seqlens, num_views, dims.total_rows, "view_cu_seqlens", &segs, true)) != SPAN_LA_OK) return st;
+  if ((st = check_cu(branch_cu_seqlens, num_branches, dims.total_rows, "branch_cu_seqlens", &segs, false)) != SPAN_LA_OK) return st;
+  if ((st = check_overlap(segs)) != SPAN_LA_OK) return st;
+  if ((st = check_parents(branch_parent, num_branches, num_views)) != SPAN_LA_OK) return st;
+  if (!segs.empty() && (st = check_operands(q, k, v, out, dims)) != SPAN_LA_OK) return st;
+  if (num_views > 0 && (view_state_out == nullptr || !aligned16(view_state_out)))
+    return fail(SPAN_LA_ERR_INVALID, "view_state_out must be a non-NULL 16-byte aligned pointer");
+  if (num_views == 0 && num_branches == 0) return SPAN_LA_OK;
+
+  // Device checks without the allocating set-up of the other entry points.
+  int dev = 0, major = 0, minor = 0, num_sms = 1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  if (!(major == 10 && minor == 3))
+    return fail(SPAN_LA_ERR_UNSUPPORTED, "libspanla is built for sm_103a only; device %d is sm_%d%d",
+                dev, major, minor);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult qr;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr);
+      if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || fn == nullptr)
+        return fail(SPAN_LA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  uint8_t* ws = nullptr;
+  unsigned* err = nullptr;
+  e = noalloc_scratch(&ws, &err);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed scratch)");
+
+  const int H = dims.num_heads;
+  const int64_t T = dims.total_rows;
+  const Plan plan = make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
+                              branch_parent, H, true);
+  std::vector<uint8_t> host;
+  const size_t off_scan = put(host, plan.scan);
+  const size_t off_bounds = put(host, plan.bounds);
+  std::vector<WorkTile> work;
+  std::vector<int32_t> cta_begin;
+  int grid = 0;
+  if (!plan.items.empty()) grid = build_schedule(plan, H, num_sms, &work, &cta_begin);
+  const size_t off_spans = put(host, plan.spans);
+  const size_t off_work = put(host, work);
+  const size_t off_begin = put(host, cta_begin);
+  const size_t off_states = host.size();
+  const size_t need = off_states + static_cast<size_t>(plan.state_slots()) * H * kStateFloats * sizeof(float);
+  if (need > kNoAllocScratchBytes)
+    return fail(SPAN_LA_ERR_INVALID,
+                "this pass needs %zu bytes of scratch; the fixed scratch of span_la_pass_noalloc holds "
+                "%zu bytes (use span_la_pass)", need, kNoAllocScratchBytes);
+
+  // The error word starts each call at zero; everything else in the scratch
+  // is written before it is read.
+  e = cudaMemsetAsync(err, 0, sizeof(unsigned), stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
+  DeviceOperands tile_ops{}, chunk_ops{};
+  const void* ops[3] = {q, k, v};
+  for (int t = 0; t < 3; ++t) {
+    CUtensorMap* tm = t == 0 ? &tile_ops.q[0] : t == 1 ? &tile_ops.k[0] : &tile_ops.v[0];
+    CUtensorMap* cm = t == 0 ? &chunk_ops.q[0] : t == 1 ? &chunk_ops.k[0] : &chunk_ops.v[0];
+    if ((st = encode_map(tm, ops[t], T, H, kTileBoxRows, 1)) != SPAN_LA_OK) return st;
+    if (t > 0 && (st = encode_map(cm, ops[t], T, H, kChunkBoxRows, kChunkBoxHeads)) != SPAN_LA_OK) return st;
+  }
+  float* states = reinterpret_cast<float*>(ws + off_states);
+  bool kernel_before = false;
+  if (plan.state_slots() > 0) {
+    e = counted_launch(kKernelSpanState, stream, [&] {
+      return launch_span_state(chunk_ops.k, chunk_ops.v, reinterpret_cast<const SpanDesc*>(ws + off_spans),
+                               static_cast<int>(plan.spans.size()), H, states, err, stream);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "span-state launch");
+    kernel_before = true;
+  }
+  if (!plan.scan.empty()) {
+    const bool pdl = kernel_before;
+    e = counted_launch(kKernelScan, stream, [&] {
+      return launch_scan(reinterpret_cast<const ScanDesc*>(ws + off_scan), static_cast<int>(plan.scan.size()),
+                         H, states, view_state_out, stream, pdl);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "scan launch");
+    kernel_before = true;
+  }
+  if (grid > 0) {
+    const bool pdl = kernel_before;
+    e = counted_launch(kKernelSpanOutput, stream, [&] {
+      return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v, reinterpret_cast<const WorkTile*>(ws + off_work),
+                                reinterpret_cast<const int32_t*>(ws + off_begin), grid, ws + off_bounds,
+                                view_state_out, states, out, H, err, stream, pdl);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "span-output launch");
+  }
+  return SPAN_LA_OK;
+}
+
 span_la_status span_la_selftest_wait_timeout(int32_t limit_us, cudaStream_t stream) {
   g_detail.clear();
   if (limit_us < 1 || limit_us > 1000000)

@@ -129,6 +129,10 @@ cudaError_t launch_tile_output(bool split, const CUtensorMap* tm_q, const CUtens
 
 cudaError_t launch_wait_timeout_probe(unsigned limit_us, unsigned* err, cudaStream_t stream);
 
+// Fixed workspace of span_la_pass_noalloc (a file-scope device array).
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+cudaError_t noalloc_scratch(uint8_t** scratch, unsigned** err);
+
 // Box sizes of the TMA descriptors each kernel expects.
 constexpr int kChunkBoxRows = kChunk;     // chunk-state kernel: 64 rows x 2 heads
 constexpr int kChunkBoxHeads = 2;

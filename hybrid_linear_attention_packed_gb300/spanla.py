@@ -29,7 +29,8 @@ STATUS = {0: "SPAN_LA_OK", 1: "SPAN_LA_ERR_INVALID", 2: "SPAN_LA_ERR_UNSUPPORTED
 EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
             "span_la_status_string", "span_la_last_error_detail", "span_la_version",
             "span_la_selftest_wait_timeout", "span_la_profile_enable", "span_la_profile_read",
-            "span_la_profile_reset", "span_la_kernel_name", "span_la_plan_stats")
+            "span_la_profile_reset", "span_la_kernel_name", "span_la_plan_stats",
+            "span_la_pass_noalloc")
 NUM_KERNELS = 6
 
 
@@ -63,6 +64,9 @@ def load_library(path: Optional[str] = None):
         lib.span_la_pass.argtypes = [vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
                                      ctypes.c_int32, i32p, vp, vp, vp]
         lib.span_la_pass.restype = ctypes.c_int
+        lib.span_la_pass_noalloc.argtypes = [vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
+                                             ctypes.c_int32, i32p, vp, vp, vp]
+        lib.span_la_pass_noalloc.restype = ctypes.c_int
         lib.span_la_branches_from_state.argtypes = [vp, ctypes.c_int32, vp, vp, vp, Dims, i32p,
                                                     ctypes.c_int32, i32p, vp, vp]
         lib.span_la_branches_from_state.restype = ctypes.c_int

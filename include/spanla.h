@@ -133,6 +133,46 @@ span_la_status span_la_branches_from_state(const float *cached_state, int32_t nu
                                            void *out, cudaStream_t stream);
 
 /*
+ * span_la_pass_noalloc -- span_la_pass for callers that cannot allocate
+ * device memory during a call.
+ *
+ * The pages have no counterpart of this entry point; it is a deployment aid.
+ * span_la_pass takes its workspace from the stream-ordered allocator on every
+ * call.  A caller that has handed the GPU's memory to its own pool, or that
+ * runs where an allocation could block or fail at the wrong moment, can use
+ * this variant instead: it computes the same pass with the same kernels, but
+ * its workspace is one fixed 16 MiB array in device memory that belongs to the
+ * library (every GPU on which it is used holds the array until the process
+ * exits).  It calls no allocating routine.
+ *
+ *   arguments        as for span_la_pass; dims.dtype must be SPAN_LA_BF16
+ *                    (fp32 inputs need per-call scratch: SPAN_LA_ERR_UNSUPPORTED)
+ *   size limit       descriptors plus one 16 KiB fp32 state per span and head
+ *                    must fit in 16 MiB (a 7,400-token or four-request 16-head
+ *                    pass does); a larger pass returns SPAN_LA_ERR_INVALID with
+ *                    the bytes it needs, before anything is enqueued
+ *   first call       the first call on a device looks up the array's device
+ *                    address (cudaGetSymbolAddress with that device current)
+ *                    and caches it; make that first call before any stream
+ *                    capture
+ *   sharing          every call uses the same array and leaves its contents
+ *                    behind; calls whose work overlaps on the GPU (other
+ *                    streams, other threads) race on it -- order them on one
+ *                    stream
+ *   errors           as for span_la_pass, except that device-side wait
+ *                    timeouts of this path land in an error word inside the
+ *                    library's fixed scratch (cleared at each call) and are
+ *                    not reported by span_la_check
+ */
+span_la_status span_la_pass_noalloc(const void *q, const void *k, const void *v,
+                                    span_la_dims dims,
+                                    const int32_t *view_cu_seqlens, int32_t num_views,
+                                    const int32_t *branch_cu_seqlens, int32_t num_branches,
+                                    const int32_t *branch_parent,
+                                    void *out, float *view_state_out,
+                                    cudaStream_t stream);
+
+/*
  * span_la_check -- synchronise `stream`, then report (and clear) the device
  * error word of the current device.  Returns SPAN_LA_ERR_CUDA if the stream
  * reports a CUDA error, SPAN_LA_ERR_TIMEOUT if a kernel's bounded wait ran
