@@ -9,19 +9,19 @@
 // final_idx >= 0.  An empty view (n = 0) gets the zero state.
 //
 // fp32 adds on CUDA cores; the kernel is bound by memory traffic.  One CTA of
-// 256 threads owns a 1,024-float quarter of one (segment, head) state and
-// walks the segment's chunks in order, keeping the running sum in registers
-// and loading eight chunks ahead so the loads stay in flight while the
-// stores drain.
+// 128 threads owns a 512-float eighth of one (segment, head) state and walks
+// the segment's chunks in order, keeping the running sum in registers and
+// loading sixteen chunks ahead so the loads stay in flight while the stores
+// drain.
 #include "spanla_internal.h"
 #include "tc_ptx.cuh"
 
 namespace spanla {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kSlices = kStateFloats / (kThreads * 4);   // 4 CTAs per (segment, head)
-constexpr int kAhead = 8;
+constexpr int kThreads = 128;
+constexpr int kSlices = kStateFloats / (kThreads * 4);   // 8 CTAs per (segment, head)
+constexpr int kAhead = 16;
 
 __device__ __forceinline__ float4 add4(float4 a, float4 b) {
   return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);

@@ -50,8 +50,11 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const int span = blockIdx.x;
-  const int h0 = blockIdx.y * kChunkBoxHeads;
+  // One CTA per (span, head pair); head pairs vary fastest, so the CTAs
+  // reading the same rows run together.
+  const int pairs = (H + kChunkBoxHeads - 1) / kChunkBoxHeads;
+  const int span = blockIdx.x / pairs;
+  const int h0 = (blockIdx.x % pairs) * kChunkBoxHeads;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
   if (tid == 0) {
@@ -205,7 +208,9 @@ cudaError_t launch_span_state(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                               const SpanDesc* spans, int n_spans, int H, float* ws,
                               unsigned* err, cudaStream_t stream) {
   if (n_spans <= 0) return cudaSuccess;
-  const dim3 grid(n_spans, (H + kChunkBoxHeads - 1) / kChunkBoxHeads);
+  const int64_t ctas = static_cast<int64_t>(n_spans) * ((H + kChunkBoxHeads - 1) / kChunkBoxHeads);
+  if (ctas > INT32_MAX) return cudaErrorInvalidConfiguration;
+  const dim3 grid(static_cast<unsigned>(ctas));
   const uint32_t bytes = SpanSmem::kRequest;
   cudaError_t e =
       cudaFuncSetAttribute(span_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);

@@ -1,0 +1,125 @@
+"""Structural GPU tests that need no oracle: determinism, sibling independence,
+in-pass branches against branches from the cached state, and the bounded-wait
+failure path ("Serving 0.88M TPS from Two RTXs and Mac Minis", section "The
+Workload": branches attend to the view, not to each other; section "Long
+Requests": branch shards reuse the view's cached state)."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import to_device
+from hybrid_linear_attention_packed_gb300 import (SpanLAError, span_la_branches_from_state,
+                                                  span_la_check, span_la_pass, spanla, workloads)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, dev):
+    q, k, v = to_device(w, dev)
+    out, state = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
+                              out=torch.full_like(q, float("nan")))
+    span_la_check()
+    return out, state
+
+
+def test_run_to_run_bit_identical(cuda_device):
+    w = workloads.packed_four(1)
+    o1, s1 = _run(w, cuda_device)
+    o2, s2 = _run(w, cuda_device)
+    seg = torch.zeros(w.T, dtype=torch.bool)
+    seg[: w.branch_cu[-1]] = True
+    assert torch.equal(o1[seg.to(cuda_device)], o2[seg.to(cuda_device)])
+    assert torch.equal(s1, s2)
+
+
+def _pack(view_len, branches, H, seed):
+    """A view plus the given list of (name, rows) branches, each row drawn from
+    the same per-branch seeded stream so a branch is identical wherever it sits."""
+    rng = np.random.default_rng([seed, 7])
+    view = rng.standard_normal((3, view_len, H, 64), dtype=np.float32)
+    parts = [view]
+    for name, rows in branches:
+        r = np.random.default_rng([seed, 100 + name])
+        parts.append(r.standard_normal((3, rows, H, 64), dtype=np.float32))
+    x = np.concatenate(parts, axis=1)
+    x[0] *= 0.125
+    x[1] *= 0.125
+    t = torch.from_numpy(x).to(torch.bfloat16)
+    lens = [rows for _, rows in branches]
+    bcu = np.concatenate([[view_len], view_len + np.cumsum(lens)]).astype(np.int32)
+    return t[0].contiguous(), t[1].contiguous(), t[2].contiguous(), bcu
+
+
+def _branch_outputs(view_len, branches, H, seed, dev):
+    q, k, v = (t.to(dev) for t in _pack(view_len, branches, H, seed)[:3])
+    bcu = _pack(view_len, branches, H, seed)[3]
+    out, _ = span_la_pass(q, k, v, [0, view_len], bcu, [0] * len(branches))
+    span_la_check()
+    res = {}
+    for i, (name, rows) in enumerate(branches):
+        res[name] = out[bcu[i]:bcu[i + 1]].clone()
+    return res
+
+
+def test_siblings_do_not_change_a_branch(cuda_device):
+    H, view_len, seed = 2, 300, 41
+    base = [(0, 30), (1, 45), (2, 20), (3, 90)]
+    ref = _branch_outputs(view_len, base, H, seed, cuda_device)
+    # removing or adding siblings after a branch leaves its tile position as it
+    # was: bit-identical
+    fewer = _branch_outputs(view_len, base[:2], H, seed, cuda_device)
+    more = _branch_outputs(view_len, base + [(4, 17), (5, 64)], H, seed, cuda_device)
+    for name in (0, 1):
+        assert torch.equal(fewer[name], ref[name])
+    for name in range(4):
+        assert torch.equal(more[name], ref[name])
+    # permuting moves branches inside the packed tiles: the tensor cores then
+    # sum the same products in another grouping, so equal to fp32 rounding
+    perm = _branch_outputs(view_len, [base[3], base[1], base[0], base[2]], H, seed, cuda_device)
+    for name in range(4):
+        a, b = perm[name].double(), ref[name].double()
+        assert float((a - b).abs().max()) <= 1e-5 * float(b.abs().max()) + 2 ** -8
+
+
+def test_in_pass_branches_equal_branches_from_the_cached_state(cuda_device):
+    w = workloads.make_pass([700, 129], [30, 60, 100, 5, 128], [0, 0, 1, 1, 0], H=3,
+                            dtype="bf16", seed=42)
+    q, k, v = to_device(w, cuda_device)
+    out, state = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+    out2 = span_la_branches_from_state(state.clone(), q, k, v, w.branch_cu, w.branch_parent,
+                                       out=torch.full_like(q, float("nan")))
+    span_la_check()
+    br = slice(int(w.branch_cu[0]), int(w.branch_cu[-1]))
+    assert torch.equal(out[br], out2[br])
+    assert torch.isnan(out2[: int(w.view_cu[-1])]).all()
+
+
+def test_bounded_wait_times_out_without_trapping(cuda_device):
+    """A kernel waits on an mbarrier that nothing completes, with a 1 ms limit:
+    it records the timeout and returns; span_la_check reports it; the context
+    stays usable."""
+    spanla.span_la_check()
+    spanla.span_la_selftest_wait_timeout(1000)
+    with pytest.raises(SpanLAError) as exc:
+        span_la_check()
+    assert exc.value.status == 5
+    span_la_check()   # the error word was cleared
+    w = workloads.make_pass([100], [10], [0], H=1, dtype="bf16", seed=43)
+    out, _ = _run(w, cuda_device)
+    assert not torch.isnan(out[: w.rows]).any()
+
+
+def test_profiler_counts_and_times_every_launch(cuda_device):
+    w = workloads.single_request(0)
+    q, k, v = to_device(w, cuda_device)
+    spanla.profile_reset()
+    spanla.profile_enable(True)
+    for _ in range(3):
+        span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+    span_la_check()
+    spanla.profile_enable(False)
+    prof = spanla.profile_read()
+    for name in ("span_state", "segmented_scan", "span_output"):
+        assert prof[name]["launches"] == 3 and prof[name]["timed"] == 3
+        assert prof[name]["ms"] > 0
+    assert prof["chunk_state"]["launches"] == 0
