@@ -16,48 +16,56 @@
 //
 // and the next tile of the item starts from S + K^T V of this one.
 //
-// Persistent CTAs (one per SM) walk a host-built list of tiles.  6 warps:
-//   warp 0     producer: Q, K, V tiles by TMA and, at an item's first tile,
-//              its fp32 start states by bulk copy, into a two-stage ring
-//   warp 1     MMA issuer (one lane; the warp zeroes partial-tile K/V rows),
-//              two TMEM accumulator buffers b = tile & 1:
-//                P_b  = Q K^T              M128 N128 K64
-//                O_b  = Q S_hi + Q S_lo    M128 N64  K64
-//                dS (+)= K^T V             M128 N64  K128
-//                O_b += P V                M128 N64  K128
-//              so P of the next tile is computed while the epilogue is still
-//              storing O of this one
-//   warps 2-5  epilogue, one tile row per thread (TMEM lane): P -> masked
-//              bf16 A operand; S + dS -> bf16 high/low B operand of the next
-//              tile; O -> global.
-// K^T V uses both tiles MN-major with M = 128: the second 64-wide M atom is the
-// V tile, so TMEM lanes 64..127 of dS are unused.
+// Persistent CTAs (one per SM) walk a host-built list of tiles, software
+// pipelined over consecutive tiles t.  11 warps:
+//   warp 0     producer: Q, K, V tiles by TMA into a three-stage ring.
+//   warp 1     P issuer (one lane; the warp zeroes partial-tile K/V rows):
+//              P(t) = Q K^T  (M128 N128 K64) as soon as tile t has landed.
+//   warp 2     O issuer (one lane): once S(t) is staged,  O(t) = Q S_hi +
+//              Q S_lo  (M128 N64 K64) and the state update  S (+)= K^T V
+//              (M128 N64 K128); once P(t) is in shared memory,  O(t) +=
+//              P(t) V  (M128 N64 K128).  P and O have two TMEM buffers each
+//              (t & 1), so P of the next tiles is computed while O of this
+//              one is still being built.
+//   warps 3-10 epilogue, two warps per TMEM lane quarter: each thread owns
+//              one tile row (TMEM lane) and half of its columns.  Per step t
+//              it stages S(t+1) (the next item's start state, fetched into
+//              registers a tile ahead, or the running state), turns P(t+1) into the
+//              masked bf16 A operand (double-buffered in shared memory), and
+//              only then stores O(t) -- so the tensor cores run ahead of it.
+// The running state of a span lives in TMEM: at the span's first tile the
+// epilogue writes the start state into the state columns, and every K^T V
+// accumulates on top of it.  K^T V uses both tiles MN-major with M = 128: the
+// second 64-wide M atom is the V tile, so TMEM lanes 64..127 of the state
+// columns are unused.
 #include "spanla_internal.h"
 #include "tc_ptx.cuh"
 
 namespace spanla {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
+constexpr int kThreads = 352;
+constexpr int kEpilogueThreads = 256;
+constexpr int kStages = 3;
 constexpr uint32_t kRowTileBytes = kTileRows * 128;        // 128 rows x 128 B
-constexpr uint32_t kStateBytes = kStateFloats * 4;         // fp32 64 x 64
-constexpr uint32_t kStageBytes = 3 * kRowTileBytes + 2 * kStateBytes;   // Q K V SA SB
+constexpr uint32_t kStageBytes = 3 * kRowTileBytes;       // Q K V
 constexpr uint32_t kStateTileBytes = kHeadDim * 128;       // 64 rows x 128 B (bf16)
+constexpr uint32_t kPBufBytes = 2 * kRowTileBytes;         // [2 blocks][128][64] bf16
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: buffer b holds P at kColP<b> (128) and O at kColO<b> (64).
-constexpr uint32_t kColP0 = 0, kColO0 = 128, kColS = 192, kColP1 = 256, kColO1 = 384;
+// TMEM columns: P buffers (128 each), O buffers (64 each), running state (64).
+constexpr uint32_t kColP0 = 0, kColP1 = 128, kColO0 = 256, kColO1 = 320, kColS = 384;
 
 struct OutSmem {
   static constexpr uint32_t kStage0 = 0;
-  static constexpr uint32_t kQ = 0, kK = kRowTileBytes, kV = 2 * kRowTileBytes,
-                            kSA = 3 * kRowTileBytes, kSB = 3 * kRowTileBytes + kStateBytes;
+  static constexpr uint32_t kQ = 0, kK = kRowTileBytes, kV = 2 * kRowTileBytes;
   static constexpr uint32_t kS = kStages * kStageBytes;          // S hi, S lo (bf16)
-  static constexpr uint32_t kP = kS + 2 * kStateTileBytes;       // [2 blocks][128][64] bf16
-  static constexpr uint32_t kBar = kP + 2 * kRowTileBytes;
+  static constexpr uint32_t kP = kS + 2 * kStateTileBytes;       // two P buffers
+  static constexpr uint32_t kBar = kP + 2 * kPBufBytes;
   // barrier slots (8 bytes each)
-  static constexpr int kFull = 0, kEmpty = 2, kPReady = 4, kOReady = 6, kTmemFree = 8,
-                       kSAccReady = 10, kPSmem = 11, kSSmem = 12, kNumBars = 13;
+  static constexpr int kFull = 0, kEmpty = kStages, kPReady = 2 * kStages,
+                       kPFree = kPReady + 2, kPSmem = kPReady + 4, kOReady = kPReady + 6,
+                       kOFree = kPReady + 8, kSSmem = kPReady + 10, kSAcc = kPReady + 11,
+                       kSFree = kPReady + 12, kNumBars = kPReady + 13;
   static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
   static constexpr uint32_t kBytes = kTmemSlot + 8;
   static constexpr uint32_t kRequest = kBytes + 1024;
@@ -81,11 +89,11 @@ __device__ __forceinline__ WorkTile load_tile(const WorkTile* p) {
   return t;
 }
 
-// Write 64 state values of row d as bf16 high / low parts into the MN-major
-// S operand ([d][64 e], 128-byte swizzle).
-__device__ __forceinline__ void stage_state_row(uint8_t* s_op, int d, const float* x) {
+// Write 32 state values (columns 32*half ..) of row d as bf16 high / low parts
+// into the MN-major S operand ([d][64 e], 128-byte swizzle).
+__device__ __forceinline__ void stage_state_half_row(uint8_t* s_op, int d, int half, const float* x) {
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {
+  for (int g = 0; g < 4; ++g) {
     uint32_t hi[4], lo[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -95,7 +103,7 @@ __device__ __forceinline__ void stage_state_row(uint8_t* s_op, int d, const floa
       hi[u] = pack_bf16x2(h0, h1);
       lo[u] = pack_bf16x2(l0, l1);
     }
-    const uint32_t off = sw128_offset(d, 8 * g);
+    const uint32_t off = sw128_offset(d, 32 * half + 8 * g);
     *reinterpret_cast<uint4*>(s_op + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
     *reinterpret_cast<uint4*>(s_op + kStateTileBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
@@ -120,16 +128,20 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(L::kFull + s), 1);
       mbar_init(bar(L::kEmpty + s), 1);
-      mbar_init(bar(L::kPReady + s), 1);
-      mbar_init(bar(L::kOReady + s), 1);
-      mbar_init(bar(L::kTmemFree + s), 128);
     }
-    mbar_init(bar(L::kSAccReady), 1);
-    mbar_init(bar(L::kPSmem), 128);
-    mbar_init(bar(L::kSSmem), 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(L::kPReady + b), 1);
+      mbar_init(bar(L::kPFree + b), kEpilogueThreads);
+      mbar_init(bar(L::kPSmem + b), kEpilogueThreads);
+      mbar_init(bar(L::kOReady + b), 1);
+      mbar_init(bar(L::kOFree + b), kEpilogueThreads);
+    }
+    mbar_init(bar(L::kSSmem), kEpilogueThreads);
+    mbar_init(bar(L::kSAcc), 1);
+    mbar_init(bar(L::kSFree), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -158,53 +170,36 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       for (; i < n; ++i) {
         const WorkTile r = nxt;
         if (i + 1 < n) nxt = load_tile(list + i + 1);
-        const int s = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
         if (!wait_or_flag(bar(L::kEmpty + s), ph ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
         const uint32_t st = base + L::kStage0 + s * kStageBytes;
-        const bool first = r.flags & kTileFirst;
-        const bool ld_a = first && r.stateA >= 0, ld_b = first && r.stateB >= 0;
-        mbar_arrive_expect_tx(bar(L::kFull + s), 3 * kRowTileBytes + (ld_a ? kStateBytes : 0) +
-                                                      (ld_b ? kStateBytes : 0));
+        mbar_arrive_expect_tx(bar(L::kFull + s), kStageBytes);
         tma_load_3d(st + L::kQ, &tm_q, bar(L::kFull + s), 0, r.row0, r.head);
         tma_load_3d(st + L::kK, &tm_k, bar(L::kFull + s), 0, r.row0, r.head);
         tma_load_3d(st + L::kV, &tm_v, bar(L::kFull + s), 0, r.row0, r.head);
-        if (ld_a)
-          bulk_copy_g2s(st + L::kSA, stateA + (static_cast<int64_t>(r.stateA) * H + r.head) * kStateFloats,
-                        kStateBytes, bar(L::kFull + s));
-        if (ld_b)
-          bulk_copy_g2s(st + L::kSB, stateB + (static_cast<int64_t>(r.stateB) * H + r.head) * kStateFloats,
-                        kStateBytes, bar(L::kFull + s));
       }
       // Wait (bounded) for the last loads to land before the CTA can exit.
       for (int u = (i > kStages ? i - kStages : 0); u < i; ++u)
-        mbar_wait_bounded(bar(L::kFull + (u & 1)), (u >> 1) & 1, ok ? kWaitLimitNs : 1000000ull);
+        mbar_wait_bounded(bar(L::kFull + u % kStages), (u / kStages) & 1, ok ? kWaitLimitNs : 1000000ull);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    bool ok = true;
+    // ------------------------------------------------------------ P issuer
     constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t id_n64_b_mn = idesc_bf16_f32(128, 64, 0, 1);
-    constexpr uint32_t id_kv = idesc_bf16_f32(128, 64, 1, 1);
     WorkTile nxt = n > 0 ? load_tile(list) : WorkTile{};
-    for (int i = 0; i < n && ok; ++i) {
+    for (int i = 0; i < n; ++i) {
       const WorkTile r = nxt;
       if (i + 1 < n) nxt = load_tile(list + i + 1);
-      const int s = i & 1, b = i & 1;
-      const uint32_t ph = (i >> 1) & 1;
+      const int s = i % kStages, b = i & 1;
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kFull + s), (i / kStages) & 1, err, kErrTimeoutTma)))
+        break;
       const uint32_t st = base + L::kStage0 + s * kStageBytes;
-      const uint32_t sq = st + L::kQ, sk = st + L::kK, sv = st + L::kV;
-      const uint32_t colP = b ? kColP1 : kColP0, colO = b ? kColO1 : kColO0;
-      const bool first = r.flags & kTileFirst, last = r.flags & kTileLast;
-      const bool has_state = !first || (r.flags & kTileHasInit);
-
-      ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kFull + s), ph, err, kErrTimeoutTma));
-      if (!ok) break;
       if (r.nrows < kTileRows) {
         // K and V rows past the tile may hold anything, even NaN; zero them so
-        // masked P entries and the state update multiply zeros.
-        uint8_t* vrow = smem + (sv - base);
-        uint8_t* krow = smem + (sk - base);
+        // masked P entries multiply zeros.  (A partial tile is the last of its
+        // item, so no state update reads them.)
+        uint8_t* vrow = smem + (st + L::kV - base);
+        uint8_t* krow = smem + (st + L::kK - base);
         for (int q = r.nrows * 8 + lane; q < kTileRows * 8; q += 32) {
           *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0u, 0u, 0u, 0u);
           *reinterpret_cast<uint4*>(krow + q * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -212,49 +207,71 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (i >= 2) ok = wait_or_flag(bar(L::kTmemFree + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+      bool ok = true;
+      if (i >= 2) ok = wait_or_flag(bar(L::kPFree + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after_sync();
       if (lane == 0) {
+        const uint32_t colP = b ? kColP1 : kColP0;
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          mma_bf16(tmem + colP, smem_desc_sw128(sq + kk * 32, 16, 1024),
-                   smem_desc_sw128(sk + kk * 32, 16, 1024), id_qk, kk > 0);
+          mma_bf16(tmem + colP, smem_desc_sw128(st + L::kQ + kk * 32, 16, 1024),
+                   smem_desc_sw128(st + L::kK + kk * 32, 16, 1024), id_qk, kk > 0);
         mma_commit(bar(L::kPReady + b));
       }
       __syncwarp();
-      // S of this tile (staged by the epilogue) -> O_b = Q S, and the state
-      // update for the next tile of the item.
-      ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kSSmem), i & 1, err, kErrTimeoutMma));
-      if (!ok) break;
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ O issuer
+    constexpr uint32_t id_n64_b_mn = idesc_bf16_f32(128, 64, 0, 1);
+    constexpr uint32_t id_kv = idesc_bf16_f32(128, 64, 1, 1);
+    WorkTile nxt = n > 0 ? load_tile(list) : WorkTile{};
+    for (int i = 0; i < n; ++i) {
+      const WorkTile r = nxt;
+      if (i + 1 < n) nxt = load_tile(list + i + 1);
+      const int s = i % kStages, b = i & 1;
+      const uint32_t st = base + L::kStage0 + s * kStageBytes;
+      const bool first = r.flags & kTileFirst, last = r.flags & kTileLast;
+      const bool has_state = !first || (r.flags & kTileHasInit);
+      const uint32_t colO = b ? kColO1 : kColO0;
+      // Q, K, V of tile i, S(i) staged, O buffer free.
+      bool ok = wait_or_flag(bar(L::kFull + s), (i / kStages) & 1, err, kErrTimeoutTma);
+      if (ok) ok = wait_or_flag(bar(L::kSSmem), i & 1, err, kErrTimeoutMma);
+      if (ok && i >= 2) ok = wait_or_flag(bar(L::kOFree + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after_sync();
       if (lane == 0) {
         if (has_state) {
           int m = 0;
           for (int kk = 0; kk < kHeadDim / 16; ++kk)
             for (int part = 0; part < 2; ++part, ++m)
-              mma_bf16(tmem + colO, smem_desc_sw128(sq + kk * 32, 16, 1024),
+              mma_bf16(tmem + colO, smem_desc_sw128(st + L::kQ + kk * 32, 16, 1024),
                        smem_desc_sw128(base + L::kS + part * kStateTileBytes + kk * 2048,
                                        kStateTileBytes, 1024),
                        id_n64_b_mn, m > 0);
         }
         if (!last) {
+          // S (+)= K^T V: on top of the start state the epilogue wrote into
+          // the state columns, or a fresh sum for an item without one.
           for (int kk = 0; kk < kTileRows / 16; ++kk)
-            mma_bf16(tmem + kColS, smem_desc_sw128(sk + kk * 2048, kRowTileBytes, 1024),
-                     smem_desc_sw128(sv + kk * 2048, kRowTileBytes, 1024), id_kv,
-                     (!first || kk > 0) ? 1u : 0u);
-          mma_commit(bar(L::kSAccReady));
+            mma_bf16(tmem + kColS, smem_desc_sw128(st + L::kK + kk * 2048, kRowTileBytes, 1024),
+                     smem_desc_sw128(st + L::kV + kk * 2048, kRowTileBytes, 1024), id_kv,
+                     (has_state || kk > 0) ? 1u : 0u);
+          mma_commit(bar(L::kSAcc));
+        } else if (i + 1 < n) {
+          mma_commit(bar(L::kSFree));   // the next item may overwrite S
         }
       }
       __syncwarp();
-      ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kPSmem), i & 1, err, kErrTimeoutMma));
-      if (!ok) break;
+      // P(i) in shared memory: O(i) += P(i) V(i); release the stage.
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kPSmem + b), (i >> 1) & 1, err, kErrTimeoutMma)))
+        break;
       tc_fence_after_sync();
       if (lane == 0) {
+        const uint32_t pbuf = base + L::kP + b * kPBufBytes;
         for (int kk = 0; kk < kTileRows / 16; ++kk)
           mma_bf16(tmem + colO,
-                   smem_desc_sw128(base + L::kP + (kk >> 2) * kRowTileBytes + (kk & 3) * 32, 16, 1024),
-                   smem_desc_sw128(sv + kk * 2048, kRowTileBytes, 1024), id_n64_b_mn,
+                   smem_desc_sw128(pbuf + (kk >> 2) * kRowTileBytes + (kk & 3) * 32, 16, 1024),
+                   smem_desc_sw128(st + L::kV + kk * 2048, kRowTileBytes, 1024), id_n64_b_mn,
                    (has_state || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::kOReady + b));
         mma_commit(bar(L::kEmpty + s));
@@ -264,57 +281,67 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
+    const int half = (warp - 3) >> 2;             // which half of the columns
     const int row = quarter * 32 + lane;          // tile row = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const bool state_rows = quarter < 2;          // lanes 0..63 hold state rows
-    uint32_t sacc = 0;
-    bool ok = true;
-    float s_init[64];
-    WorkTile nxt = n > 0 ? load_tile(list) : WorkTile{};
-    for (int i = 0; i < n && ok; ++i) {
-      const WorkTile r = nxt;
-      if (i + 1 < n) nxt = load_tile(list + i + 1);
-      const int s = i & 1, b = i & 1;
-      const uint32_t ph = (i >> 1) & 1;
-      const uint32_t colP = b ? kColP1 : kColP0, colO = b ? kColO1 : kColO0;
-      const bool first = r.flags & kTileFirst, last = r.flags & kTileLast;
+    uint32_t sacc = 0, sfree = 0;
+    float s_next[32];                             // next item's start state (row, half)
 
-      if (first) {
-        // The item's start state (landed with the stage) -> S operand.
-        const bool has_init = r.flags & kTileHasInit;
-        if (has_init) {
-          ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kFull + s), ph, err, kErrTimeoutTma));
-          if (!ok) break;
+    // Load the start state of the item starting at tile record `r` (state rows only).
+    auto fetch_state = [&](const WorkTile& r) {
+      float* x = s_next;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] = 0.f;
+      if (!state_rows) return;
+      if (r.stateA >= 0) {
+        const float4* a = reinterpret_cast<const float4*>(
+            stateA + ((static_cast<int64_t>(r.stateA) * H + r.head) * kHeadDim + row) * kHeadDim) + half * 8;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 v4 = __ldcg(a + c);
+          x[4 * c] += v4.x; x[4 * c + 1] += v4.y; x[4 * c + 2] += v4.z; x[4 * c + 3] += v4.w;
         }
-        if (state_rows) {
-          const uint8_t* st = smem + L::kStage0 + s * kStageBytes;
-#pragma unroll
-          for (int e = 0; e < 64; ++e) s_init[e] = 0.f;
-          if (r.stateA >= 0) {
-            const float4* a = reinterpret_cast<const float4*>(st + L::kSA) + row * 16;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const float4 x = a[c];
-              s_init[4 * c] += x.x; s_init[4 * c + 1] += x.y;
-              s_init[4 * c + 2] += x.z; s_init[4 * c + 3] += x.w;
-            }
-          }
-          if (r.stateB >= 0) {
-            const float4* bb = reinterpret_cast<const float4*>(st + L::kSB) + row * 16;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const float4 x = bb[c];
-              s_init[4 * c] += x.x; s_init[4 * c + 1] += x.y;
-              s_init[4 * c + 2] += x.z; s_init[4 * c + 3] += x.w;
-            }
-          }
-          if (has_init) stage_state_row(smem + L::kS, row, s_init);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bar(L::kSSmem));
       }
+      if (r.stateB >= 0) {
+        const float4* bb = reinterpret_cast<const float4*>(
+            stateB + ((static_cast<int64_t>(r.stateB) * H + r.head) * kHeadDim + row) * kHeadDim) + half * 8;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 v4 = __ldcg(bb + c);
+          x[4 * c] += v4.x; x[4 * c + 1] += v4.y; x[4 * c + 2] += v4.z; x[4 * c + 3] += v4.w;
+        }
+      }
+    };
 
-      // Segment start of this row inside the tile.
+    // First tile of an item: its start state -> S operand (after the previous
+    // tile's Q S has read the operand) and, when the item has more tiles, into
+    // the TMEM state columns the state updates accumulate on.
+    auto stage_first = [&](int i, const WorkTile& r) -> bool {
+      if (i > 0) {
+        const bool ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kSFree), sfree & 1, err, kErrTimeoutMma));
+        ++sfree;
+        if (!ok) return false;
+      }
+      if (state_rows && (r.flags & kTileHasInit)) {
+        stage_state_half_row(smem + L::kS, row, half, s_next);
+        if (!(r.flags & kTileLast)) {
+          uint32_t u[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(s_next[e]);
+          tmem_st_32cols(tmem + lane_base + kColS + half * 32, u);
+          tmem_st_wait();
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kSSmem));
+      return true;
+    };
+
+    // P(i) -> mask -> bf16 -> P buffer (i & 1), this thread's row and half.
+    auto p_work = [&](int i, const WorkTile& r) -> bool {
+      const int b = i & 1;
       int seg_start = 0;
       if (r.nbound > 1) {
         const int nb = r.nbound < kInlineBounds ? r.nbound : kInlineBounds;
@@ -325,88 +352,119 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           if (sb <= row) seg_start = sb;
         }
       }
-
-      // P row -> mask -> bf16 -> K-major A operand of P V.
-      ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kPReady + b), ph, err, kErrTimeoutMma));
-      if (!ok) break;
+      const int hi_col = row < r.nrows ? row : -1;   // last kept column of this row
+      const int c0 = half * 64, c1 = half * 64 + 63;
+      // Warp-uniform shortcuts: this half-row block entirely kept or entirely masked.
+      const bool all_kept = __all_sync(0xffffffffu, seg_start <= c0 && c1 <= hi_col);
+      const bool all_zero = __all_sync(0xffffffffu, c0 > hi_col || c1 < seg_start);
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kPReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
+        return false;
       tc_fence_after_sync();
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
+      uint8_t* pbuf = smem + L::kP + b * kPBufBytes + half * kRowTileBytes;
+      if (all_zero) {
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kPFree + b));
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<uint4*>(pbuf + sw128_offset(row, g * 8)) = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        const uint32_t colP = b ? kColP1 : kColP0;
         uint32_t r0[32], r1[32];
         tmem_ld_32cols(tmem + lane_base + colP + half * 64, r0);
         tmem_ld_32cols(tmem + lane_base + colP + half * 64 + 32, r1);
         tmem_ld_wait();
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kPFree + b));
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const int j0 = half * 64 + g * 8;
+          const int j0 = c0 + g * 8;
           uint32_t pk[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int jj = j0 + 2 * u;
             const int ci = (g & 3) * 8 + 2 * u;
             float p0 = __uint_as_float(g < 4 ? r0[ci] : r1[ci]);
             float p1 = __uint_as_float(g < 4 ? r0[ci + 1] : r1[ci + 1]);
-            p0 = (jj >= seg_start && jj <= row && row < r.nrows) ? p0 : 0.f;
-            p1 = (jj + 1 >= seg_start && jj + 1 <= row && row < r.nrows) ? p1 : 0.f;
+            if (!all_kept) {
+              const int jj = j0 + 2 * u;
+              p0 = (jj >= seg_start && jj <= hi_col) ? p0 : 0.f;
+              p1 = (jj + 1 >= seg_start && jj + 1 <= hi_col) ? p1 : 0.f;
+            }
             pk[u] = pack_bf16x2(p0, p1);
           }
-          const uint32_t off = half * kRowTileBytes + sw128_offset(row, g * 8);
-          *reinterpret_cast<uint4*>(smem + L::kP + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(pbuf + sw128_offset(row, g * 8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
       fence_proxy_async_smem();
-      tc_fence_before_sync();
-      mbar_arrive(bar(L::kPSmem));
+      mbar_arrive(bar(L::kPSmem + b));
+      return true;
+    };
 
-      if (!last) {
-        // Next tile's state S + dS -> S operand.
-        ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kSAccReady), sacc & 1, err, kErrTimeoutMma));
-        ++sacc;
-        if (!ok) break;
-        tc_fence_after_sync();
-        if (state_rows) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_32cols(tmem + lane_base + kColS, r0);
-          tmem_ld_32cols(tmem + lane_base + kColS + 32, r1);
-          tmem_ld_wait();
-          float x[64];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            x[e] = s_init[e] + __uint_as_float(r0[e]);
-            x[e + 32] = s_init[e + 32] + __uint_as_float(r1[e]);
-          }
-          stage_state_row(smem + L::kS, row, x);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        mbar_arrive(bar(L::kSSmem));
-      }
-
-      // O row -> global.
-      ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + b), ph, err, kErrTimeoutMma));
-      if (!ok) break;
+    // Not the item's last tile: the running state S(i+1) -> S operand.
+    auto s_work = [&](const WorkTile& r) -> bool {
+      if (r.flags & kTileLast) return true;
+      const bool ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kSAcc), sacc & 1, err, kErrTimeoutMma));
+      ++sacc;
+      if (!ok) return false;
       tc_fence_after_sync();
-      uint32_t r0[32], r1[32];
-      tmem_ld_32cols(tmem + lane_base + colO, r0);
-      tmem_ld_32cols(tmem + lane_base + colO + 32, r1);
+      if (state_rows) {
+        uint32_t r0[32];
+        tmem_ld_32cols(tmem + lane_base + kColS + half * 32, r0);
+        tmem_ld_wait();
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r0[e]);
+        stage_state_half_row(smem + L::kS, row, half, x);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();   // the state was read before the next K^T V writes it
+      mbar_arrive(bar(L::kSSmem));
+      return true;
+    };
+
+    // O(i) -> global (rows of the tile only).
+    auto o_work = [&](int i, const WorkTile& r) -> bool {
+      const int b = i & 1;
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
+        return false;
+      tc_fence_after_sync();
+      const uint32_t colO = b ? kColO1 : kColO0;
+      uint32_t r0[32];
+      tmem_ld_32cols(tmem + lane_base + colO + half * 32, r0);
       tmem_ld_wait();
       tc_fence_before_sync();
-      mbar_arrive(bar(L::kTmemFree + b));
+      mbar_arrive(bar(L::kOFree + b));
       if (row < r.nrows) {
         uint4* dst = reinterpret_cast<uint4*>(
-            out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim);
+            out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim + half * 32);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           dst[c] = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c]), __uint_as_float(r0[8 * c + 1])),
                               pack_bf16x2(__uint_as_float(r0[8 * c + 2]), __uint_as_float(r0[8 * c + 3])),
                               pack_bf16x2(__uint_as_float(r0[8 * c + 4]), __uint_as_float(r0[8 * c + 5])),
                               pack_bf16x2(__uint_as_float(r0[8 * c + 6]), __uint_as_float(r0[8 * c + 7])));
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          dst[4 + c] = make_uint4(pack_bf16x2(__uint_as_float(r1[8 * c]), __uint_as_float(r1[8 * c + 1])),
-                                  pack_bf16x2(__uint_as_float(r1[8 * c + 2]), __uint_as_float(r1[8 * c + 3])),
-                                  pack_bf16x2(__uint_as_float(r1[8 * c + 4]), __uint_as_float(r1[8 * c + 5])),
-                                  pack_bf16x2(__uint_as_float(r1[8 * c + 6]), __uint_as_float(r1[8 * c + 7])));
+      }
+      return true;
+    };
+
+    if (n > 0) {
+      WorkTile cur = load_tile(list);
+      WorkTile nxt = n > 1 ? load_tile(list + 1) : WorkTile{};
+      fetch_state(cur);
+      bool ok = stage_first(0, cur);
+      if (n > 1 && (nxt.flags & kTileFirst)) fetch_state(nxt);
+      ok = ok && p_work(0, cur) && s_work(cur);
+      for (int i = 0; i < n && ok; ++i) {
+        WorkTile nxt2 = i + 2 < n ? load_tile(list + i + 2) : WorkTile{};
+        if (i + 1 < n) {
+          if (nxt.flags & kTileFirst) ok = stage_first(i + 1, nxt);
+          // s_next is free again: fetch the start state of tile i+2 if it
+          // begins an item.
+          if (ok && i + 2 < n && (nxt2.flags & kTileFirst)) fetch_state(nxt2);
+          ok = ok && p_work(i + 1, nxt) && s_work(nxt);
+        }
+        ok = ok && o_work(i, cur);
+        cur = nxt;
+        nxt = nxt2;
       }
     }
   }
