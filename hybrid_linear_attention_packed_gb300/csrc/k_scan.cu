@@ -11,8 +11,8 @@
 // fp32 adds on CUDA cores; the kernel is bound by memory traffic.  One CTA of
 // 128 threads owns a 512-float eighth of one (segment, head) state and walks
 // the segment's chunks in order, keeping the running sum in registers and
-// loading sixteen chunks ahead so the loads stay in flight while the stores
-// drain.
+// loading thirty-two chunks ahead so the loads stay in flight while the
+// stores drain.
 #include "spanla_internal.h"
 #include "tc_ptx.cuh"
 
@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kSlices = kStateFloats / (kThreads * 4);   // 8 CTAs per (segment, head)
-constexpr int kAhead = 16;
+constexpr int kAhead = 32;
 
 __device__ __forceinline__ float4 add4(float4 a, float4 b) {
   return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);

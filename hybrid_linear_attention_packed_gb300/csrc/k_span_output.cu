@@ -18,21 +18,24 @@
 //
 // Persistent CTAs (one per SM) walk a host-built list of tiles, software
 // pipelined over consecutive tiles t.  11 warps:
-//   warp 0     producer: Q, K, V tiles by TMA into a three-stage ring.
+//   warp 0     producer: Q, K, V tiles by TMA into a four-stage ring.
 //   warp 1     P issuer (one lane; the warp zeroes partial-tile K/V rows):
 //              P(t) = Q K^T  (M128 N128 K64) as soon as tile t has landed.
 //   warp 2     O issuer (one lane): once S(t) is staged,  O(t) = Q S_hi +
 //              Q S_lo  (M128 N64 K64) and the state update  S (+)= K^T V
-//              (M128 N64 K128); once P(t) is in shared memory,  O(t) +=
-//              P(t) V  (M128 N64 K128).  P and O have two TMEM buffers each
-//              (t & 1), so P of the next tiles is computed while O of this
-//              one is still being built.
+//              (M128 N64 K128); once the epilogue has turned P(t) into bf16
+//              in place,  O(t) += P(t) V  (M128 N64 K128) with P read from
+//              tensor memory.  P and O have two TMEM buffers each (t & 1),
+//              so P of the next tiles is computed while O of this one is
+//              still being built.
 //   warps 3-10 epilogue, two warps per TMEM lane quarter: each thread owns
 //              one tile row (TMEM lane) and half of its columns.  Per step t
 //              it stages S(t+1) (the next item's start state, fetched into
-//              registers a tile ahead, or the running state), turns P(t+1) into the
-//              masked bf16 A operand (double-buffered in shared memory), and
-//              only then stores O(t) -- so the tensor cores run ahead of it.
+//              registers a tile ahead, or the running state), turns P(t+1)
+//              into the masked bf16 A operand in place in tensor memory (the
+//              half-row of fp32 columns [64h, 64h+64) becomes bf16 pairs in
+//              columns [64h, 64h+32)), and only then stores O(t) -- so the
+//              tensor cores run ahead of it.
 // The running state of a span lives in TMEM: at the span's first tile the
 // epilogue writes the start state into the state columns, and every K^T V
 // accumulates on top of it.  K^T V uses both tiles MN-major with M = 128: the
@@ -46,11 +49,10 @@ namespace {
 
 constexpr int kThreads = 352;
 constexpr int kEpilogueThreads = 256;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr uint32_t kRowTileBytes = kTileRows * 128;        // 128 rows x 128 B
 constexpr uint32_t kStageBytes = 3 * kRowTileBytes;       // Q K V
 constexpr uint32_t kStateTileBytes = kHeadDim * 128;       // 64 rows x 128 B (bf16)
-constexpr uint32_t kPBufBytes = 2 * kRowTileBytes;         // [2 blocks][128][64] bf16
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: P buffers (128 each), O buffers (64 each), running state (64).
 constexpr uint32_t kColP0 = 0, kColP1 = 128, kColO0 = 256, kColO1 = 320, kColS = 384;
@@ -59,13 +61,12 @@ struct OutSmem {
   static constexpr uint32_t kStage0 = 0;
   static constexpr uint32_t kQ = 0, kK = kRowTileBytes, kV = 2 * kRowTileBytes;
   static constexpr uint32_t kS = kStages * kStageBytes;          // S hi, S lo (bf16)
-  static constexpr uint32_t kP = kS + 2 * kStateTileBytes;       // two P buffers
-  static constexpr uint32_t kBar = kP + 2 * kPBufBytes;
+  static constexpr uint32_t kBar = kS + 2 * kStateTileBytes;
   // barrier slots (8 bytes each)
   static constexpr int kFull = 0, kEmpty = kStages, kPReady = 2 * kStages,
-                       kPFree = kPReady + 2, kPSmem = kPReady + 4, kOReady = kPReady + 6,
-                       kOFree = kPReady + 8, kSSmem = kPReady + 10, kSAcc = kPReady + 11,
-                       kSFree = kPReady + 12, kNumBars = kPReady + 13;
+                       kPDone = kPReady + 2, kOReady = kPReady + 4, kOFree = kPReady + 6,
+                       kSSmem = kPReady + 8, kSAcc = kPReady + 9, kSFree = kPReady + 10,
+                       kNumBars = kPReady + 11;
   static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
   static constexpr uint32_t kBytes = kTmemSlot + 8;
   static constexpr uint32_t kRequest = kBytes + 1024;
@@ -134,8 +135,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::kPReady + b), 1);
-      mbar_init(bar(L::kPFree + b), kEpilogueThreads);
-      mbar_init(bar(L::kPSmem + b), kEpilogueThreads);
+      mbar_init(bar(L::kPDone + b), kEpilogueThreads);
       mbar_init(bar(L::kOReady + b), 1);
       mbar_init(bar(L::kOFree + b), kEpilogueThreads);
     }
@@ -207,8 +207,9 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_proxy_async_smem();
       }
       __syncwarp();
+      // P buffer b is free once P V of tile i-2 (which read it) has completed.
       bool ok = true;
-      if (i >= 2) ok = wait_or_flag(bar(L::kPFree + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (i >= 2) ok = wait_or_flag(bar(L::kOReady + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after_sync();
       if (lane == 0) {
@@ -262,17 +263,16 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
       }
       __syncwarp();
-      // P(i) in shared memory: O(i) += P(i) V(i); release the stage.
-      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kPSmem + b), (i >> 1) & 1, err, kErrTimeoutMma)))
+      // P(i) is bf16 in TMEM: O(i) += P(i) V(i); release the stage.
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kPDone + b), (i >> 1) & 1, err, kErrTimeoutMma)))
         break;
       tc_fence_after_sync();
       if (lane == 0) {
-        const uint32_t pbuf = base + L::kP + b * kPBufBytes;
+        const uint32_t colP = b ? kColP1 : kColP0;
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16(tmem + colO,
-                   smem_desc_sw128(pbuf + (kk >> 2) * kRowTileBytes + (kk & 3) * 32, 16, 1024),
-                   smem_desc_sw128(st + L::kV + kk * 2048, kRowTileBytes, 1024), id_n64_b_mn,
-                   (has_state || kk > 0) ? 1u : 0u);
+          mma_bf16_tmem_a(tmem + colO, tmem + colP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                          smem_desc_sw128(st + L::kV + kk * 2048, kRowTileBytes, 1024),
+                          id_n64_b_mn, (has_state || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::kOReady + b));
         mma_commit(bar(L::kEmpty + s));
       }
@@ -360,42 +360,33 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kPReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
         return false;
       tc_fence_after_sync();
-      uint8_t* pbuf = smem + L::kP + b * kPBufBytes + half * kRowTileBytes;
+      const uint32_t colP = (b ? kColP1 : kColP0) + half * 64;
+      uint32_t pk[32];
       if (all_zero) {
-        tc_fence_before_sync();
-        mbar_arrive(bar(L::kPFree + b));
 #pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<uint4*>(pbuf + sw128_offset(row, g * 8)) = make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < 32; ++c) pk[c] = 0u;
       } else {
-        const uint32_t colP = b ? kColP1 : kColP0;
         uint32_t r0[32], r1[32];
-        tmem_ld_32cols(tmem + lane_base + colP + half * 64, r0);
-        tmem_ld_32cols(tmem + lane_base + colP + half * 64 + 32, r1);
+        tmem_ld_32cols(tmem + lane_base + colP, r0);
+        tmem_ld_32cols(tmem + lane_base + colP + 32, r1);
         tmem_ld_wait();
-        tc_fence_before_sync();
-        mbar_arrive(bar(L::kPFree + b));
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const int j0 = c0 + g * 8;
-          uint32_t pk[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int ci = (g & 3) * 8 + 2 * u;
-            float p0 = __uint_as_float(g < 4 ? r0[ci] : r1[ci]);
-            float p1 = __uint_as_float(g < 4 ? r0[ci + 1] : r1[ci + 1]);
-            if (!all_kept) {
-              const int jj = j0 + 2 * u;
-              p0 = (jj >= seg_start && jj <= hi_col) ? p0 : 0.f;
-              p1 = (jj + 1 >= seg_start && jj + 1 <= hi_col) ? p1 : 0.f;
-            }
-            pk[u] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < 32; ++c) {
+          const int jj = c0 + 2 * c;
+          float p0 = __uint_as_float(c < 16 ? r0[2 * c] : r1[2 * c - 32]);
+          float p1 = __uint_as_float(c < 16 ? r0[2 * c + 1] : r1[2 * c - 31]);
+          if (!all_kept) {
+            p0 = (jj >= seg_start && jj <= hi_col) ? p0 : 0.f;
+            p1 = (jj + 1 >= seg_start && jj + 1 <= hi_col) ? p1 : 0.f;
           }
-          *reinterpret_cast<uint4*>(pbuf + sw128_offset(row, g * 8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          pk[c] = pack_bf16x2(p0, p1);
         }
       }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(L::kPSmem + b));
+      // bf16 pairs of this half-row replace the first 32 of its 64 fp32 columns.
+      tmem_st_32cols(tmem + lane_base + colP, pk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kPDone + b));
       return true;
     };
 

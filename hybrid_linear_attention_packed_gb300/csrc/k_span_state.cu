@@ -7,14 +7,19 @@
 // that follows (one scan for every view of the pass) moves one state per span
 // instead of one per chunk.
 //
-// One CTA (128 threads) handles one span for two adjacent heads h0, h0+1.  A
-// three-stage TMA ring brings K and V of both heads in 64-row chunks
-// ([head][64 rows][64 d] bf16, 128-byte swizzle).  Both operands of K^T V are
-// MN-major (the contraction runs over tokens, the row dimension):
-//   A (M = 128) = [K_h0 | K_h1]^T, B (N = 64) = V_h,
-// so TMEM columns 64h..64h+63 accumulate [K_h0^T V_h ; K_h1^T V_h] and lanes
-// 64h..64h+63 of them hold the wanted K_h^T V_h.  Rows of the last chunk past
-// the span's end are zeroed in shared memory before its MMAs.
+// Persistent CTAs (one per SM) walk the (span, head) units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ... (heads fastest, so CTAs reading the same rows
+// run together).  4 warps:
+//   warp 2     producer: K and V of one head, 128 rows (two chunks) at a
+//              time ([128 rows][64 d] bf16, 128-byte swizzle), into a
+//              six-stage ring, running ahead across units.
+//   warp 3     MMA issuer: per 128 rows 8 MMAs  acc (+)= K^T V  with both
+//              operands MN-major (the contraction runs over tokens): A (M =
+//              128) = [K | V]^T -- the V tile is the second 64-wide M atom and
+//              only TMEM lanes 0..63 (K^T V) are kept -- and B (N = 64) = V.
+//              Two TMEM accumulators alternate between units.  The warp
+//              zeroes rows past a segment's end in a partial last chunk.
+//   warps 0-1  epilogue: TMEM lanes 0..63 (state rows) -> fp32 state slot.
 #include "spanla_internal.h"
 #include "tc_ptx.cuh"
 
@@ -22,25 +27,32 @@ namespace spanla {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kStages = 3;
-constexpr uint32_t kHeadTileBytes = kChunk * 128;                     // 64 rows x 128 B
-constexpr uint32_t kOperandBytes = kChunkBoxHeads * kHeadTileBytes;   // 16 KiB (2 heads)
-constexpr uint32_t kStageBytes = 2 * kOperandBytes;                   // K + V
-constexpr uint32_t kTmemCols = 128;
+constexpr int kStages = 6;
+constexpr int kRows = 2 * kChunk;                        // rows per stage
+constexpr uint32_t kTileBytes = kRows * 128;             // 128 rows x 128 B (one head)
+constexpr uint32_t kStageBytes = 2 * kTileBytes;         // K, V
+constexpr uint32_t kTmemCols = 128;                      // two 64-column accumulators
 
 struct SpanSmem {
   static constexpr uint32_t kStage0 = 0;
-  static constexpr uint32_t kBarFull = kStages * kStageBytes;
-  static constexpr uint32_t kBarEmpty = kBarFull + 8 * kStages;
-  static constexpr uint32_t kBarDone = kBarEmpty + 8 * kStages;
-  static constexpr uint32_t kTmemSlot = kBarDone + 8;
+  static constexpr uint32_t kBar = kStages * kStageBytes;
+  static constexpr int kFull = 0, kEmpty = kStages, kAccReady = 2 * kStages,
+                       kAccFree = 2 * kStages + 2, kNumBars = 2 * kStages + 4;
+  static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
   static constexpr uint32_t kBytes = kTmemSlot + 8;
   static constexpr uint32_t kRequest = kBytes + 1024;
 };
 
-__global__ void __launch_bounds__(kThreads)
+__device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity, unsigned* err,
+                                             unsigned code) {
+  if (mbar_wait_bounded(bar, parity, kWaitLimitNs)) return true;
+  atomicOr(err, code);
+  return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
 span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const SpanDesc* __restrict__ spans, int H, float* __restrict__ ws,
+                  const SpanDesc* __restrict__ spans, int n_spans, int H, float* __restrict__ ws,
                   unsigned* __restrict__ err) {
   using L = SpanSmem;
   extern __shared__ uint8_t smem_raw[];
@@ -50,19 +62,19 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  // One CTA per (span, head pair); head pairs vary fastest, so the CTAs
-  // reading the same rows run together.
-  const int pairs = (H + kChunkBoxHeads - 1) / kChunkBoxHeads;
-  const int span = blockIdx.x / pairs;
-  const int h0 = (blockIdx.x % pairs) * kChunkBoxHeads;
+  const int lane = tid & 31;
+  auto bar = [&](int slot) { return base + L::kBar + 8u * slot; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(base + L::kBarFull + 8 * s, 1);
-      mbar_init(base + L::kBarEmpty + 8 * s, 1);
+      mbar_init(bar(L::kFull + s), 1);
+      mbar_init(bar(L::kEmpty + s), 1);
     }
-    mbar_init(base + L::kBarDone, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(L::kAccReady + b), 1);
+      mbar_init(bar(L::kAccFree + b), 64);
+    }
     fence_mbar_init();
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -77,128 +89,105 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   const uint32_t tmem = *tmem_slot;
 
   griddep_wait();   // descriptors come from a copy earlier in the stream
-  const SpanDesc sd = spans[span];
-  const int n_chunks = (sd.len + kChunk - 1) / kChunk;
-  const int tail = sd.len - (n_chunks - 1) * kChunk;   // rows of the last chunk
+  const int64_t n_units = static_cast<int64_t>(n_spans) * H;
 
-  auto issue_load = [&](int c) {
-    const int s = c % kStages;
-    const uint32_t st = base + L::kStage0 + s * kStageBytes;
-    const uint32_t full = base + L::kBarFull + 8 * s;
-    mbar_arrive_expect_tx(full, kStageBytes);
-    tma_load_3d(st, &tm_k, full, 0, sd.row0 + c * kChunk, h0);
-    tma_load_3d(st + kOperandBytes, &tm_v, full, 0, sd.row0 + c * kChunk, h0);
-  };
-
-  // Thread 0 issues every load and MMA.  `issued` / `consumed` count chunks
-  // whose loads were issued / whose MMAs were issued (thread 0 only).
-  bool ok = true;
-  int issued = 0, consumed = 0;
-  if (tid == 0)
-    for (; issued < n_chunks && issued < kStages; ++issued) issue_load(issued);
-
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 64, /*a MN*/ 1, /*b MN*/ 1);
-  for (int c = 0; c < n_chunks; ++c) {
-    const int s = c % kStages;
-    const uint32_t ph = (c / kStages) & 1;
-    const uint32_t st = base + L::kStage0 + s * kStageBytes;
-    const uint32_t full = base + L::kBarFull + 8 * s;
-    const uint32_t empty = base + L::kBarEmpty + 8 * s;
-    const bool partial = (c == n_chunks - 1) && tail < kChunk;
-    if (partial) {
-      // Only the last chunk can be partial.  Thread 0 reaches this barrier
-      // after issuing the MMAs of every earlier chunk, so the stage's barrier
-      // is now in this chunk's phase.  Every thread then helps zero rows
-      // >= tail of the 4 head tiles of K and V.
-      ok = __syncthreads_and(ok);
-      if (ok) {
-        const bool got = mbar_wait_bounded(full, ph, kWaitLimitNs);
-        if (got) {
-          const int dead = kChunk - tail;
-          uint8_t* stage = smem + (st - base);
-          for (int r = tid; r < 4 * dead * 8; r += kThreads) {
-            const int piece = r & 7, idx = r >> 3;
-            const int tile = idx / dead, row = tail + idx % dead;
-            *reinterpret_cast<uint4*>(stage + tile * kHeadTileBytes + row * 128 + piece * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+  if (warp == 2) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int c = 0;   // running chunk count (ring position)
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const SpanDesc sd = spans[u / H];
+        const int h = static_cast<int>(u % H);
+        const int n_chunks = (sd.len + kRows - 1) / kRows;
+        for (int j = 0; j < n_chunks; ++j, ++c) {
+          const int s = c % kStages;
+          if (!wait_or_flag(bar(L::kEmpty + s), ((c / kStages) & 1) ^ 1, err, kErrTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = base + L::kStage0 + s * kStageBytes;
+          mbar_arrive_expect_tx(bar(L::kFull + s), kStageBytes);
+          tma_load_3d(st, &tm_k, bar(L::kFull + s), 0, sd.row0 + j * kRows, h);
+          tma_load_3d(st + kTileBytes, &tm_v, bar(L::kFull + s), 0, sd.row0 + j * kRows, h);
+        }
+      }
+      // Let the last loads land (bounded) before the CTA can exit.
+      for (int u = (c > kStages ? c - kStages : 0); u < c; ++u)
+        mbar_wait_bounded(bar(L::kFull + u % kStages), (u / kStages) & 1, ok ? kWaitLimitNs : 1000000ull);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 64, /*a MN*/ 1, /*b MN*/ 1);
+    int c = 0, k = 0;   // running chunk count, running unit count (of this CTA)
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++k) {
+      const SpanDesc sd = spans[u / H];
+      const int n_chunks = (sd.len + kRows - 1) / kRows;
+      const int b = k & 1;
+      if (k >= 2) ok = wait_or_flag(bar(L::kAccFree + b), ((k - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after_sync();
+      for (int j = 0; j < n_chunks; ++j, ++c) {
+        const int s = c % kStages;
+        ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kFull + s), (c / kStages) & 1, err, kErrTimeoutTma));
+        if (!ok) break;
+        const uint32_t st = base + L::kStage0 + s * kStageBytes;
+        const int rows = sd.len - j * kRows;
+        if (rows < kRows) {
+          // Rows past the span's end belong to other segments: zero them in K and V.
+          uint8_t* kt = smem + (st - base);
+          for (int q = rows * 8 + lane; q < kRows * 8; q += 32) {
+            *reinterpret_cast<uint4*>(kt + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(kt + kTileBytes + q * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
-        } else {
-          atomicOr(err, kErrTimeoutTma);
         }
-        ok = __syncthreads_and(got);
-      }
-    }
-    if (tid == 0 && ok) {
-      if (!partial && !mbar_wait_bounded(full, ph, kWaitLimitNs)) {
-        atomicOr(err, kErrTimeoutTma);
-        ok = false;
-      }
-      if (ok) {
+        __syncwarp();
         tc_fence_after_sync();
-        for (int hh = 0; hh < kChunkBoxHeads; ++hh) {
-          for (int kk = 0; kk < kChunk / 16; ++kk) {
-            const uint64_t a = smem_desc_sw128(st + kk * 2048, kHeadTileBytes, 1024);
-            const uint64_t b = smem_desc_sw128(st + kOperandBytes + hh * kHeadTileBytes + kk * 2048,
-                                               kHeadTileBytes, 1024);
-            mma_bf16(tmem + hh * 64, a, b, idesc, (c > 0 || kk > 0) ? 1u : 0u);
-          }
+        if (lane == 0) {
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            mma_bf16(tmem + b * 64, smem_desc_sw128(st + kk * 2048, kTileBytes, 1024),
+                     smem_desc_sw128(st + kTileBytes + kk * 2048, kTileBytes, 1024), idesc,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(L::kEmpty + s));
+          if (j + 1 == n_chunks) mma_commit(bar(L::kAccReady + b));
         }
-        mma_commit(empty);
-        consumed = c + 1;
-        if (issued < n_chunks) {
-          // The stage is reloaded once the MMAs reading it have completed.
-          if (!mbar_wait_bounded(empty, ph, kWaitLimitNs)) {
-            atomicOr(err, kErrTimeoutMma);
-            ok = false;
-          } else {
-            issue_load(issued++);
-          }
-        }
+        __syncwarp();
       }
     }
-  }
-  if (tid == 0) {
-    if (ok) {
-      mma_commit(base + L::kBarDone);
-    } else {
-      // Give up: let the loads still in flight land (bounded) before the
-      // CTA's shared memory is released.
-      for (int c = consumed; c < issued; ++c)
-        mbar_wait_bounded(base + L::kBarFull + 8 * (c % kStages), (c / kStages) & 1, 1000000ull);
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0, 1)
+    const int d = warp * 32 + lane;   // state row = TMEM lane (0..63)
+    int k = 0;
+    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
+      const int b = k & 1;
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kAccReady + b), (k >> 1) & 1, err, kErrTimeoutMma)))
+        break;
+      tc_fence_after_sync();
+      uint32_t r0[32], r1[32];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * 64;
+      tmem_ld_32cols(taddr, r0);
+      tmem_ld_32cols(taddr + 32, r1);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kAccFree + b));
+      float4* dst = reinterpret_cast<float4*>(ws + (u * kHeadDim + d) * kHeadDim);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
+                             __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
+                                 __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
     }
   }
+
   griddep_launch_dependents();
-  ok = __syncthreads_and(ok);
-
-  if (ok) {
-    const bool done = mbar_wait_bounded(base + L::kBarDone, 0, kWaitLimitNs);
-    if (!done) atomicOr(err, kErrTimeoutMma);
-    tc_fence_after_sync();
-    const int hh = warp >> 1;
-    const int h = h0 + hh;
-    const int i = tid - hh * 64;
-    uint32_t r0[32], r1[32];
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + hh * 64;
-    tmem_ld_32cols(taddr, r0);
-    tmem_ld_32cols(taddr + 32, r1);
-    tmem_ld_wait();
-    if (done && h < H) {
-      float4* dst = reinterpret_cast<float4*>(
-          ws + ((static_cast<int64_t>(span) * H + h) * kHeadDim + i) * kHeadDim);
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        dst[c] = make_float4(__uint_as_float(r0[4 * c]), __uint_as_float(r0[4 * c + 1]),
-                             __uint_as_float(r0[4 * c + 2]), __uint_as_float(r0[4 * c + 3]));
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        dst[8 + c] = make_float4(__uint_as_float(r1[4 * c]), __uint_as_float(r1[4 * c + 1]),
-                                 __uint_as_float(r1[4 * c + 2]), __uint_as_float(r1[4 * c + 3]));
-    }
-  }
-
   tc_fence_before_sync();
   __syncthreads();
+  tc_fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -206,16 +195,13 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
 cudaError_t launch_span_state(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                               const SpanDesc* spans, int n_spans, int H, float* ws,
-                              unsigned* err, cudaStream_t stream) {
-  if (n_spans <= 0) return cudaSuccess;
-  const int64_t ctas = static_cast<int64_t>(n_spans) * ((H + kChunkBoxHeads - 1) / kChunkBoxHeads);
-  if (ctas > INT32_MAX) return cudaErrorInvalidConfiguration;
-  const dim3 grid(static_cast<unsigned>(ctas));
+                              int grid, unsigned* err, cudaStream_t stream) {
+  if (n_spans <= 0 || grid <= 0) return cudaSuccess;
   const uint32_t bytes = SpanSmem::kRequest;
   cudaError_t e =
       cudaFuncSetAttribute(span_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  span_state_kernel<<<grid, kThreads, bytes, stream>>>(tm_k[0], tm_v[0], spans, H, ws, err);
+  span_state_kernel<<<grid, kThreads, bytes, stream>>>(tm_k[0], tm_v[0], spans, n_spans, H, ws, err);
   return cudaGetLastError();
 }
 

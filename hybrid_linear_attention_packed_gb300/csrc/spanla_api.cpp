@@ -519,7 +519,11 @@ span_la_status run_plan(const Plan& plan, const void* q, const void* k, const vo
         CUtensorMap* tm = t == 0 ? &tile_ops.q[p] : t == 1 ? &tile_ops.k[p] : &tile_ops.v[p];
         CUtensorMap* cm = t == 0 ? &chunk_ops.q[p] : t == 1 ? &chunk_ops.k[p] : &chunk_ops.v[p];
         st = encode_map(tm, parts[t][p], T, H, kTileBoxRows, 1);
-        if (st == SPAN_LA_OK && t > 0) st = encode_map(cm, parts[t][p], T, H, kChunkBoxRows, kChunkBoxHeads);
+        // K and V boxes of the state kernel: 64 rows of two heads (chunk
+        // mode) or of one head (span mode).
+        if (st == SPAN_LA_OK && t > 0)
+          st = plan.span_mode ? encode_map(cm, parts[t][p], T, H, kSpanBoxRows, 1)
+                              : encode_map(cm, parts[t][p], T, H, kChunkBoxRows, kChunkBoxHeads);
       }
     }
     if (st != SPAN_LA_OK) break;
@@ -529,9 +533,12 @@ span_la_status run_plan(const Plan& plan, const void* q, const void* k, const vo
     if (plan.state_slots() > 0) {
       e = plan.span_mode
               ? counted_launch(kKernelSpanState, stream, [&] {
+                  const int grid = static_cast<int>(std::min<int64_t>(
+                      static_cast<int64_t>(plan.spans.size()) * H, dev->num_sms));
                   return launch_span_state(chunk_ops.k, chunk_ops.v,
                                            reinterpret_cast<const SpanDesc*>(ws + off_a),
-                                           static_cast<int>(plan.spans.size()), H, states, dev->err, stream);
+                                           static_cast<int>(plan.spans.size()), H, states, grid,
+                                           dev->err, stream);
                 })
               : counted_launch(kKernelChunk, stream, [&] {
                   return launch_chunk_state(split, chunk_ops.k, chunk_ops.v,
@@ -830,14 +837,15 @@ span_la_status span_la_pass_noalloc(const void* q, const void* k, const void* v,
     CUtensorMap* tm = t == 0 ? &tile_ops.q[0] : t == 1 ? &tile_ops.k[0] : &tile_ops.v[0];
     CUtensorMap* cm = t == 0 ? &chunk_ops.q[0] : t == 1 ? &chunk_ops.k[0] : &chunk_ops.v[0];
     if ((st = encode_map(tm, ops[t], T, H, kTileBoxRows, 1)) != SPAN_LA_OK) return st;
-    if (t > 0 && (st = encode_map(cm, ops[t], T, H, kChunkBoxRows, kChunkBoxHeads)) != SPAN_LA_OK) return st;
+    if (t > 0 && (st = encode_map(cm, ops[t], T, H, kSpanBoxRows, 1)) != SPAN_LA_OK) return st;
   }
   float* states = reinterpret_cast<float*>(ws + off_states);
   bool kernel_before = false;
   if (plan.state_slots() > 0) {
     e = counted_launch(kKernelSpanState, stream, [&] {
+      const int sgrid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(plan.spans.size()) * H, num_sms));
       return launch_span_state(chunk_ops.k, chunk_ops.v, reinterpret_cast<const SpanDesc*>(ws + off_spans),
-                               static_cast<int>(plan.spans.size()), H, states, err, stream);
+                               static_cast<int>(plan.spans.size()), H, states, sgrid, err, stream);
     });
     if (e != cudaSuccess) return cuda_fail(e, "span-state launch");
     kernel_before = true;

@@ -110,7 +110,7 @@ cudaError_t launch_scan(const ScanDesc* scan, int n_scan, int H, float* ws, floa
 
 cudaError_t launch_span_state(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                               const SpanDesc* spans, int n_spans, int H, float* ws,
-                              unsigned* err, cudaStream_t stream);
+                              int grid, unsigned* err, cudaStream_t stream);
 
 cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                const CUtensorMap* tm_v, const WorkTile* work,
@@ -136,6 +136,7 @@ cudaError_t noalloc_scratch(uint8_t** scratch, unsigned** err);
 // Box sizes of the TMA descriptors each kernel expects.
 constexpr int kChunkBoxRows = kChunk;     // chunk-state kernel: 64 rows x 2 heads
 constexpr int kChunkBoxHeads = 2;
+constexpr int kSpanBoxRows = 2 * kChunk;  // span-state kernel: 128 rows x 1 head
 constexpr int kTileBoxRows = kTileRows;   // tile-output kernel: 128 rows x 1 head
 
 }  // namespace spanla
