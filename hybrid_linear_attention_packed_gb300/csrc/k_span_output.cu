@@ -28,14 +28,14 @@
 //              tensor memory.  P and O have two TMEM buffers each (t & 1),
 //              so P of the next tiles is computed while O of this one is
 //              still being built.
-//   warps 3-10 epilogue, two warps per TMEM lane quarter: each thread owns
-//              one tile row (TMEM lane) and half of its columns.  Per step t
-//              it stages S(t+1) (the next item's start state, fetched into
-//              registers a tile ahead, or the running state), turns P(t+1)
-//              into the masked bf16 A operand in place in tensor memory (the
-//              half-row of fp32 columns [64h, 64h+64) becomes bf16 pairs in
-//              columns [64h, 64h+32)), and only then stores O(t) -- so the
-//              tensor cores run ahead of it.
+//   warps 3-6  P conversion, one warp per TMEM lane quarter: each thread owns
+//              one tile row (TMEM lane) and turns P(t) into the masked bf16
+//              A operand in place in tensor memory -- the 128 fp32 columns of
+//              its row become 128 bf16 in the first 64 columns.
+//   warps 7-10 state and output, one warp per lane quarter: per step t they
+//              stage S(t+1) (the next item's start state, fetched into
+//              registers a tile ahead, or the running state) and only then
+//              store O(t), so the tensor cores run ahead of them.
 // The running state of a span lives in TMEM: at the span's first tile the
 // epilogue writes the start state into the state columns, and every K^T V
 // accumulates on top of it.  K^T V uses both tiles MN-major with M = 128: the
@@ -48,7 +48,8 @@ namespace spanla {
 namespace {
 
 constexpr int kThreads = 352;
-constexpr int kEpilogueThreads = 256;
+constexpr int kGroupWarps = 4;                           // P conversion; state and output
+constexpr int kGroupThreads = 32 * kGroupWarps;
 constexpr int kStages = 4;
 constexpr uint32_t kRowTileBytes = kTileRows * 128;        // 128 rows x 128 B
 constexpr uint32_t kStageBytes = 3 * kRowTileBytes;       // Q K V
@@ -135,11 +136,11 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::kPReady + b), 1);
-      mbar_init(bar(L::kPDone + b), kEpilogueThreads);
+      mbar_init(bar(L::kPDone + b), kGroupThreads);
       mbar_init(bar(L::kOReady + b), 1);
-      mbar_init(bar(L::kOFree + b), kEpilogueThreads);
+      mbar_init(bar(L::kOFree + b), kGroupThreads);
     }
-    mbar_init(bar(L::kSSmem), kEpilogueThreads);
+    mbar_init(bar(L::kSSmem), kGroupThreads);
     mbar_init(bar(L::kSAcc), 1);
     mbar_init(bar(L::kSFree), 1);
     fence_mbar_init();
@@ -270,7 +271,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (lane == 0) {
         const uint32_t colP = b ? kColP1 : kColP0;
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_tmem_a(tmem + colO, tmem + colP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+          mma_bf16_tmem_a(tmem + colO, tmem + colP + kk * 8,
                           smem_desc_sw128(st + L::kV + kk * 2048, kRowTileBytes, 1024),
                           id_n64_b_mn, (has_state || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::kOReady + b));
@@ -278,36 +279,96 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       }
       __syncwarp();
     }
-  } else {
-    // ------------------------------------------------------------ epilogue
+  } else if (warp < 3 + kGroupWarps) {
+    // ------------------------------------------------------------ P conversion
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
-    const int half = (warp - 3) >> 2;             // which half of the columns
+    const int row = quarter * 32 + lane;          // tile row = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    WorkTile nxt = n > 0 ? load_tile(list) : WorkTile{};
+    for (int i = 0; i < n; ++i) {
+      const WorkTile r = nxt;
+      if (i + 1 < n) nxt = load_tile(list + i + 1);
+      const int b = i & 1;
+      int seg_start = 0;
+      if (r.nbound > 1) {
+        const int nb = r.nbound < kInlineBounds ? r.nbound : kInlineBounds;
+        for (int q = 1; q < nb; ++q)
+          if (r.inl[q] <= row) seg_start = r.inl[q];
+        for (int q = kInlineBounds; q < r.nbound; ++q) {
+          const int sb = bounds[r.bound0 + q];
+          if (sb <= row) seg_start = sb;
+        }
+      }
+      const int hi_col = row < r.nrows ? row : -1;   // last kept column of this row
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kPReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
+        break;
+      tc_fence_after_sync();
+      const uint32_t colP = b ? kColP1 : kColP0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c0 = h * 64, c1 = h * 64 + 63;
+        // Warp-uniform shortcuts: this half-row block entirely kept or entirely masked.
+        const bool all_kept = __all_sync(0xffffffffu, seg_start <= c0 && c1 <= hi_col);
+        const bool all_zero = __all_sync(0xffffffffu, c0 > hi_col || c1 < seg_start);
+        uint32_t pk[32];
+        if (all_zero) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = 0u;
+        } else {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32cols(tmem + lane_base + colP + c0, r0);
+          tmem_ld_32cols(tmem + lane_base + colP + c0 + 32, r1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int jj = c0 + 2 * c;
+            float p0 = __uint_as_float(c < 16 ? r0[2 * c] : r1[2 * c - 32]);
+            float p1 = __uint_as_float(c < 16 ? r0[2 * c + 1] : r1[2 * c - 31]);
+            if (!all_kept) {
+              p0 = (jj >= seg_start && jj <= hi_col) ? p0 : 0.f;
+              p1 = (jj + 1 >= seg_start && jj + 1 <= hi_col) ? p1 : 0.f;
+            }
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+        }
+        // bf16 pairs of columns [c0, c0+64) go to columns [c0/2, c0/2+32): the
+        // whole row of P ends up as 128 bf16 in the first 64 columns, all of
+        // them read (and converted) before any is overwritten.
+        tmem_st_32cols(tmem + lane_base + colP + 32 * h, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kPDone + b));
+    }
+  } else {
+    // ------------------------------------------------------------ state and output
+    const int quarter = warp & 3;                 // TMEM lane quarter of this warp
     const int row = quarter * 32 + lane;          // tile row = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const bool state_rows = quarter < 2;          // lanes 0..63 hold state rows
     uint32_t sacc = 0, sfree = 0;
-    float s_next[32];                             // next item's start state (row, half)
+    float s_next[kHeadDim];                       // next item's start state (this row)
 
     // Load the start state of the item starting at tile record `r` (state rows only).
     auto fetch_state = [&](const WorkTile& r) {
       float* x = s_next;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] = 0.f;
+      for (int e = 0; e < kHeadDim; ++e) x[e] = 0.f;
       if (!state_rows) return;
       if (r.stateA >= 0) {
         const float4* a = reinterpret_cast<const float4*>(
-            stateA + ((static_cast<int64_t>(r.stateA) * H + r.head) * kHeadDim + row) * kHeadDim) + half * 8;
+            stateA + ((static_cast<int64_t>(r.stateA) * H + r.head) * kHeadDim + row) * kHeadDim);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 16; ++c) {
           const float4 v4 = __ldcg(a + c);
           x[4 * c] += v4.x; x[4 * c + 1] += v4.y; x[4 * c + 2] += v4.z; x[4 * c + 3] += v4.w;
         }
       }
       if (r.stateB >= 0) {
         const float4* bb = reinterpret_cast<const float4*>(
-            stateB + ((static_cast<int64_t>(r.stateB) * H + r.head) * kHeadDim + row) * kHeadDim) + half * 8;
+            stateB + ((static_cast<int64_t>(r.stateB) * H + r.head) * kHeadDim + row) * kHeadDim);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 16; ++c) {
           const float4 v4 = __ldcg(bb + c);
           x[4 * c] += v4.x; x[4 * c + 1] += v4.y; x[4 * c + 2] += v4.z; x[4 * c + 3] += v4.w;
         }
@@ -324,12 +385,16 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (!ok) return false;
       }
       if (state_rows && (r.flags & kTileHasInit)) {
-        stage_state_half_row(smem + L::kS, row, half, s_next);
+        stage_state_half_row(smem + L::kS, row, 0, s_next);
+        stage_state_half_row(smem + L::kS, row, 1, s_next + 32);
         if (!(r.flags & kTileLast)) {
-          uint32_t u[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(s_next[e]);
-          tmem_st_32cols(tmem + lane_base + kColS + half * 32, u);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t u[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(s_next[32 * h + e]);
+            tmem_st_32cols(tmem + lane_base + kColS + 32 * h, u);
+          }
           tmem_st_wait();
         }
       }
@@ -339,72 +404,23 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       return true;
     };
 
-    // P(i) -> mask -> bf16 -> P buffer (i & 1), this thread's row and half.
-    auto p_work = [&](int i, const WorkTile& r) -> bool {
-      const int b = i & 1;
-      int seg_start = 0;
-      if (r.nbound > 1) {
-        const int nb = r.nbound < kInlineBounds ? r.nbound : kInlineBounds;
-        for (int q = 1; q < nb; ++q)
-          if (r.inl[q] <= row) seg_start = r.inl[q];
-        for (int q = kInlineBounds; q < r.nbound; ++q) {
-          const int sb = bounds[r.bound0 + q];
-          if (sb <= row) seg_start = sb;
-        }
-      }
-      const int hi_col = row < r.nrows ? row : -1;   // last kept column of this row
-      const int c0 = half * 64, c1 = half * 64 + 63;
-      // Warp-uniform shortcuts: this half-row block entirely kept or entirely masked.
-      const bool all_kept = __all_sync(0xffffffffu, seg_start <= c0 && c1 <= hi_col);
-      const bool all_zero = __all_sync(0xffffffffu, c0 > hi_col || c1 < seg_start);
-      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kPReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
-        return false;
-      tc_fence_after_sync();
-      const uint32_t colP = (b ? kColP1 : kColP0) + half * 64;
-      uint32_t pk[32];
-      if (all_zero) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = 0u;
-      } else {
-        uint32_t r0[32], r1[32];
-        tmem_ld_32cols(tmem + lane_base + colP, r0);
-        tmem_ld_32cols(tmem + lane_base + colP + 32, r1);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int jj = c0 + 2 * c;
-          float p0 = __uint_as_float(c < 16 ? r0[2 * c] : r1[2 * c - 32]);
-          float p1 = __uint_as_float(c < 16 ? r0[2 * c + 1] : r1[2 * c - 31]);
-          if (!all_kept) {
-            p0 = (jj >= seg_start && jj <= hi_col) ? p0 : 0.f;
-            p1 = (jj + 1 >= seg_start && jj + 1 <= hi_col) ? p1 : 0.f;
-          }
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-      }
-      // bf16 pairs of this half-row replace the first 32 of its 64 fp32 columns.
-      tmem_st_32cols(tmem + lane_base + colP, pk);
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(bar(L::kPDone + b));
-      return true;
-    };
-
-    // Not the item's last tile: the running state S(i+1) -> S operand.
-    auto s_work = [&](const WorkTile& r) -> bool {
-      if (r.flags & kTileLast) return true;
+    // Tile r is not its item's last: the running state after it -> S operand.
+    auto s_work = [&]() -> bool {
       const bool ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kSAcc), sacc & 1, err, kErrTimeoutMma));
       ++sacc;
       if (!ok) return false;
       tc_fence_after_sync();
       if (state_rows) {
-        uint32_t r0[32];
-        tmem_ld_32cols(tmem + lane_base + kColS + half * 32, r0);
-        tmem_ld_wait();
-        float x[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r0[e]);
-        stage_state_half_row(smem + L::kS, row, half, x);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r0[32];
+          tmem_ld_32cols(tmem + lane_base + kColS + 32 * h, r0);
+          tmem_ld_wait();
+          float x[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r0[e]);
+          stage_state_half_row(smem + L::kS, row, h, x);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();   // the state was read before the next K^T V writes it
@@ -419,20 +435,27 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         return false;
       tc_fence_after_sync();
       const uint32_t colO = b ? kColO1 : kColO0;
-      uint32_t r0[32];
-      tmem_ld_32cols(tmem + lane_base + colO + half * 32, r0);
+      uint32_t r0[32], r1[32];
+      tmem_ld_32cols(tmem + lane_base + colO, r0);
+      tmem_ld_32cols(tmem + lane_base + colO + 32, r1);
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(L::kOFree + b));
       if (row < r.nrows) {
         uint4* dst = reinterpret_cast<uint4*>(
-            out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim + half * 32);
+            out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           dst[c] = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c]), __uint_as_float(r0[8 * c + 1])),
                               pack_bf16x2(__uint_as_float(r0[8 * c + 2]), __uint_as_float(r0[8 * c + 3])),
                               pack_bf16x2(__uint_as_float(r0[8 * c + 4]), __uint_as_float(r0[8 * c + 5])),
                               pack_bf16x2(__uint_as_float(r0[8 * c + 6]), __uint_as_float(r0[8 * c + 7])));
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          dst[4 + c] = make_uint4(pack_bf16x2(__uint_as_float(r1[8 * c]), __uint_as_float(r1[8 * c + 1])),
+                                  pack_bf16x2(__uint_as_float(r1[8 * c + 2]), __uint_as_float(r1[8 * c + 3])),
+                                  pack_bf16x2(__uint_as_float(r1[8 * c + 4]), __uint_as_float(r1[8 * c + 5])),
+                                  pack_bf16x2(__uint_as_float(r1[8 * c + 6]), __uint_as_float(r1[8 * c + 7])));
       }
       return true;
     };
@@ -443,15 +466,15 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       fetch_state(cur);
       bool ok = stage_first(0, cur);
       if (n > 1 && (nxt.flags & kTileFirst)) fetch_state(nxt);
-      ok = ok && p_work(0, cur) && s_work(cur);
       for (int i = 0; i < n && ok; ++i) {
         WorkTile nxt2 = i + 2 < n ? load_tile(list + i + 2) : WorkTile{};
+        // S(i+1) first: the O issuer needs it right after P V of tile i.
         if (i + 1 < n) {
-          if (nxt.flags & kTileFirst) ok = stage_first(i + 1, nxt);
-          // s_next is free again: fetch the start state of tile i+2 if it
+          ok = (cur.flags & kTileLast) ? stage_first(i + 1, nxt) : s_work();
+          // s_next is free again (the current item's start state was staged
+          // at its first tile): fetch the start state of tile i+2 if it
           // begins an item.
           if (ok && i + 2 < n && (nxt2.flags & kTileFirst)) fetch_state(nxt2);
-          ok = ok && p_work(i + 1, nxt) && s_work(nxt);
         }
         ok = ok && o_work(i, cur);
         cur = nxt;
