@@ -21,13 +21,14 @@
 //   warp 0     producer: Q, K, V tiles by TMA into a four-stage ring.
 //   warp 1     P issuer (one lane; the warp zeroes partial-tile K/V rows):
 //              P(t) = Q K^T  (M128 N128 K64) as soon as tile t has landed.
-//   warp 2     O issuer (one lane): once S(t) is staged,  O(t) = Q S_hi +
-//              Q S_lo  (M128 N64 K64) and the state update  S (+)= K^T V
-//              (M128 N64 K128); once the epilogue has turned P(t) into bf16
-//              in place,  O(t) += P(t) V  (M128 N64 K128) with P read from
-//              tensor memory.  P and O have two TMEM buffers each (t & 1),
-//              so P of the next tiles is computed while O of this one is
-//              still being built.
+//   warp 2     O issuer (one lane), per tile in this order: (1) the state
+//              update  S (+)= K^T V  (M128 N64 K128) once the state columns
+//              have been read out; (2) once the P conversion has turned P(t)
+//              into bf16 in place,  O(t) = P(t) V  (M128 N64 K128) with P
+//              read from tensor memory; (3) once S(t) is staged,  O(t) +=
+//              Q S_hi + Q S_lo  (M128 N64 K64).  P and O have two TMEM
+//              buffers each and S two shared-memory operands (t & 1), so the
+//              next tiles proceed while this one is still being built.
 //   warps 3-6  P conversion, one warp per TMEM lane quarter: each thread owns
 //              one tile row (TMEM lane) and turns P(t) into the masked bf16
 //              A operand in place in tensor memory -- the 128 fp32 columns of
@@ -37,10 +38,11 @@
 //              registers a tile ahead, or the running state) and only then
 //              store O(t), so the tensor cores run ahead of them.
 // The running state of a span lives in TMEM: at the span's first tile the
-// epilogue writes the start state into the state columns, and every K^T V
-// accumulates on top of it.  K^T V uses both tiles MN-major with M = 128: the
-// second 64-wide M atom is the V tile, so TMEM lanes 64..127 of the state
-// columns are unused.
+// start state is written into the state columns, and every K^T V accumulates
+// on top of it.  K^T V runs with M = 128 and the K tile as both 64-wide M
+// atoms, so TMEM lanes 64..127 hold a copy of state rows 0..63: the lower
+// copy is read for columns 0..31, the upper for columns 32..63, and all four
+// state/output warps share the staging of S as bf16 high / low parts.
 #include "spanla_internal.h"
 #include "tc_ptx.cuh"
 
@@ -54,6 +56,7 @@ constexpr int kStages = 4;
 constexpr uint32_t kRowTileBytes = kTileRows * 128;        // 128 rows x 128 B
 constexpr uint32_t kStageBytes = 3 * kRowTileBytes;       // Q K V
 constexpr uint32_t kStateTileBytes = kHeadDim * 128;       // 64 rows x 128 B (bf16)
+constexpr uint32_t kSOpBytes = 2 * kStateTileBytes;         // S as bf16 hi + lo
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: P buffers (128 each), O buffers (64 each), running state (64).
 constexpr uint32_t kColP0 = 0, kColP1 = 128, kColO0 = 256, kColO1 = 320, kColS = 384;
@@ -61,13 +64,15 @@ constexpr uint32_t kColP0 = 0, kColP1 = 128, kColO0 = 256, kColO1 = 320, kColS =
 struct OutSmem {
   static constexpr uint32_t kStage0 = 0;
   static constexpr uint32_t kQ = 0, kK = kRowTileBytes, kV = 2 * kRowTileBytes;
-  static constexpr uint32_t kS = kStages * kStageBytes;          // S hi, S lo (bf16)
-  static constexpr uint32_t kBar = kS + 2 * kStateTileBytes;
-  // barrier slots (8 bytes each)
+  static constexpr uint32_t kS = kStages * kStageBytes;          // two S operands (hi, lo)
+  static constexpr uint32_t kBar = kS + 2 * kSOpBytes;
+  // barrier slots (8 bytes each).  Barriers that one side may complete again
+  // before the other has waited on them (a start state needs no wait before
+  // it is staged) come in pairs used by alternate tiles.
   static constexpr int kFull = 0, kEmpty = kStages, kPReady = 2 * kStages,
                        kPDone = kPReady + 2, kOReady = kPReady + 4, kOFree = kPReady + 6,
-                       kSSmem = kPReady + 8, kSAcc = kPReady + 9, kSFree = kPReady + 10,
-                       kNumBars = kPReady + 11;
+                       kSSmem = kPReady + 8, kSRead = kPReady + 10, kSAcc = kPReady + 12,
+                       kNumBars = kPReady + 13;
   static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
   static constexpr uint32_t kBytes = kTmemSlot + 8;
   static constexpr uint32_t kRequest = kBytes + 1024;
@@ -141,8 +146,10 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_init(bar(L::kOFree + b), kGroupThreads);
     }
     mbar_init(bar(L::kSSmem), kGroupThreads);
+    mbar_init(bar(L::kSSmem + 1), kGroupThreads);
+    mbar_init(bar(L::kSRead), kGroupThreads);
+    mbar_init(bar(L::kSRead + 1), kGroupThreads);
     mbar_init(bar(L::kSAcc), 1);
-    mbar_init(bar(L::kSFree), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -235,45 +242,49 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const bool first = r.flags & kTileFirst, last = r.flags & kTileLast;
       const bool has_state = !first || (r.flags & kTileHasInit);
       const uint32_t colO = b ? kColO1 : kColO0;
-      // Q, K, V of tile i, S(i) staged, O buffer free.
+      const uint32_t sop = base + L::kS + b * kSOpBytes;
+      // (1) The state columns hold S(i) and have been read out (or hold the
+      // item's start state): S (+)= K^T V.
       bool ok = wait_or_flag(bar(L::kFull + s), (i / kStages) & 1, err, kErrTimeoutTma);
-      if (ok) ok = wait_or_flag(bar(L::kSSmem), i & 1, err, kErrTimeoutMma);
-      if (ok && i >= 2) ok = wait_or_flag(bar(L::kOFree + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (ok) ok = wait_or_flag(bar(L::kSRead + b), (i >> 1) & 1, err, kErrTimeoutMma);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after_sync();
-      if (lane == 0) {
-        if (has_state) {
-          int m = 0;
-          for (int kk = 0; kk < kHeadDim / 16; ++kk)
-            for (int part = 0; part < 2; ++part, ++m)
-              mma_bf16(tmem + colO, smem_desc_sw128(st + L::kQ + kk * 32, 16, 1024),
-                       smem_desc_sw128(base + L::kS + part * kStateTileBytes + kk * 2048,
-                                       kStateTileBytes, 1024),
-                       id_n64_b_mn, m > 0);
-        }
-        if (!last) {
-          // S (+)= K^T V: on top of the start state the epilogue wrote into
-          // the state columns, or a fresh sum for an item without one.
-          for (int kk = 0; kk < kTileRows / 16; ++kk)
-            mma_bf16(tmem + kColS, smem_desc_sw128(st + L::kK + kk * 2048, kRowTileBytes, 1024),
-                     smem_desc_sw128(st + L::kV + kk * 2048, kRowTileBytes, 1024), id_kv,
-                     (has_state || kk > 0) ? 1u : 0u);
-          mma_commit(bar(L::kSAcc));
-        } else if (i + 1 < n) {
-          mma_commit(bar(L::kSFree));   // the next item may overwrite S
-        }
+      if (lane == 0 && !last) {
+        // A = [K | K]^T (both 64-wide M atoms read the K tile: leading byte
+        // offset 0), so TMEM lanes 64..127 hold a second copy of rows 0..63
+        // and four warps can read the state, two column halves each.
+        for (int kk = 0; kk < kTileRows / 16; ++kk)
+          mma_bf16(tmem + kColS, smem_desc_sw128(st + L::kK + kk * 2048, 0, 1024),
+                   smem_desc_sw128(st + L::kV + kk * 2048, kRowTileBytes, 1024), id_kv,
+                   (has_state || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::kSAcc));
       }
       __syncwarp();
-      // P(i) is bf16 in TMEM: O(i) += P(i) V(i); release the stage.
-      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kPDone + b), (i >> 1) & 1, err, kErrTimeoutMma)))
-        break;
+      // (2) P(i) is bf16 in TMEM and the O buffer is free: O(i) = P(i) V(i).
+      ok = wait_or_flag(bar(L::kPDone + b), (i >> 1) & 1, err, kErrTimeoutMma);
+      if (ok && i >= 2) ok = wait_or_flag(bar(L::kOFree + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after_sync();
       if (lane == 0) {
         const uint32_t colP = b ? kColP1 : kColP0;
         for (int kk = 0; kk < kTileRows / 16; ++kk)
           mma_bf16_tmem_a(tmem + colO, tmem + colP + kk * 8,
                           smem_desc_sw128(st + L::kV + kk * 2048, kRowTileBytes, 1024),
-                          id_n64_b_mn, (has_state || kk > 0) ? 1u : 0u);
+                          id_n64_b_mn, kk > 0 ? 1u : 0u);
+      }
+      __syncwarp();
+      // (3) S(i) staged: O(i) += Q S_hi + Q S_lo; release the stage.
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kSSmem + b), (i >> 1) & 1, err, kErrTimeoutMma)))
+        break;
+      tc_fence_after_sync();
+      if (lane == 0) {
+        if (has_state) {
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            for (int part = 0; part < 2; ++part)
+              mma_bf16(tmem + colO, smem_desc_sw128(st + L::kQ + kk * 32, 16, 1024),
+                       smem_desc_sw128(sop + part * kStateTileBytes + kk * 2048, kStateTileBytes, 1024),
+                       id_n64_b_mn, 1u);
+        }
         mma_commit(bar(L::kOReady + b));
         mma_commit(bar(L::kEmpty + s));
       }
@@ -345,86 +356,74 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
     const int row = quarter * 32 + lane;          // tile row = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const bool state_rows = quarter < 2;          // lanes 0..63 hold state rows
-    uint32_t sacc = 0, sfree = 0;
-    float s_next[kHeadDim];                       // next item's start state (this row)
+    // State work: lanes 0..63 and their copy in lanes 64..127 hold state rows
+    // d = row & 63; the lower copy handles columns 0..31, the upper 32..63.
+    const int d = row & 63, sh = row >> 6;
+    uint32_t sacc = 0;
+    float s_next[32];                             // next item's start state (row d, half sh)
 
-    // Load the start state of the item starting at tile record `r` (state rows only).
+    // Load the start state of the item starting at tile record `r`.
     auto fetch_state = [&](const WorkTile& r) {
       float* x = s_next;
 #pragma unroll
-      for (int e = 0; e < kHeadDim; ++e) x[e] = 0.f;
-      if (!state_rows) return;
+      for (int e = 0; e < 32; ++e) x[e] = 0.f;
       if (r.stateA >= 0) {
         const float4* a = reinterpret_cast<const float4*>(
-            stateA + ((static_cast<int64_t>(r.stateA) * H + r.head) * kHeadDim + row) * kHeadDim);
+            stateA + ((static_cast<int64_t>(r.stateA) * H + r.head) * kHeadDim + d) * kHeadDim) + sh * 8;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < 8; ++c) {
           const float4 v4 = __ldcg(a + c);
           x[4 * c] += v4.x; x[4 * c + 1] += v4.y; x[4 * c + 2] += v4.z; x[4 * c + 3] += v4.w;
         }
       }
       if (r.stateB >= 0) {
         const float4* bb = reinterpret_cast<const float4*>(
-            stateB + ((static_cast<int64_t>(r.stateB) * H + r.head) * kHeadDim + row) * kHeadDim);
+            stateB + ((static_cast<int64_t>(r.stateB) * H + r.head) * kHeadDim + d) * kHeadDim) + sh * 8;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < 8; ++c) {
           const float4 v4 = __ldcg(bb + c);
           x[4 * c] += v4.x; x[4 * c + 1] += v4.y; x[4 * c + 2] += v4.z; x[4 * c + 3] += v4.w;
         }
       }
     };
 
-    // First tile of an item: its start state -> S operand (after the previous
-    // tile's Q S has read the operand) and, when the item has more tiles, into
-    // the TMEM state columns the state updates accumulate on.
-    auto stage_first = [&](int i, const WorkTile& r) -> bool {
-      if (i > 0) {
-        const bool ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kSFree), sfree & 1, err, kErrTimeoutMma));
-        ++sfree;
-        if (!ok) return false;
-      }
-      if (state_rows && (r.flags & kTileHasInit)) {
-        stage_state_half_row(smem + L::kS, row, 0, s_next);
-        stage_state_half_row(smem + L::kS, row, 1, s_next + 32);
-        if (!(r.flags & kTileLast)) {
+    // First tile t of an item: its start state into the TMEM state columns
+    // (when the item has more tiles) and into S operand t & 1.  The operand
+    // was last read by Q S of tile t-2, whose completion o_work(t-2) saw.
+    auto stage_first = [&](int t, const WorkTile& r) {
+      const bool init = r.flags & kTileHasInit;
+      if (init && !(r.flags & kTileLast)) {
+        uint32_t u[32];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t u[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(s_next[32 * h + e]);
-            tmem_st_32cols(tmem + lane_base + kColS + 32 * h, u);
-          }
-          tmem_st_wait();
-        }
+        for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(s_next[e]);
+        tmem_st_32cols(tmem + lane_base + kColS + 32 * sh, u);
+        tmem_st_wait();
       }
-      fence_proxy_async_smem();
       tc_fence_before_sync();
-      mbar_arrive(bar(L::kSSmem));
-      return true;
+      mbar_arrive(bar(L::kSRead + (t & 1)));
+      if (init) stage_state_half_row(smem + L::kS + (t & 1) * kSOpBytes, d, sh, s_next);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::kSSmem + (t & 1)));
     };
 
-    // Tile r is not its item's last: the running state after it -> S operand.
-    auto s_work = [&]() -> bool {
+    // Tile t continues an item: the running state after tile t-1 -> registers
+    // (then the state columns are free for the next K^T V) -> S operand t & 1.
+    auto s_work = [&](int t) -> bool {
       const bool ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kSAcc), sacc & 1, err, kErrTimeoutMma));
       ++sacc;
       if (!ok) return false;
       tc_fence_after_sync();
-      if (state_rows) {
+      uint32_t r0[32];
+      tmem_ld_32cols(tmem + lane_base + kColS + 32 * sh, r0);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kSRead + (t & 1)));
+      float x[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t r0[32];
-          tmem_ld_32cols(tmem + lane_base + kColS + 32 * h, r0);
-          tmem_ld_wait();
-          float x[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r0[e]);
-          stage_state_half_row(smem + L::kS, row, h, x);
-        }
-      }
+      for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r0[e]);
+      stage_state_half_row(smem + L::kS + (t & 1) * kSOpBytes, d, sh, x);
       fence_proxy_async_smem();
-      tc_fence_before_sync();   // the state was read before the next K^T V writes it
-      mbar_arrive(bar(L::kSSmem));
+      mbar_arrive(bar(L::kSSmem + (t & 1)));
       return true;
     };
 
@@ -464,13 +463,15 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       WorkTile cur = load_tile(list);
       WorkTile nxt = n > 1 ? load_tile(list + 1) : WorkTile{};
       fetch_state(cur);
-      bool ok = stage_first(0, cur);
+      stage_first(0, cur);
       if (n > 1 && (nxt.flags & kTileFirst)) fetch_state(nxt);
+      bool ok = true;
       for (int i = 0; i < n && ok; ++i) {
         WorkTile nxt2 = i + 2 < n ? load_tile(list + i + 2) : WorkTile{};
         // S(i+1) first: the O issuer needs it right after P V of tile i.
         if (i + 1 < n) {
-          ok = (cur.flags & kTileLast) ? stage_first(i + 1, nxt) : s_work();
+          if (cur.flags & kTileLast) stage_first(i + 1, nxt);
+          else ok = s_work(i + 1);
           // s_next is free again (the current item's start state was staged
           // at its first tile): fetch the start state of tile i+2 if it
           // begins an item.
