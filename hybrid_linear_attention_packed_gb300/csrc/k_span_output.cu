@@ -360,20 +360,19 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // d = row & 63; the lower copy handles columns 0..31, the upper 32..63.
     const int d = row & 63, sh = row >> 6;
     uint32_t sacc = 0;
-    float s_next[32];                             // next item's start state (row d, half sh)
+    // Next item's start state (row d, half sh): the two parts as loaded,
+    // summed only when staged, so the loads stay in flight meanwhile.
+    float s_a[32], s_b[32];
 
-    // Load the start state of the item starting at tile record `r`.
+    // Issue the loads of the start state of the item starting at tile record `r`.
     auto fetch_state = [&](const WorkTile& r) {
-      float* x = s_next;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] = 0.f;
       if (r.stateA >= 0) {
         const float4* a = reinterpret_cast<const float4*>(
             stateA + ((static_cast<int64_t>(r.stateA) * H + r.head) * kHeadDim + d) * kHeadDim) + sh * 8;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const float4 v4 = __ldcg(a + c);
-          x[4 * c] += v4.x; x[4 * c + 1] += v4.y; x[4 * c + 2] += v4.z; x[4 * c + 3] += v4.w;
+          s_a[4 * c] = v4.x; s_a[4 * c + 1] = v4.y; s_a[4 * c + 2] = v4.z; s_a[4 * c + 3] = v4.w;
         }
       }
       if (r.stateB >= 0) {
@@ -382,7 +381,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const float4 v4 = __ldcg(bb + c);
-          x[4 * c] += v4.x; x[4 * c + 1] += v4.y; x[4 * c + 2] += v4.z; x[4 * c + 3] += v4.w;
+          s_b[4 * c] = v4.x; s_b[4 * c + 1] = v4.y; s_b[4 * c + 2] = v4.z; s_b[4 * c + 3] = v4.w;
         }
       }
     };
@@ -392,16 +391,22 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // was last read by Q S of tile t-2, whose completion o_work(t-2) saw.
     auto stage_first = [&](int t, const WorkTile& r) {
       const bool init = r.flags & kTileHasInit;
+      float x[32];
+      if (init) {
+        const bool ha = r.stateA >= 0, hb = r.stateB >= 0;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = ha ? (hb ? s_a[e] + s_b[e] : s_a[e]) : s_b[e];
+      }
       if (init && !(r.flags & kTileLast)) {
         uint32_t u[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(s_next[e]);
+        for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(x[e]);
         tmem_st_32cols(tmem + lane_base + kColS + 32 * sh, u);
         tmem_st_wait();
       }
       tc_fence_before_sync();
       mbar_arrive(bar(L::kSRead + (t & 1)));
-      if (init) stage_state_half_row(smem + L::kS + (t & 1) * kSOpBytes, d, sh, s_next);
+      if (init) stage_state_half_row(smem + L::kS + (t & 1) * kSOpBytes, d, sh, x);
       fence_proxy_async_smem();
       mbar_arrive(bar(L::kSSmem + (t & 1)));
     };
@@ -434,27 +439,26 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         return false;
       tc_fence_after_sync();
       const uint32_t colO = b ? kColO1 : kColO0;
-      uint32_t r0[32], r1[32];
-      tmem_ld_32cols(tmem + lane_base + colO, r0);
-      tmem_ld_32cols(tmem + lane_base + colO + 32, r1);
-      tmem_ld_wait();
-      tc_fence_before_sync();
-      mbar_arrive(bar(L::kOFree + b));
-      if (row < r.nrows) {
-        uint4* dst = reinterpret_cast<uint4*>(
-            out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim);
+      uint4* dst = reinterpret_cast<uint4*>(
+          out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim);
+      const bool store = row < r.nrows;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          dst[c] = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c]), __uint_as_float(r0[8 * c + 1])),
-                              pack_bf16x2(__uint_as_float(r0[8 * c + 2]), __uint_as_float(r0[8 * c + 3])),
-                              pack_bf16x2(__uint_as_float(r0[8 * c + 4]), __uint_as_float(r0[8 * c + 5])),
-                              pack_bf16x2(__uint_as_float(r0[8 * c + 6]), __uint_as_float(r0[8 * c + 7])));
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r0[32];
+        tmem_ld_32cols(tmem + lane_base + colO + 32 * h, r0);
+        tmem_ld_wait();
+        if (h == 1) {
+          tc_fence_before_sync();
+          mbar_arrive(bar(L::kOFree + b));
+        }
+        if (store) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          dst[4 + c] = make_uint4(pack_bf16x2(__uint_as_float(r1[8 * c]), __uint_as_float(r1[8 * c + 1])),
-                                  pack_bf16x2(__uint_as_float(r1[8 * c + 2]), __uint_as_float(r1[8 * c + 3])),
-                                  pack_bf16x2(__uint_as_float(r1[8 * c + 4]), __uint_as_float(r1[8 * c + 5])),
-                                  pack_bf16x2(__uint_as_float(r1[8 * c + 6]), __uint_as_float(r1[8 * c + 7])));
+          for (int c = 0; c < 4; ++c)
+            dst[4 * h + c] = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c]), __uint_as_float(r0[8 * c + 1])),
+                                        pack_bf16x2(__uint_as_float(r0[8 * c + 2]), __uint_as_float(r0[8 * c + 3])),
+                                        pack_bf16x2(__uint_as_float(r0[8 * c + 4]), __uint_as_float(r0[8 * c + 5])),
+                                        pack_bf16x2(__uint_as_float(r0[8 * c + 6]), __uint_as_float(r0[8 * c + 7])));
+        }
       }
       return true;
     };
