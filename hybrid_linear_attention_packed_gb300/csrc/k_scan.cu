@@ -30,6 +30,9 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) {
 __global__ void __launch_bounds__(kThreads)
 segmented_scan_kernel(const ScanDesc* __restrict__ scan, int H, float* __restrict__ ws,
                       float* __restrict__ final_out) {
+  // The next kernel may be scheduled now: it waits for this grid's completion
+  // before it reads anything written here.
+  griddep_launch_dependents();
   griddep_wait();   // chunk states from the previous kernel
   const ScanDesc sd = scan[blockIdx.x];
   const int h = blockIdx.y;
@@ -51,7 +54,6 @@ segmented_scan_kernel(const ScanDesc* __restrict__ scan, int H, float* __restric
       }
     }
   }
-  griddep_launch_dependents();
   if (sd.final_idx >= 0) {
     float* f = final_out + (static_cast<int64_t>(sd.final_idx) * H + h) * kStateFloats + off;
     *reinterpret_cast<float4*>(f) = run;

@@ -57,6 +57,7 @@ constexpr uint32_t kRowTileBytes = kTileRows * 128;        // 128 rows x 128 B
 constexpr uint32_t kStageBytes = 3 * kRowTileBytes;       // Q K V
 constexpr uint32_t kStateTileBytes = kHeadDim * 128;       // 64 rows x 128 B (bf16)
 constexpr uint32_t kSOpBytes = 2 * kStateTileBytes;         // S as bf16 hi + lo
+constexpr int kCoordSlots = 64;                              // tile coordinates staged for the producer
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: P buffers (128 each), O buffers (64 each), running state (64).
 constexpr uint32_t kColP0 = 0, kColP1 = 128, kColO0 = 256, kColO1 = 320, kColS = 384;
@@ -74,7 +75,8 @@ struct OutSmem {
                        kSSmem = kPReady + 8, kSRead = kPReady + 10, kSAcc = kPReady + 12,
                        kNumBars = kPReady + 13;
   static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
-  static constexpr uint32_t kBytes = kTmemSlot + 8;
+  static constexpr uint32_t kCoord = kTmemSlot + 8;              // (row0, head) of the first tiles
+  static constexpr uint32_t kBytes = kCoord + 8 * kCoordSlots;
   static constexpr uint32_t kRequest = kBytes + 1024;
 };
 static_assert(OutSmem::kRequest <= 227 * 1024, "shared memory budget");
@@ -164,28 +166,33 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  griddep_wait();   // states from the scan, schedule from the descriptor copy
+  // The schedule comes from a copy that completed before the first kernel of
+  // the pass began, and Q, K, V from before that: every role but the one that
+  // reads the start states runs ahead of the previous kernel's completion.
   const int i_begin = cta_begin[blockIdx.x];
   const int n = cta_begin[blockIdx.x + 1] - i_begin;
   const WorkTile* list = work + i_begin;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The (row0, head) of the first tiles, all loads in flight at once, so the
+    // ring fills without a dependent load per tile.
+    int2* coord = reinterpret_cast<int2*>(smem + L::kCoord);
+    for (int j = lane; j < kCoordSlots && j < n; j += 32) coord[j] = make_int2(list[j].row0, list[j].head);
+    __syncwarp();
     if (lane == 0) {
       bool ok = true;
       int i = 0;
-      WorkTile nxt = n > 0 ? load_tile(list) : WorkTile{};
       for (; i < n; ++i) {
-        const WorkTile r = nxt;
-        if (i + 1 < n) nxt = load_tile(list + i + 1);
+        const int2 rc = i < kCoordSlots ? coord[i] : make_int2(list[i].row0, list[i].head);
         const int s = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
         if (!wait_or_flag(bar(L::kEmpty + s), ph ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
         const uint32_t st = base + L::kStage0 + s * kStageBytes;
         mbar_arrive_expect_tx(bar(L::kFull + s), kStageBytes);
-        tma_load_3d(st + L::kQ, &tm_q, bar(L::kFull + s), 0, r.row0, r.head);
-        tma_load_3d(st + L::kK, &tm_k, bar(L::kFull + s), 0, r.row0, r.head);
-        tma_load_3d(st + L::kV, &tm_v, bar(L::kFull + s), 0, r.row0, r.head);
+        tma_load_3d(st + L::kQ, &tm_q, bar(L::kFull + s), 0, rc.x, rc.y);
+        tma_load_3d(st + L::kK, &tm_k, bar(L::kFull + s), 0, rc.x, rc.y);
+        tma_load_3d(st + L::kV, &tm_v, bar(L::kFull + s), 0, rc.x, rc.y);
       }
       // Wait (bounded) for the last loads to land before the CTA can exit.
       for (int u = (i > kStages ? i - kStages : 0); u < i; ++u)
@@ -463,6 +470,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       return true;
     };
 
+    griddep_wait();   // start states from the scan
     if (n > 0) {
       WorkTile cur = load_tile(list);
       WorkTile nxt = n > 1 ? load_tile(list + 1) : WorkTile{};

@@ -32,6 +32,7 @@ constexpr int kRows = 2 * kChunk;                        // rows per stage
 constexpr uint32_t kTileBytes = kRows * 128;             // 128 rows x 128 B (one head)
 constexpr uint32_t kStageBytes = 2 * kTileBytes;         // K, V
 constexpr uint32_t kTmemCols = 128;                      // two 64-column accumulators
+constexpr int kDescSlots = 128;                          // span records staged in shared memory
 
 struct SpanSmem {
   static constexpr uint32_t kStage0 = 0;
@@ -39,7 +40,8 @@ struct SpanSmem {
   static constexpr int kFull = 0, kEmpty = kStages, kAccReady = 2 * kStages,
                        kAccFree = 2 * kStages + 2, kNumBars = 2 * kStages + 4;
   static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
-  static constexpr uint32_t kBytes = kTmemSlot + 8;
+  static constexpr uint32_t kDesc = kTmemSlot + 8;               // this CTA's span records
+  static constexpr uint32_t kBytes = kDesc + kDescSlots * sizeof(SpanDesc);
   static constexpr uint32_t kRequest = kBytes + 1024;
 };
 
@@ -83,24 +85,34 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  griddep_wait();   // descriptors come from a copy earlier in the stream
+  // The scan may be scheduled now: it waits for this grid's completion itself.
+  griddep_launch_dependents();
+  const int64_t n_units = static_cast<int64_t>(n_spans) * H;
+  // Stage the span records of this CTA's first units in shared memory, all
+  // loads in flight at once, so the producer does not wait on one per unit.
+  SpanDesc* sdesc = reinterpret_cast<SpanDesc*>(smem + L::kDesc);
+  for (int j = tid; j < kDescSlots; j += kThreads) {
+    const int64_t u = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
+    if (u < n_units) sdesc[j] = spans[u / H];
+  }
+  auto span_of = [&](int64_t u, int j) { return j < kDescSlots ? sdesc[j] : spans[u / H]; };
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-
-  griddep_wait();   // descriptors come from a copy earlier in the stream
-  const int64_t n_units = static_cast<int64_t>(n_spans) * H;
 
   if (warp == 2) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int c = 0;   // running chunk count (ring position)
       bool ok = true;
-      for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const SpanDesc sd = spans[u / H];
+      int j = 0;   // unit count of this CTA
+      for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++j) {
+        const SpanDesc sd = span_of(u, j);
         const int h = static_cast<int>(u % H);
         const int n_chunks = (sd.len + kRows - 1) / kRows;
-        for (int j = 0; j < n_chunks; ++j, ++c) {
+        for (int q = 0; q < n_chunks; ++q, ++c) {
           const int s = c % kStages;
           if (!wait_or_flag(bar(L::kEmpty + s), ((c / kStages) & 1) ^ 1, err, kErrTimeoutMma)) {
             ok = false;
@@ -108,8 +120,8 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           }
           const uint32_t st = base + L::kStage0 + s * kStageBytes;
           mbar_arrive_expect_tx(bar(L::kFull + s), kStageBytes);
-          tma_load_3d(st, &tm_k, bar(L::kFull + s), 0, sd.row0 + j * kRows, h);
-          tma_load_3d(st + kTileBytes, &tm_v, bar(L::kFull + s), 0, sd.row0 + j * kRows, h);
+          tma_load_3d(st, &tm_k, bar(L::kFull + s), 0, sd.row0 + q * kRows, h);
+          tma_load_3d(st + kTileBytes, &tm_v, bar(L::kFull + s), 0, sd.row0 + q * kRows, h);
         }
       }
       // Let the last loads land (bounded) before the CTA can exit.
@@ -122,7 +134,7 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     int c = 0, k = 0;   // running chunk count, running unit count (of this CTA)
     bool ok = true;
     for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++k) {
-      const SpanDesc sd = spans[u / H];
+      const SpanDesc sd = span_of(u, k);
       const int n_chunks = (sd.len + kRows - 1) / kRows;
       const int b = k & 1;
       if (k >= 2) ok = wait_or_flag(bar(L::kAccFree + b), ((k - 2) >> 1) & 1, err, kErrTimeoutMma);
@@ -184,7 +196,6 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
   }
 
-  griddep_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
