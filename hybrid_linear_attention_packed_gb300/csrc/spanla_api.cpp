@@ -458,47 +458,177 @@ span_la_status encode_map(CUtensorMap* map, const void* base, int64_t T, int H, 
   return SPAN_LA_OK;
 }
 
-// Common tail of both entry points: workspace, descriptor upload, launches.
-span_la_status run_plan(const Plan& plan, const void* q, const void* k, const void* v,
-                        const span_la_dims& dims, const float* stateA, float* final_out,
-                        void* out, cudaStream_t stream, DeviceState* dev) {
-  const int H = dims.num_heads;
-  const int64_t T = dims.total_rows;
-  const bool split = dims.dtype == SPAN_LA_F32;
-  if (plan.n_out_tiles() == 0 && plan.scan.empty()) return SPAN_LA_OK;
-
-  // Descriptor block (uploaded with one copy), then the state slots and, for
-  // fp32 inputs, the six bf16 part arrays.
+// Descriptors of a plan: one block the kernels read, plus what the launches
+// need to know about it.
+struct DescBlock {
   std::vector<uint8_t> host;
-  const size_t off_scan = put(host, plan.scan);
-  const size_t off_bounds = put(host, plan.bounds);
-  size_t off_a = 0, off_b = 0, off_c = 0;
-  int grid = 0;
+  size_t off_scan = 0, off_bounds = 0, off_a = 0, off_b = 0, off_c = 0;
+  int grid = 0;            // span_output CTAs (span mode)
+  int n_scan = 0, n_spans = 0, n_chunks = 0, n_tiles = 0, state_slots = 0;
+  size_t n_out_tiles = 0;
+  bool span_mode = true;
+};
+
+DescBlock make_desc(const Plan& plan, int H, int num_sms) {
+  DescBlock d;
+  d.span_mode = plan.span_mode;
+  d.off_scan = put(d.host, plan.scan);
+  d.off_bounds = put(d.host, plan.bounds);
   if (plan.span_mode) {
     std::vector<WorkTile> work;
     std::vector<int32_t> cta_begin;
-    if (!plan.items.empty()) grid = build_schedule(plan, H, dev->num_sms, &work, &cta_begin);
-    off_a = put(host, plan.spans);
-    off_b = put(host, work);
-    off_c = put(host, cta_begin);
+    if (!plan.items.empty()) d.grid = build_schedule(plan, H, num_sms, &work, &cta_begin);
+    d.off_a = put(d.host, plan.spans);
+    d.off_b = put(d.host, work);
+    d.off_c = put(d.host, cta_begin);
   } else {
-    off_a = put(host, plan.chunks);
-    off_b = put(host, plan.tiles);
+    d.off_a = put(d.host, plan.chunks);
+    d.off_b = put(d.host, plan.tiles);
   }
-  const size_t desc_bytes = host.size();
+  d.n_scan = static_cast<int>(plan.scan.size());
+  d.n_spans = static_cast<int>(plan.spans.size());
+  d.n_chunks = static_cast<int>(plan.chunks.size());
+  d.n_tiles = static_cast<int>(plan.tiles.size());
+  d.state_slots = plan.state_slots();
+  d.n_out_tiles = plan.n_out_tiles();
+  return d;
+}
+
+// ------------------------------------------------------------------ plan cache
+// Passes with the same metadata (every layer of a model step, for instance)
+// reuse one uploaded descriptor block: the plan depends on the metadata, the
+// head count, the dtype and the SM count only.  A block is uploaded on the
+// calling stream; a call on another stream first waits for that upload.  At
+// most kCacheEntries blocks are kept per process; evicting one synchronises
+// the device before freeing it.  Calls made while their stream is being
+// captured into a graph bypass the cache.
+constexpr int kCacheEntries = 16;
+
+struct CacheEntry {
+  int device = -1;
+  std::vector<int32_t> key;
+  DescBlock desc;
+  uint8_t* d_block = nullptr;
+  cudaEvent_t uploaded = nullptr;
+  cudaStream_t upload_stream = nullptr;
+  uint64_t last_use = 0;
+};
+
+std::mutex g_cache_mu;
+std::vector<CacheEntry> g_cache;
+uint64_t g_cache_clock = 0;
+
+std::vector<int32_t> plan_key(int device, int dtype, int H, int from_state, int num_sms,
+                              const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
+                              int32_t B, const int32_t* parent) {
+  std::vector<int32_t> key = {device, dtype, H, from_state, num_sms, V, B};
+  if (V > 0) key.insert(key.end(), view_cu, view_cu + V + 1);
+  if (B > 0) {
+    key.insert(key.end(), branch_cu, branch_cu + B + 1);
+    key.insert(key.end(), parent, parent + B);
+  }
+  return key;
+}
+
+// The device block for `key` (built by `build` on a miss), usable on `stream`.
+// The caller holds g_cache_mu until its launches are enqueued, so that no
+// other call evicts the block meanwhile.
+template <typename Build>
+span_la_status cached_block(const std::vector<int32_t>& key, int device, cudaStream_t stream,
+                            Build&& build, const DescBlock** desc, const uint8_t** block) {
+  for (CacheEntry& en : g_cache) {
+    if (en.device == device && en.key == key) {
+      if (en.upload_stream != stream) {
+        cudaError_t e = cudaStreamWaitEvent(stream, en.uploaded, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(descriptor upload)");
+      }
+      en.last_use = ++g_cache_clock;
+      *desc = &en.desc;
+      *block = en.d_block;
+      return SPAN_LA_OK;
+    }
+  }
+  if (static_cast<int>(g_cache.size()) >= kCacheEntries) {
+    size_t victim = 0;
+    for (size_t i = 1; i < g_cache.size(); ++i)
+      if (g_cache[i].last_use < g_cache[victim].last_use) victim = i;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize(plan cache eviction)");
+    cudaFree(g_cache[victim].d_block);
+    cudaEventDestroy(g_cache[victim].uploaded);
+    g_cache.erase(g_cache.begin() + victim);
+  }
+  CacheEntry en;
+  en.device = device;
+  en.key = key;
+  en.desc = build();
+  const size_t bytes = std::max<size_t>(en.desc.host.size(), 256);
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&en.d_block), bytes);
+  if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMalloc(descriptors, %zu): %s", bytes, cudaGetErrorString(e));
+  if (!en.desc.host.empty())
+    e = cudaMemcpyAsync(en.d_block, en.desc.host.data(), en.desc.host.size(), cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&en.uploaded, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventRecord(en.uploaded, stream);
+  if (e != cudaSuccess) {
+    cudaFree(en.d_block);
+    return cuda_fail(e, "descriptor upload");
+  }
+  en.upload_stream = stream;
+  en.last_use = ++g_cache_clock;
+  g_cache.push_back(std::move(en));
+  *desc = &g_cache.back().desc;
+  *block = g_cache.back().d_block;
+  return SPAN_LA_OK;
+}
+
+// Common tail of both entry points: descriptors (cached, or uploaded into the
+// call's workspace while the stream is being captured), workspace, launches.
+template <typename BuildPlan>
+span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan, const void* q,
+                        const void* k, const void* v, const span_la_dims& dims, const float* stateA,
+                        float* final_out, void* out, cudaStream_t stream, DeviceState* dev, int device) {
+  const int H = dims.num_heads;
+  const int64_t T = dims.total_rows;
+  const bool split = dims.dtype == SPAN_LA_F32;
+
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  const bool use_cache = cap == cudaStreamCaptureStatusNone;
+  std::unique_lock<std::mutex> cache_lock(g_cache_mu, std::defer_lock);
+  DescBlock local;
+  const DescBlock* desc = nullptr;
+  const uint8_t* block = nullptr;
+  span_la_status st = SPAN_LA_OK;
+  if (use_cache) {
+    cache_lock.lock();
+    st = cached_block(key, device, stream, [&] { return make_desc(build_plan(), H, dev->num_sms); }, &desc,
+                      &block);
+    if (st != SPAN_LA_OK) return st;
+  } else {
+    local = make_desc(build_plan(), H, dev->num_sms);
+    desc = &local;
+  }
+  if (desc->n_out_tiles == 0 && desc->n_scan == 0) return SPAN_LA_OK;
+
+  // Workspace: the descriptor block when it is not cached, the state slots
+  // and, for fp32 inputs, the six bf16 part arrays.
+  const size_t desc_bytes = use_cache ? 0 : align256(desc->host.size());
   const size_t off_states = desc_bytes;
-  const size_t state_bytes = static_cast<size_t>(plan.state_slots()) * H * kStateFloats * sizeof(float);
+  const size_t state_bytes = static_cast<size_t>(desc->state_slots) * H * kStateFloats * sizeof(float);
   const size_t off_parts = align256(off_states + state_bytes);
   const size_t part_bytes = static_cast<size_t>(T) * H * kHeadDim * 2;
-  const size_t total = off_parts + (split ? 6 * part_bytes : 0);
+  const size_t total = std::max<size_t>(off_parts + (split ? 6 * part_bytes : 0), 256);
 
   uint8_t* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), total, stream);
+  e = cudaMallocAsync(reinterpret_cast<void**>(&ws), total, stream);
   if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): %s", total, cudaGetErrorString(e));
-  span_la_status st = SPAN_LA_OK;
   do {
-    e = cudaMemcpyAsync(ws, host.data(), desc_bytes, cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess) { st = cuda_fail(e, "cudaMemcpyAsync(descriptors)"); break; }
+    if (!use_cache) {
+      e = cudaMemcpyAsync(ws, desc->host.data(), desc->host.size(), cudaMemcpyHostToDevice, stream);
+      if (e != cudaSuccess) { st = cuda_fail(e, "cudaMemcpyAsync(descriptors)"); break; }
+      block = ws;
+    }
 
     // bf16 operand arrays the kernels read through TMA: the inputs themselves,
     // or, for fp32 inputs, their bf16 high / low parts made by the split kernel.
@@ -513,7 +643,7 @@ span_la_status run_plan(const Plan& plan, const void* q, const void* k, const vo
       if (e != cudaSuccess) { st = cuda_fail(e, "split kernel launch"); break; }
     }
     DeviceOperands tile_ops{}, chunk_ops{};
-    const bool need_maps = plan.n_out_tiles() > 0 || plan.state_slots() > 0;   // implies T > 0
+    const bool need_maps = desc->n_out_tiles > 0 || desc->state_slots > 0;   // implies T > 0
     for (int t = 0; t < 3 && st == SPAN_LA_OK && need_maps; ++t) {
       for (int p = 0; p < (split ? 2 : 1) && st == SPAN_LA_OK; ++p) {
         CUtensorMap* tm = t == 0 ? &tile_ops.q[p] : t == 1 ? &tile_ops.k[p] : &tile_ops.v[p];
@@ -522,56 +652,54 @@ span_la_status run_plan(const Plan& plan, const void* q, const void* k, const vo
         // K and V boxes of the state kernel: 64 rows of two heads (chunk
         // mode) or of one head (span mode).
         if (st == SPAN_LA_OK && t > 0)
-          st = plan.span_mode ? encode_map(cm, parts[t][p], T, H, kSpanBoxRows, 1)
-                              : encode_map(cm, parts[t][p], T, H, kChunkBoxRows, kChunkBoxHeads);
+          st = desc->span_mode ? encode_map(cm, parts[t][p], T, H, kSpanBoxRows, 1)
+                               : encode_map(cm, parts[t][p], T, H, kChunkBoxRows, kChunkBoxHeads);
       }
     }
     if (st != SPAN_LA_OK) break;
 
     float* states = reinterpret_cast<float*>(ws + off_states);
     bool kernel_before = split;   // a kernel precedes the next launch in the stream
-    if (plan.state_slots() > 0) {
-      e = plan.span_mode
+    if (desc->state_slots > 0) {
+      e = desc->span_mode
               ? counted_launch(kKernelSpanState, stream, [&] {
-                  const int grid = static_cast<int>(std::min<int64_t>(
-                      static_cast<int64_t>(plan.spans.size()) * H, dev->num_sms));
+                  const int sgrid = static_cast<int>(std::min<int64_t>(
+                      static_cast<int64_t>(desc->n_spans) * H, dev->num_sms));
                   return launch_span_state(chunk_ops.k, chunk_ops.v,
-                                           reinterpret_cast<const SpanDesc*>(ws + off_a),
-                                           static_cast<int>(plan.spans.size()), H, states, grid,
-                                           dev->err, stream);
+                                           reinterpret_cast<const SpanDesc*>(block + desc->off_a),
+                                           desc->n_spans, H, states, sgrid, dev->err, stream);
                 })
               : counted_launch(kKernelChunk, stream, [&] {
                   return launch_chunk_state(split, chunk_ops.k, chunk_ops.v,
-                                            reinterpret_cast<const ChunkDesc*>(ws + off_a),
-                                            static_cast<int>(plan.chunks.size()), H, states, dev->err, stream);
+                                            reinterpret_cast<const ChunkDesc*>(block + desc->off_a),
+                                            desc->n_chunks, H, states, dev->err, stream);
                 });
       if (e != cudaSuccess) { st = cuda_fail(e, "chunk/span-state launch"); break; }
       kernel_before = true;
     }
-    if (!plan.scan.empty()) {
+    if (desc->n_scan > 0) {
       const bool pdl = kernel_before;
       e = counted_launch(kKernelScan, stream, [&] {
-        return launch_scan(reinterpret_cast<const ScanDesc*>(ws + off_scan),
-                           static_cast<int>(plan.scan.size()), H, states, final_out, stream, pdl);
+        return launch_scan(reinterpret_cast<const ScanDesc*>(block + desc->off_scan), desc->n_scan, H,
+                           states, final_out, stream, pdl);
       });
       if (e != cudaSuccess) { st = cuda_fail(e, "scan launch"); break; }
       kernel_before = true;
     }
-    if (plan.n_out_tiles() > 0) {
-      if (plan.span_mode) {
+    if (desc->n_out_tiles > 0) {
+      if (desc->span_mode) {
         const bool pdl = kernel_before;
         e = counted_launch(kKernelSpanOutput, stream, [&] {
           return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v,
-                                    reinterpret_cast<const WorkTile*>(ws + off_b),
-                                    reinterpret_cast<const int32_t*>(ws + off_c), grid,
-                                    ws + off_bounds, stateA, states, out, H, dev->err, stream, pdl);
+                                    reinterpret_cast<const WorkTile*>(block + desc->off_b),
+                                    reinterpret_cast<const int32_t*>(block + desc->off_c), desc->grid,
+                                    block + desc->off_bounds, stateA, states, out, H, dev->err, stream, pdl);
         });
       } else {
         e = counted_launch(kKernelTile, stream, [&] {
           return launch_tile_output(split, tile_ops.q, tile_ops.k, tile_ops.v,
-                                    reinterpret_cast<const TileDesc*>(ws + off_b),
-                                    static_cast<int>(plan.tiles.size()), ws + off_bounds, stateA,
-                                    states, out, H, dev->err, stream);
+                                    reinterpret_cast<const TileDesc*>(block + desc->off_b), desc->n_tiles,
+                                    block + desc->off_bounds, stateA, states, out, H, dev->err, stream);
         });
       }
       if (e != cudaSuccess) { st = cuda_fail(e, "output launch"); break; }
@@ -616,9 +744,15 @@ span_la_status span_la_pass(const void* q, const void* k, const void* v, span_la
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != SPAN_LA_OK) return st;
 
-  const Plan plan = make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
-                              branch_parent, dims.num_heads, dims.dtype == SPAN_LA_BF16);
-  return run_plan(plan, q, k, v, dims, view_state_out, view_state_out, out, stream, dev);
+  int device = 0;
+  cudaGetDevice(&device);
+  const std::vector<int32_t> key = plan_key(device, dims.dtype, dims.num_heads, 0, dev->num_sms, view_cu_seqlens,
+                                            num_views, branch_cu_seqlens, num_branches, branch_parent);
+  auto build = [&] {
+    return make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches, branch_parent,
+                     dims.num_heads, dims.dtype == SPAN_LA_BF16);
+  };
+  return run_plan(key, build, q, k, v, dims, view_state_out, view_state_out, out, stream, dev, device);
 }
 
 span_la_status span_la_branches_from_state(const float* cached_state, int32_t num_states,
@@ -642,9 +776,15 @@ span_la_status span_la_branches_from_state(const float* cached_state, int32_t nu
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != SPAN_LA_OK) return st;
 
-  const Plan plan = make_plan(nullptr, 0, branch_cu_seqlens, num_branches, branch_parent,
-                              dims.num_heads, dims.dtype == SPAN_LA_BF16);
-  return run_plan(plan, q, k, v, dims, cached_state, nullptr, out, stream, dev);
+  int device = 0;
+  cudaGetDevice(&device);
+  const std::vector<int32_t> key = plan_key(device, dims.dtype, dims.num_heads, 1, dev->num_sms, nullptr, 0,
+                                            branch_cu_seqlens, num_branches, branch_parent);
+  auto build = [&] {
+    return make_plan(nullptr, 0, branch_cu_seqlens, num_branches, branch_parent, dims.num_heads,
+                     dims.dtype == SPAN_LA_BF16);
+  };
+  return run_plan(key, build, q, k, v, dims, cached_state, nullptr, out, stream, dev, device);
 }
 
 span_la_status span_la_check(cudaStream_t stream) {

@@ -123,3 +123,26 @@ def test_profiler_counts_and_times_every_launch(cuda_device):
         assert prof[name]["launches"] == 3 and prof[name]["timed"] == 3
         assert prof[name]["ms"] > 0
     assert prof["chunk_state"]["launches"] == 0
+
+
+def test_plan_reused_across_calls_and_streams(cuda_device):
+    """Passes with the same metadata reuse one uploaded descriptor block (the
+    plan depends on the metadata only): new inputs on the same and on another
+    stream still give the oracle's results."""
+    from helpers import TOL, f64, rel_err, segment_rows
+    from oracle import oracle_pass
+    base = workloads.make_pass([700, 129], [30, 60, 100, 5], [0, 0, 1, 1], H=3, dtype="bf16", seed=50)
+    side = torch.cuda.Stream(device=cuda_device)
+    for i, stream in enumerate([torch.cuda.current_stream(cuda_device), side, side]):
+        w = workloads.make_pass([700, 129], [30, 60, 100, 5], [0, 0, 1, 1], H=3, dtype="bf16", seed=51 + i)
+        assert np.array_equal(w.view_cu, base.view_cu) and np.array_equal(w.branch_cu, base.branch_cu)
+        with torch.cuda.stream(stream):
+            q, k, v = to_device(w, cuda_device)
+            out, state = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
+                                      out=torch.full_like(q, float("nan")))
+        stream.synchronize()
+        span_la_check()
+        ref, ref_state = oracle_pass(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu, w.branch_parent)
+        seg = segment_rows(w)
+        assert rel_err(f64(out)[seg], ref[seg]) <= TOL["bf16"]
+        assert rel_err(f64(state), ref_state) <= TOL["bf16"]
