@@ -181,13 +181,15 @@ cudaError_t launch_chunk_state(bool split, const CUtensorMap* tm_k, const CUtens
   if (split) {
     auto kern = chunk_state_kernel<2>;
     const uint32_t bytes = ChunkSmem<2>::kRequest;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    static std::atomic<uint64_t> done{0};
+    cudaError_t e = set_smem_limit_once(kern, bytes, done);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, bytes, stream>>>(tm_k[0], tm_k[1], tm_v[0], tm_v[1], chunks, H, ws, err);
   } else {
     auto kern = chunk_state_kernel<1>;
     const uint32_t bytes = ChunkSmem<1>::kRequest;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    static std::atomic<uint64_t> done{0};
+    cudaError_t e = set_smem_limit_once(kern, bytes, done);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, bytes, stream>>>(tm_k[0], tm_k[0], tm_v[0], tm_v[0], chunks, H, ws, err);
   }

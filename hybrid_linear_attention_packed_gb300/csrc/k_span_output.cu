@@ -512,8 +512,8 @@ cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                unsigned* err, cudaStream_t stream, bool pdl) {
   if (grid <= 0) return cudaSuccess;
   const uint32_t bytes = OutSmem::kRequest;
-  cudaError_t e =
-      cudaFuncSetAttribute(span_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  static std::atomic<uint64_t> done{0};
+  cudaError_t e = set_smem_limit_once(span_output_kernel, bytes, done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -209,8 +209,8 @@ cudaError_t launch_span_state(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                               int grid, unsigned* err, cudaStream_t stream) {
   if (n_spans <= 0 || grid <= 0) return cudaSuccess;
   const uint32_t bytes = SpanSmem::kRequest;
-  cudaError_t e =
-      cudaFuncSetAttribute(span_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  static std::atomic<uint64_t> done{0};
+  cudaError_t e = set_smem_limit_once(span_state_kernel, bytes, done);
   if (e != cudaSuccess) return e;
   span_state_kernel<<<grid, kThreads, bytes, stream>>>(tm_k[0], tm_v[0], spans, n_spans, H, ws, err);
   return cudaGetLastError();

@@ -342,14 +342,16 @@ cudaError_t launch_tile_output(bool split, const CUtensorMap* tm_q, const CUtens
   if (split) {
     auto kern = tile_output_kernel<2>;
     const uint32_t bytes = TileSmem<2>::kRequest;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    static std::atomic<uint64_t> done{0};
+    cudaError_t e = set_smem_limit_once(kern, bytes, done);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, bytes, stream>>>(tm_q[0], tm_q[1], tm_k[0], tm_k[1], tm_v[0], tm_v[1],
                                             tiles, bounds, stateA, stateB, out, H, err);
   } else {
     auto kern = tile_output_kernel<1>;
     const uint32_t bytes = TileSmem<1>::kRequest;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    static std::atomic<uint64_t> done{0};
+    cudaError_t e = set_smem_limit_once(kern, bytes, done);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, bytes, stream>>>(tm_q[0], tm_q[0], tm_k[0], tm_k[0], tm_v[0], tm_v[0],
                                             tiles, bounds, stateA, stateB, out, H, err);

@@ -2,6 +2,7 @@
 // descriptor build, workspace, launches) and its CUDA kernels.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -96,6 +97,20 @@ struct DeviceOperands {
   // TMA descriptors; [0] = bf16 value (or high part), [1] = low part (fp32 inputs).
   CUtensorMap q[2], k[2], v[2];
 };
+
+// Raise a kernel's dynamic shared-memory limit once per device (`done` holds
+// one bit per device it was set on).
+template <typename Kernel>
+inline cudaError_t set_smem_limit_once(Kernel kernel, uint32_t bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Kernel launchers (each returns the launch error, if any).
 cudaError_t launch_split_f32(const float* q, const float* k, const float* v, int64_t n,

@@ -60,7 +60,9 @@ def load_library(path: Optional[str] = None):
             raise RuntimeError("libspanla.so not found at %s: build it with "
                                "hybrid_linear_attention_packed_gb300.build.build()" % p)
         lib = ctypes.CDLL(p)
-        vp, i32p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)
+        # int32 arrays go in as addresses (c_void_p also takes ctypes pointers)
+        vp = ctypes.c_void_p
+        i32p = vp
         lib.span_la_pass.argtypes = [vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
                                      ctypes.c_int32, i32p, vp, vp, vp]
         lib.span_la_pass.restype = ctypes.c_int
@@ -107,15 +109,18 @@ def _raise(lib, status: int, where: str):
 def _i32(a) -> np.ndarray:
     if a is None:
         return np.zeros(0, dtype=np.int32)
+    if isinstance(a, np.ndarray) and a.dtype == np.int32 and a.ndim == 1 and a.flags.c_contiguous:
+        return a
     if isinstance(a, torch.Tensor):
         a = a.detach().cpu().numpy()
     return np.ascontiguousarray(np.asarray(a, dtype=np.int64).reshape(-1).astype(np.int32))
 
 
 def _iptr(a: np.ndarray):
+    """Address of an int32 array for a ``const int32_t*`` argument (None when empty)."""
     if a.size == 0:
         return None
-    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    return a.ctypes.data
 
 
 def _stream_handle(stream) -> int:
