@@ -134,7 +134,7 @@ cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                unsigned* err, cudaStream_t stream, bool pdl);
 
 // Work items the planner aims for when it picks the span length G.
-constexpr int kTargetItems = 4 * 152;
+constexpr int kTargetItems = 2 * 152;
 constexpr int kMaxSpanTiles = 8;
 
 cudaError_t launch_tile_output(bool split, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
