@@ -10,10 +10,11 @@
 // Persistent CTAs (one per SM) walk the (span, head) units u = blockIdx.x,
 // blockIdx.x + gridDim.x, ... (heads fastest, so CTAs reading the same rows
 // run together).  4 warps:
-//   warp 2     producer: K and V of one head, 128 rows (two chunks) at a
-//              time ([128 rows][64 d] bf16, 128-byte swizzle), into a
-//              six-stage ring, running ahead across units.
-//   warp 3     MMA issuer: per 128 rows 8 MMAs  acc (+)= K^T V  with both
+//   warp 2     producer: K and V of one head, 256 rows (four chunks) at a
+//              time ([256 rows][64 d] bf16, 128-byte swizzle; 32 KB boxes
+//              stream faster than 16 KB ones), into a three-stage ring,
+//              running ahead across units.
+//   warp 3     MMA issuer: per 256 rows 16 MMAs  acc (+)= K^T V  with both
 //              operands MN-major (the contraction runs over tokens): A (M =
 //              128) = [K | V]^T -- the V tile is the second 64-wide M atom and
 //              only TMEM lanes 0..63 (K^T V) are kept -- and B (N = 64) = V.
@@ -27,8 +28,8 @@ namespace spanla {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kStages = 6;
-constexpr int kRows = 2 * kChunk;                        // rows per stage
+constexpr int kStages = 3;
+constexpr int kRows = 4 * kChunk;                        // rows per stage
 constexpr uint32_t kTileBytes = kRows * 128;             // 128 rows x 128 B (one head)
 constexpr uint32_t kStageBytes = 2 * kTileBytes;         // K, V
 constexpr uint32_t kTmemCols = 128;                      // two 64-column accumulators

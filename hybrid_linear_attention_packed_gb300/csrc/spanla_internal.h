@@ -151,7 +151,7 @@ cudaError_t noalloc_scratch(uint8_t** scratch, unsigned** err);
 // Box sizes of the TMA descriptors each kernel expects.
 constexpr int kChunkBoxRows = kChunk;     // chunk-state kernel: 64 rows x 2 heads
 constexpr int kChunkBoxHeads = 2;
-constexpr int kSpanBoxRows = 2 * kChunk;  // span-state kernel: 128 rows x 1 head
+constexpr int kSpanBoxRows = 4 * kChunk;  // span-state kernel: 256 rows x 1 head
 constexpr int kTileBoxRows = kTileRows;   // tile-output kernel: 128 rows x 1 head
 
 }  // namespace spanla
