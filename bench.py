@@ -162,6 +162,19 @@ def io_bytes(w, esize: int) -> int:
     return w.rows * w.H * 64 * esize * 4 + w.V * w.H * STATE_BYTES
 
 
+def chunked_method_bytes(w, esize: int) -> int:
+    """Bytes of the chunked three-launch method as the pages lay it out, one
+    fp32 64x64 state per 64-token chunk: q, k, v read and o written (4 rows),
+    k and v read again by the state kernel (2 rows), and each chunk state
+    written, read and written by the scan and read by the output kernel
+    (4 x 16 KiB per 64 rows) -- per view token-head; branch rows count q, k,
+    v, o only."""
+    row = 64 * esize
+    view_rows = int(w.view_lens.sum())
+    per_view_row = 6 * row + 4 * STATE_BYTES // 64
+    return (view_rows * per_view_row + (w.rows - view_rows) * 4 * row) * w.H
+
+
 def kernel_sha(name: str) -> str:
     files = {"tile_output": "k_tile_output.cu", "chunk_state": "k_chunk_state.cu",
              "segmented_scan": "k_scan.cu", "split_f32": "k_misc.cu",
@@ -363,10 +376,13 @@ def main():
                 "peak_source": peak_src,
                 "alg_bytes_per_launch": dk["alg_bytes"]}
     step_bytes = sum(alg[n] for n in kernels)
+    chunked = chunked_method_bytes(w, esize)
     pass_roofline = {"method_bytes": step_bytes,
                      "method_frac": step_bytes / (ms / 1e3) / 1e9 / hbm_peak,
                      "io_bytes": io_bytes(w, esize),
-                     "io_frac": io_bytes(w, esize) / (ms / 1e3) / 1e9 / hbm_peak}
+                     "io_frac": io_bytes(w, esize) / (ms / 1e3) / 1e9 / hbm_peak,
+                     "chunked_method_bytes": chunked,
+                     "chunked_method_frac": chunked / (ms / 1e3) / 1e9 / hbm_peak}
 
     # End to end through the public API with host buffers: every step copies
     # its q, k, v from pinned host memory, runs the call and reads out and the
