@@ -201,17 +201,28 @@ def recorded_traffic(kernel: str, workload: str):
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_time(w, budget_s: float = 8.0, max_reps: int = 50):
-    """Time the float64 oracle on the whole workload, repeated within ~budget_s."""
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+def oracle_time(w, budget_s: float = 8.0, max_reps: int = 50, nthreads: int = 0):
+    """Time the float64 oracle on the whole workload, repeated within ~budget_s
+    (nthreads = 0: every host core)."""
     from oracle import oracle_max_threads, oracle_pass
     q, k, v = (t.double().numpy() for t in (w.q, w.k, w.v))
     times = []
     t_all = time.perf_counter()
     while len(times) < max_reps and (time.perf_counter() - t_all) < budget_s:
         t0 = time.perf_counter()
-        oracle_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+        oracle_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, nthreads=nthreads)
         times.append(time.perf_counter() - t0)
-    return statistics.median(times), len(times), oracle_max_threads()
+    return statistics.median(times), len(times), (nthreads or oracle_max_threads())
 
 
 def run_reference(args):
@@ -479,15 +490,64 @@ def main():
         t = torch.tensor([e2e_ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    # Host time to enqueue one call (the device kept busy so that no launch
+    # waits on it), and the device time per call with the L2 warm: calls
+    # enqueued back to back with no flush between them.
+    busy = torch.empty(256 << 20, dtype=torch.float32, device=dev)
+    host_us = []
+    for _ in range(50):
+        busy.zero_()
+        t_h = time.perf_counter()
+        step()
+        host_us.append((time.perf_counter() - t_h) * 1e6)
+    torch.cuda.synchronize()
+    del busy
+    # Back to back through the C entry points with prepared arguments, so that
+    # the host (about 14 us per call) stays ahead of the device.
+    lib = spanla.load_library()
+    dims = spanla.Dims(q.shape[0], q.shape[1], 64, spanla.SPAN_LA_BF16 if w.dtype == "bf16" else spanla.SPAN_LA_F32)
+    sh = stream.cuda_stream
+    if shards_mode:
+        raw = [(cached.data_ptr(), 1, q.data_ptr(), k.data_ptr(), v.data_ptr(), dims, cu.ctypes.data,
+                len(cu) - 1, par.ctypes.data, out.data_ptr(), sh) for cu, par in zip(shard_cu, shard_par)]
+        fn = lib.span_la_branches_from_state
+    else:
+        vcu, bcu, par = (np.ascontiguousarray(a, dtype=np.int32) for a in (w.view_cu, w.branch_cu, w.branch_parent))
+        raw = [(q.data_ptr(), k.data_ptr(), v.data_ptr(), dims, vcu.ctypes.data, len(vcu) - 1,
+                bcu.ctypes.data if len(bcu) else None, max(len(bcu) - 1, 0),
+                par.ctypes.data if len(par) else None, out.data_ptr(), state.data_ptr(), sh)]
+        fn = lib.span_la_pass
+
+    def raw_step():
+        for a in raw:
+            fn(*a)
+
+    NW = 200
+    w_start = torch.cuda.Event(enable_timing=True)
+    w_end = torch.cuda.Event(enable_timing=True)
+    for _ in range(5):
+        raw_step()
+    w_start.record(stream)
+    for _ in range(NW):
+        raw_step()
+    w_end.record(stream)
+    torch.cuda.synchronize()
+    spanla.span_la_check()
+    warm_us = w_start.elapsed_time(w_end) * 1e3 / NW
+
     h2d = 3 * (w.T - row_lo) * w.H * 64 * esize
     d2h = (w.T - row_lo) * w.H * 64 * esize + (0 if shards_mode else w.V * w.H * STATE_BYTES)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not shards_mode:
         med, reps, cores = oracle_time(w)
+        med1, reps1, _ = oracle_time(w, budget_s=6.0, max_reps=3, nthreads=1)
         cpu = {"value": w.rows / med, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "the whole workload (%d rows x %d heads), median of %d passes"
-                         % (w.rows, w.H, reps)}
+                         % (w.rows, w.H, reps),
+               "one_thread": {"value": w.rows / med1, "unit": UNIT, "cores": 1,
+                              "sample": "median of %d passes" % reps1},
+               "cpu_model": cpu_model()}
 
     vs = None
     if args.workload == "single":
@@ -510,7 +570,9 @@ def main():
                 "clocks": summarize_clocks(clock_rows, t0, t1),
                 "step_ms_p50": statistics.median(step_ms),
                 "profiled_kernel_us_sum": profiled_step_us,
-                "step_ms_min": min(step_ms)}
+                "step_ms_min": min(step_ms),
+                "host_enqueue_us": statistics.median(host_us),
+                "warm_l2_us_per_step": warm_us}
         print(json.dumps(line))
     if pg:
         pg.barrier()
