@@ -10,4 +10,5 @@ from .spanla import (  # noqa: F401
     span_la_branches_from_state,
     span_la_check,
     span_la_pass,
+    ViewStateCache,
 )

@@ -756,6 +756,10 @@ span_la_status check_operands(const void* q, const void* k, const void* v, void*
 
 }  // namespace
 
+namespace spanla {
+void set_last_error_detail(const char* text) { g_detail = text; }
+}  // namespace spanla
+
 extern "C" {
 
 span_la_status span_la_pass(const void* q, const void* k, const void* v, span_la_dims dims,

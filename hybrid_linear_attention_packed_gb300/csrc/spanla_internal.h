@@ -98,6 +98,9 @@ struct DeviceOperands {
   CUtensorMap q[2], k[2], v[2];
 };
 
+// Set the calling thread's last-error text (span_la_last_error_detail).
+void set_last_error_detail(const char* text);
+
 // Raise a kernel's dynamic shared-memory limit once per device (`done` holds
 // one bit per device it was set on).
 template <typename Kernel>

@@ -30,7 +30,9 @@ EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
             "span_la_status_string", "span_la_last_error_detail", "span_la_version",
             "span_la_selftest_wait_timeout", "span_la_profile_enable", "span_la_profile_read",
             "span_la_profile_reset", "span_la_kernel_name", "span_la_plan_stats",
-            "span_la_pass_noalloc")
+            "span_la_pass_noalloc", "span_la_cache_create", "span_la_cache_destroy",
+            "span_la_cache_put", "span_la_cache_contains", "span_la_cache_branches",
+            "span_la_cache_stats")
 NUM_KERNELS = 6
 
 
@@ -96,6 +98,20 @@ def load_library(path: Optional[str] = None):
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)]
         lib.span_la_plan_stats.restype = ctypes.c_int
+        lib.span_la_cache_create.argtypes = [ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.POINTER(ctypes.c_void_p)]
+        lib.span_la_cache_create.restype = ctypes.c_int
+        lib.span_la_cache_destroy.argtypes = [vp]
+        lib.span_la_cache_destroy.restype = ctypes.c_int
+        lib.span_la_cache_put.argtypes = [vp, vp, ctypes.c_int32, vp, vp]
+        lib.span_la_cache_put.restype = ctypes.c_int
+        lib.span_la_cache_contains.argtypes = [vp, vp, ctypes.c_int32, vp]
+        lib.span_la_cache_contains.restype = ctypes.c_int
+        lib.span_la_cache_branches.argtypes = [vp, vp, vp, vp, vp, Dims, i32p, ctypes.c_int32,
+                                               vp, vp]
+        lib.span_la_cache_branches.restype = ctypes.c_int
+        lib.span_la_cache_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
+        lib.span_la_cache_stats.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -206,6 +222,96 @@ def span_la_branches_from_state(cached_state: torch.Tensor, q: torch.Tensor, k: 
                                          _stream_handle(stream))
     _raise(lib, st, "span_la_branches_from_state")
     return out
+
+
+def _keys(keys) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(keys, dtype=np.uint64).reshape(-1))
+    return a
+
+
+CACHE_FIELDS = ("entries", "capacity", "hits", "misses", "evictions", "puts")
+
+
+class ViewStateCache:
+    """Keyed least-recently-used cache of view final states in device memory
+    (``span_la_cache_*``): put a pass's ``view_state_out`` rows under keys,
+    then run branches (or shards of them) from the cached states by key."""
+
+    def __init__(self, num_heads: int, capacity: int):
+        self._lib = load_library()
+        handle = ctypes.c_void_p()
+        _raise(self._lib, self._lib.span_la_cache_create(int(num_heads), int(capacity),
+                                                         ctypes.byref(handle)),
+               "span_la_cache_create")
+        self._handle = handle.value
+        self.num_heads = int(num_heads)
+        self.capacity = int(capacity)
+
+    def close(self) -> None:
+        if self._handle:
+            handle, self._handle = self._handle, None
+            _raise(self._lib, self._lib.span_la_cache_destroy(handle), "span_la_cache_destroy")
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _live(self):
+        if not self._handle:
+            raise ValueError("the cache is closed")
+        return self._handle
+
+    def put(self, keys, states: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+        """Store states[i] (fp32 CUDA [n, H, 64, 64], contiguous) under keys[i]."""
+        ks = _keys(keys)
+        if (states.dtype != torch.float32 or not states.is_contiguous() or not states.is_cuda
+                or states.dim() != 4 or tuple(states.shape[1:]) != (self.num_heads, 64, 64)
+                or states.shape[0] != ks.size):
+            raise ValueError("states must be contiguous fp32 CUDA [len(keys), H, 64, 64]")
+        _raise(self._lib, self._lib.span_la_cache_put(self._live(), ks.ctypes.data, ks.size,
+                                                      states.data_ptr(), _stream_handle(stream)),
+               "span_la_cache_put")
+
+    def contains(self, keys) -> np.ndarray:
+        ks = _keys(keys)
+        present = np.zeros(ks.size, dtype=np.int32)
+        _raise(self._lib, self._lib.span_la_cache_contains(
+            self._live(), ks.ctypes.data if ks.size else None, ks.size,
+            present.ctypes.data if ks.size else None), "span_la_cache_contains")
+        return present.astype(bool)
+
+    def branches(self, parent_keys, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                 branch_cu_seqlens: Sequence[int], out: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """Branch b forks from the state cached under parent_keys[b]."""
+        dims = _dims_of(q, k, v)
+        bcu = _i32(branch_cu_seqlens)
+        B = max(len(bcu) - 1, 0)
+        ks = _keys(parent_keys)
+        if ks.size != B:
+            raise ValueError("one parent key per branch")
+        if out is None:
+            out = torch.empty_like(q)
+        if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+            raise ValueError("out must be a contiguous CUDA tensor like q")
+        _raise(self._lib, self._lib.span_la_cache_branches(
+            self._live(), ks.ctypes.data if ks.size else None, q.data_ptr(), k.data_ptr(),
+            v.data_ptr(), dims, _iptr(bcu), B, out.data_ptr(), _stream_handle(stream)),
+            "span_la_cache_branches")
+        return out
+
+    def stats(self) -> dict:
+        st = (ctypes.c_int64 * len(CACHE_FIELDS))()
+        _raise(self._lib, self._lib.span_la_cache_stats(self._live(), st), "span_la_cache_stats")
+        return dict(zip(CACHE_FIELDS, (int(x) for x in st)))
 
 
 def span_la_check(stream: Optional[torch.cuda.Stream] = None) -> None:

@@ -251,6 +251,65 @@ span_la_status span_la_profile_reset(void);
 /* Static name of kernel id k, or NULL. */
 const char *span_la_kernel_name(int32_t k);
 
+/*
+ * View-state cache ("Serving 0.88M TPS from Two RTXs and Mac Minis", section
+ * "Long Requests": the shards of a long request reuse the view's cached state
+ * instead of recomputing the view, 3.4x faster than without the cache).
+ *
+ * A cache holds up to `capacity` view final states of `num_heads` heads
+ * (fp32 [H][64][64] each, 16 KiB per head) in device memory of the device
+ * current at creation, under 64-bit keys the caller chooses (a request id, a
+ * hash of the view's tokens).  When full, a put evicts the least recently
+ * used entries; a lookup or a branch call that names a key counts as a use.
+ * The cache orders its own device memory across streams with CUDA events: a
+ * branch call waits for the put of each state it reads, and a put into a
+ * slot waits for every earlier branch call that read the state it replaces,
+ * on whatever streams they were enqueued.  The caller still orders the
+ * states a put copies from (normally by putting on the stream of the pass
+ * that wrote them).  A cache object may be used from several host threads
+ * (calls are serialised by a lock); it is not tied to a stream.
+ */
+typedef struct span_la_view_cache span_la_view_cache;
+
+/* Create a cache (cudaMalloc of capacity * num_heads * 16 KiB).  capacity >= 1,
+ * num_heads >= 1.  *cache receives the handle. */
+span_la_status span_la_cache_create(int32_t num_heads, int32_t capacity, span_la_view_cache **cache);
+
+/* Free the cache (synchronises the device first).  NULL is allowed. */
+span_la_status span_la_cache_destroy(span_la_view_cache *cache);
+
+/*
+ * Insert or refresh n states: state i (device, fp32 [H][64][64] at
+ * states + i * H * 4096) goes under keys[i] (host array of n distinct keys),
+ * copied device-to-device on `stream`.  A key already present is overwritten
+ * in place; new keys take free slots, then the least recently used slots of
+ * keys not in this call.  1 <= n <= capacity.  A typical put follows a
+ * span_la_pass on the same stream, with states = view_state_out.
+ */
+span_la_status span_la_cache_put(span_la_view_cache *cache, const uint64_t *keys, int32_t n,
+                                 const float *states, cudaStream_t stream);
+
+/* present[i] = 1 if keys[i] is cached (the entry counts as used), else 0.
+ * keys and present are host arrays of n entries. */
+span_la_status span_la_cache_contains(span_la_view_cache *cache, const uint64_t *keys, int32_t n,
+                                      int32_t *present);
+
+/*
+ * Branches forking from cached view states: as span_la_branches_from_state,
+ * with branch b starting from the state cached under parent_keys[b] (host
+ * array of num_branches keys).  Every key must be present, else
+ * SPAN_LA_ERR_INVALID and nothing is enqueued.  The branches of one long
+ * request can be run as several calls (shards) over the same cached state.
+ */
+span_la_status span_la_cache_branches(span_la_view_cache *cache, const uint64_t *parent_keys,
+                                      const void *q, const void *k, const void *v,
+                                      span_la_dims dims, const int32_t *branch_cu_seqlens,
+                                      int32_t num_branches, void *out, cudaStream_t stream);
+
+/* stats[0..5] = entries, capacity, hits, misses, evictions, puts (counts of
+ * keys; a hit or a miss is one key looked up by contains or by a branch call). */
+span_la_status span_la_cache_stats(const span_la_view_cache *cache, int64_t *stats);
+
 #ifdef __cplusplus
 }
 #endif

@@ -130,3 +130,26 @@ def test_plan_covers_every_row_once(lib, dtype, name):
         assert 1 <= G <= 8
         assert st["state_slots"] == sum(-(-int(L) // (128 * G)) for L in list(w.view_lens)
                                         + [L for L in w.branch_lens if L > 128])
+
+
+def test_view_cache_validation_without_a_device(lib):
+    """Argument checks of the view-state cache run before any CUDA call; with no
+    device, create reports the CUDA error instead of returning a handle."""
+    handle = ctypes.c_void_p(123)
+    st = lib.span_la_cache_create(0, 4, ctypes.byref(handle))
+    assert st == 1 and "num_heads" in lib.span_la_last_error_detail().decode()
+    assert handle.value is None
+    st = lib.span_la_cache_create(2, 0, ctypes.byref(handle))
+    assert st == 1 and "capacity" in lib.span_la_last_error_detail().decode()
+    st = lib.span_la_cache_create(2, 4, None)
+    assert st == 1
+    assert lib.span_la_cache_destroy(None) == 0
+    st = lib.span_la_cache_put(None, None, 1, FAKE, None)
+    assert st == 1 and "NULL" in lib.span_la_last_error_detail().decode()
+    stats = (ctypes.c_int64 * 6)()
+    assert lib.span_la_cache_stats(None, stats) == 1
+    st = lib.span_la_cache_create(2, 4, ctypes.byref(handle))
+    if st == 0:   # a device is visible after all: release it
+        assert lib.span_la_cache_destroy(handle) == 0
+    else:
+        assert st == 3 and handle.value is None
