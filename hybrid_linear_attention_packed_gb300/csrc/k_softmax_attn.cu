@@ -1,0 +1,399 @@
+// Softmax-attention kernel (bf16 inputs) over the packed rows of a pass: the
+// hybrid model's few softmax layers, on the same views and branches as its
+// linear layers.
+//
+// "Serving 0.88M TPS from Two RTXs and Mac Minis", section "The Workload"
+// (a branch sees its view and not its siblings) and section "Long Requests"
+// (the softmax layers' K/V of a view is what a branch reuses).  Per head and
+// query row t,
+//
+//     o_t = sum_j softmax_j(scale * q_t . k_j) v_j ,   lse_t = log sum_j exp(scale * q_t . k_j)
+//
+// over the keys row t sees: its own view's rows up to t, or, for a branch
+// row, all of the parent view's rows and its own branch's rows up to t.
+//
+// Work unit = one SaItem: up to 128 query rows of one head and the sequence
+// of 128-key blocks they attend to (prefix blocks, then own blocks; only the
+// last own block -- the tile itself -- is masked).  Per key block g, with the
+// usual running maximum m and sum l per row (online softmax):
+//
+//     S_g = Q K_g^T                 (tcgen05, M128 N128 K64, fp32 in TMEM)
+//     P_g = exp(scale (S_g - m_g))  (bf16, written back over S_g in TMEM)
+//     O_g = P_g V_g                 (tcgen05 with A = P_g from TMEM, M128 N64 K128)
+//     o   = o * exp(scale (m_{g-1} - m_g)) + O_g      (in registers)
+//
+// Persistent CTAs (one per SM) walk a host-built list of items.  6 warps:
+//   warp 0     producer: Q of each item, K and V of each key block, by TMA
+//              (Q double-buffered per item, K/V in a four-stage ring).
+//   warp 1     MMA issuer (one lane): S_g as soon as block g has landed and
+//              its TMEM buffer is free, then O_{g-1} once P_{g-1} is ready;
+//              S/P and O have two TMEM buffers each (g & 1).
+//   warps 2-5  softmax, one warp per TMEM lane quarter, one query row per
+//              thread: mask, running max, exponentials, row sum, P as bf16
+//              in place; then o += O_{g-1}; at the end of an item o / l (and
+//              lse) to global memory.
+#include "spanla_internal.h"
+#include "tc_ptx.cuh"
+
+namespace spanla {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kStages = 4;
+constexpr uint32_t kTileBytes = kTileRows * 128;             // 128 rows x 128 B (bf16 x 64)
+constexpr uint32_t kStageBytes = 2 * kTileBytes;             // K, V
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: S/P buffers (128 each), O buffers (64 each).
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 320;
+
+struct SaSmem {
+  static constexpr uint32_t kQ = 0;                              // two Q tiles
+  static constexpr uint32_t kStage0 = 2 * kTileBytes;
+  static constexpr uint32_t kBar = kStage0 + kStages * kStageBytes;
+  static constexpr int kFull = 0, kEmpty = kStages, kQFull = 2 * kStages, kQFree = kQFull + 2,
+                       kSReady = kQFull + 4, kPDone = kQFull + 6, kOReady = kQFull + 8,
+                       kOFree = kQFull + 10, kNumBars = kQFull + 12;
+  static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
+  static constexpr uint32_t kBytes = kTmemSlot + 8;
+  static constexpr uint32_t kRequest = kBytes + 1024;
+};
+static_assert(SaSmem::kRequest <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity, unsigned* err,
+                                             unsigned code) {
+  if (mbar_wait_bounded(bar, parity, kWaitLimitNs)) return true;
+  atomicOr(err, code);
+  return false;
+}
+
+__device__ __forceinline__ SaItem load_item(const SaItem* p) {
+  SaItem t;
+  const uint4* src = reinterpret_cast<const uint4*>(p);
+  uint4* dst = reinterpret_cast<uint4*>(&t);
+  dst[0] = __ldg(src);
+  dst[1] = __ldg(src + 1);
+  return t;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Key block jb of an item: first key row, valid keys, and whether it is the
+// item's own (masked) diagonal block.
+struct KeyBlock {
+  int32_t kr0;
+  int32_t cnt;
+  bool diag;
+};
+
+__device__ __forceinline__ int32_t num_blocks(const SaItem& it) {
+  return (it.pn + kTileRows - 1) / kTileRows + (it.r0 - it.os) / kTileRows + 1;
+}
+
+__device__ __forceinline__ KeyBlock key_block(const SaItem& it, int32_t jb) {
+  const int32_t npre = (it.pn + kTileRows - 1) / kTileRows;
+  if (jb < npre) return {it.ps + jb * kTileRows, min(kTileRows, it.pn - jb * kTileRows), false};
+  const int32_t kr0 = it.os + (jb - npre) * kTileRows;
+  return {kr0, kr0 == it.r0 ? it.nrows : kTileRows, kr0 == it.r0};
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const SaItem* __restrict__ items,
+                    const int32_t* __restrict__ cta_begin, const uint8_t* __restrict__ bounds,
+                    float scale_log2e, float scale, __nv_bfloat16* __restrict__ out,
+                    float* __restrict__ lse, int H, unsigned* __restrict__ err) {
+  using L = SaSmem;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  auto bar = [&](int slot) { return base + L::kBar + 8u * slot; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(L::kFull + s), 1);
+      mbar_init(bar(L::kEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(L::kQFull + b), 1);
+      mbar_init(bar(L::kQFree + b), 1);
+      mbar_init(bar(L::kSReady + b), 1);
+      mbar_init(bar(L::kPDone + b), kSoftmaxThreads);
+      mbar_init(bar(L::kOReady + b), 1);
+      mbar_init(bar(L::kOFree + b), kSoftmaxThreads);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const int i_begin = cta_begin[blockIdx.x];
+  const int n = cta_begin[blockIdx.x + 1] - i_begin;
+  const SaItem* list = items + i_begin;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      int g = 0;
+      for (int i = 0; i < n && ok; ++i) {
+        const SaItem it = load_item(list + i);
+        const int qb = i & 1;
+        if (!wait_or_flag(bar(L::kQFree + qb), ((i >> 1) & 1) ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(L::kQFull + qb), kTileBytes);
+        tma_load_3d(base + L::kQ + qb * kTileBytes, &tm_q, bar(L::kQFull + qb), 0, it.r0, it.head);
+        const int nb = num_blocks(it);
+        for (int jb = 0; jb < nb; ++jb, ++g) {
+          const KeyBlock kb = key_block(it, jb);
+          const int s = g % kStages;
+          if (!wait_or_flag(bar(L::kEmpty + s), ((g / kStages) & 1) ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
+          const uint32_t st = base + L::kStage0 + s * kStageBytes;
+          mbar_arrive_expect_tx(bar(L::kFull + s), kStageBytes);
+          tma_load_3d(st, &tm_k, bar(L::kFull + s), 0, kb.kr0, it.head);
+          tma_load_3d(st + kTileBytes, &tm_v, bar(L::kFull + s), 0, kb.kr0, it.head);
+        }
+      }
+      // Wait (bounded) for the loads in flight before the CTA can exit.
+      for (int u = (g > kStages ? g - kStages : 0); u < g; ++u)
+        mbar_wait_bounded(bar(L::kFull + u % kStages), (u / kStages) & 1, ok ? kWaitLimitNs : 1000000ull);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t id_pv = idesc_bf16_f32(128, 64, 0, 1);
+    int g = 0;
+    int prev_stage = -1;   // stage of block g-1, whose P V is still to issue
+    bool ok = true;
+    // O_{g-1} = P_{g-1} V_{g-1} once P_{g-1} is bf16 and its O buffer is free.
+    auto issue_pv = [&](int gp) -> bool {
+      const int b = gp & 1;
+      bool w = wait_or_flag(bar(L::kPDone + b), (gp >> 1) & 1, err, kErrTimeoutMma);
+      if (w && gp >= 2) w = wait_or_flag(bar(L::kOFree + b), ((gp - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (!__all_sync(0xffffffffu, w)) return false;
+      tc_fence_after_sync();
+      if (lane == 0) {
+        const uint32_t st = base + L::kStage0 + prev_stage * kStageBytes;
+        const uint32_t colS = b ? kColS1 : kColS0, colO = b ? kColO1 : kColO0;
+        for (int kk = 0; kk < kTileRows / 16; ++kk)
+          mma_bf16_tmem_a(tmem + colO, tmem + colS + kk * 8,
+                          smem_desc_sw128(st + kTileBytes + kk * 2048, kTileBytes, 1024), id_pv,
+                          kk > 0 ? 1u : 0u);
+        mma_commit(bar(L::kOReady + b));
+        mma_commit(bar(L::kEmpty + prev_stage));
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int i = 0; i < n && ok; ++i) {
+      const SaItem it = load_item(list + i);
+      const int qb = i & 1;
+      const uint32_t qaddr = base + L::kQ + qb * kTileBytes;
+      ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kQFull + qb), (i >> 1) & 1, err, kErrTimeoutTma));
+      const int nb = num_blocks(it);
+      for (int jb = 0; jb < nb && ok; ++jb, ++g) {
+        const KeyBlock kb = key_block(it, jb);
+        const int s = g % kStages, b = g & 1;
+        const uint32_t st = base + L::kStage0 + s * kStageBytes;
+        bool w = wait_or_flag(bar(L::kFull + s), (g / kStages) & 1, err, kErrTimeoutTma);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        if (kb.cnt < kTileRows) {
+          // V rows past the block's keys may hold anything, even NaN (rows of
+          // no segment); their P entries are 0, so make the rows 0 as well.
+          uint8_t* vrow = smem + (st + kTileBytes - base);
+          for (int q = kb.cnt * 8 + lane; q < kTileRows * 8; q += 32)
+            *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        // S/P buffer b was last read by P V of block g-2.
+        w = true;
+        if (g >= 2) w = wait_or_flag(bar(L::kOReady + b), ((g - 2) >> 1) & 1, err, kErrTimeoutMma);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after_sync();
+        if (lane == 0) {
+          const uint32_t colS = b ? kColS1 : kColS0;
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            mma_bf16(tmem + colS, smem_desc_sw128(qaddr + kk * 32, 16, 1024),
+                     smem_desc_sw128(st + kk * 32, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
+          mma_commit(bar(L::kSReady + b));
+          if (jb == nb - 1) mma_commit(bar(L::kQFree + qb));
+        }
+        __syncwarp();
+        if (g >= 1 && !issue_pv(g - 1)) { ok = false; break; }
+        prev_stage = s;
+      }
+    }
+    if (ok && g >= 1) issue_pv(g - 1);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;                 // TMEM lane quarter of this warp
+    const int row = quarter * 32 + lane;          // query row in the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    float o[kHeadDim];
+#pragma unroll
+    for (int c = 0; c < kHeadDim; ++c) o[c] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, alpha_pend = 0.f;
+    SaItem done_it{};        // item whose last block is pending
+    float m_done = 0.f, l_done = 1.f;
+    int g = 0;
+
+    // o (of item `it`) / l -> global row; lse = scale * m + log(l).
+    auto finish = [&](const SaItem& it, float m, float l) {
+      if (row < it.nrows) {
+        const float inv = 1.f / l;
+        uint4* dst = reinterpret_cast<uint4*>(out + ((static_cast<int64_t>(it.r0) + row) * H + it.head) * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                              pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                              pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                              pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+        if (lse != nullptr) lse[(static_cast<int64_t>(it.r0) + row) * H + it.head] = scale * m + logf(l);
+      }
+    };
+    // o = o * alpha + O_gp.
+    auto accumulate = [&](int gp, float alpha) -> bool {
+      const int b = gp & 1;
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + b), (gp >> 1) & 1, err, kErrTimeoutMma)))
+        return false;
+      tc_fence_after_sync();
+      const uint32_t colO = b ? kColO1 : kColO0;
+      uint32_t r0[32], r1[32];
+      tmem_ld_32cols(tmem + lane_base + colO, r0);
+      tmem_ld_32cols(tmem + lane_base + colO + 32, r1);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kOFree + b));
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        o[c] = fmaf(o[c], alpha, __uint_as_float(r0[c]));
+        o[32 + c] = fmaf(o[32 + c], alpha, __uint_as_float(r1[c]));
+      }
+      return true;
+    };
+
+    bool ok = true;
+    for (int i = 0; i < n && ok; ++i) {
+      const SaItem it = load_item(list + i);
+      int seg_start = 0;
+      for (int q = 0; q < it.nseg; ++q) {
+        const int sb = bounds[it.seg0 + q];
+        if (sb <= row) seg_start = sb;
+      }
+      const int hi_col = row < it.nrows ? row : -1;   // last visible key of the diagonal block
+      const int nb = num_blocks(it);
+      for (int jb = 0; jb < nb && ok; ++jb, ++g) {
+        const KeyBlock kb = key_block(it, jb);
+        const int b = g & 1;
+        if (jb == 0) {
+          m_done = m_run;
+          l_done = l_run;
+          m_run = -INFINITY;
+          l_run = 0.f;
+        }
+        if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kSReady + b), (g >> 1) & 1, err, kErrTimeoutMma))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t colS = b ? kColS1 : kColS0;
+        uint32_t sr[128];
+        tmem_ld_32cols(tmem + lane_base + colS, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld_32cols(tmem + lane_base + colS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_ld_32cols(tmem + lane_base + colS + 64, *reinterpret_cast<uint32_t(*)[32]>(sr + 64));
+        tmem_ld_32cols(tmem + lane_base + colS + 96, *reinterpret_cast<uint32_t(*)[32]>(sr + 96));
+        tmem_ld_wait();
+        float s[128];
+        if (kb.diag) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            s[c] = (c >= seg_start && c <= hi_col) ? __uint_as_float(sr[c]) : -INFINITY;
+        } else if (kb.cnt < kTileRows) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = c < kb.cnt ? __uint_as_float(sr[c]) : -INFINITY;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        const float m_new = fmaxf(m_run, mx);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float neg = -m_use * scale_log2e;
+        const float alpha = ex2(fmaf(m_run, scale_log2e, neg));   // 0 when m_run = -inf
+        float sum = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = ex2(fmaf(s[2 * c], scale_log2e, neg));
+          const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2e, neg));
+          sum += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        // The 128 bf16 of P go over the first 64 columns of the S buffer
+        // (all of S is in registers already).
+        tmem_st_32cols(tmem + lane_base + colS, *reinterpret_cast<uint32_t(*)[32]>(pk));
+        tmem_st_32cols(tmem + lane_base + colS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kPDone + b));
+        l_run = fmaf(l_run, alpha, sum);
+        m_run = m_new;
+        // Fold in O of the previous block (the previous item's last block when
+        // jb == 0, which then completes that item).
+        if (g >= 1) {
+          if (!accumulate(g - 1, alpha_pend)) { ok = false; break; }
+          if (jb == 0) finish(done_it, m_done, l_done);
+        }
+        alpha_pend = alpha;
+        if (jb == nb - 1) done_it = it;
+      }
+    }
+    if (ok && g >= 1 && accumulate(g - 1, alpha_pend)) finish(done_it, m_run, l_run);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_softmax_attn(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                const CUtensorMap* tm_v, const SaItem* items,
+                                const int32_t* cta_begin, int grid, const uint8_t* bounds,
+                                float scale_log2e, float scale, void* out, float* lse, int H,
+                                unsigned* err, cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  const uint32_t bytes = SaSmem::kRequest;
+  static std::atomic<uint64_t> done{0};
+  cudaError_t e = set_smem_limit_once(softmax_attn_kernel, bytes, done);
+  if (e != cudaSuccess) return e;
+  softmax_attn_kernel<<<grid, kThreads, bytes, stream>>>(tm_q[0], tm_k[0], tm_v[0], items, cta_begin, bounds,
+                                                         scale_log2e, scale,
+                                                         static_cast<__nv_bfloat16*>(out), lse, H, err);
+  return cudaGetLastError();
+}
+
+}  // namespace spanla

@@ -7,6 +7,7 @@
 // over descriptor tables built here from the host metadata, so that each step
 // is one launch for the whole pass however many views and branches it holds.
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -109,9 +110,10 @@ span_la_status device_state(DeviceState** out) {
 
 // ------------------------------------------------------------------ profiling
 constexpr int kKernelSplit = 0, kKernelChunk = 1, kKernelScan = 2, kKernelTile = 3,
-              kKernelSpanState = 4, kKernelSpanOutput = 5;
+              kKernelSpanState = 4, kKernelSpanOutput = 5, kKernelSoftmax = 6;
 const char* const kKernelNames[SPAN_LA_NUM_KERNELS] = {"split_f32", "chunk_state", "segmented_scan",
-                                                       "tile_output", "span_state", "span_output"};
+                                                       "tile_output", "span_state", "span_output",
+                                                       "softmax_attn"};
 
 std::atomic<int64_t> g_launches[SPAN_LA_NUM_KERNELS];
 std::atomic<bool> g_profiling{false};
@@ -745,6 +747,104 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
   return st;
 }
 
+// ------------------------------------------------------------------ softmax layer
+// Descriptor block of a softmax-layer plan: items, CTA ranges, segment starts.
+DescBlock make_softmax_desc(const SoftmaxPlan& plan) {
+  DescBlock d;
+  d.off_a = put(d.host, plan.items);
+  d.off_c = put(d.host, plan.cta_begin);
+  d.off_bounds = put(d.host, plan.bounds);
+  d.grid = plan.grid;
+  d.n_out_tiles = plan.items.size();
+  return d;
+}
+
+// TMA descriptors of the last softmax call's operands per device (guarded by
+// g_cache_mu).
+struct SoftmaxMaps {
+  bool valid = false;
+  const void* q = nullptr;
+  const void* k = nullptr;
+  const void* v = nullptr;
+  int64_t T = 0;
+  int H = 0;
+  DeviceOperands ops{};
+};
+SoftmaxMaps g_sa_maps[kMaxDevices];
+
+span_la_status run_softmax(const std::vector<int32_t>& key, const int32_t* view_cu, int32_t V,
+                           const int32_t* branch_cu, int32_t B, const int32_t* parent, const void* q,
+                           const void* k, const void* v, const span_la_dims& dims, float scale, void* out,
+                           float* lse, cudaStream_t stream, DeviceState* dev, int device) {
+  const int H = dims.num_heads;
+  const int64_t T = dims.total_rows;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  const bool use_cache = cap == cudaStreamCaptureStatusNone;
+  auto build = [&] { return make_softmax_desc(make_softmax_plan(view_cu, V, branch_cu, B, parent, H, dev->num_sms)); };
+  std::unique_lock<std::mutex> cache_lock(g_cache_mu, std::defer_lock);
+  DescBlock local;
+  const DescBlock* desc = nullptr;
+  const uint8_t* block = nullptr;
+  span_la_status st = SPAN_LA_OK;
+  if (use_cache) {
+    cache_lock.lock();
+    st = cached_block(key, device, stream, build, &desc, &block);
+    if (st != SPAN_LA_OK) return st;
+  } else {
+    local = build();
+    desc = &local;
+  }
+  if (desc->n_out_tiles == 0) return SPAN_LA_OK;
+
+  uint8_t* ws = nullptr;
+  if (!use_cache) {
+    const size_t bytes = std::max<size_t>(desc->host.size(), 256);
+    e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
+    if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): %s", bytes, cudaGetErrorString(e));
+    e = cudaMemcpyAsync(ws, desc->host.data(), desc->host.size(), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) st = cuda_fail(e, "cudaMemcpyAsync(descriptors)");
+    block = ws;
+  }
+  if (st == SPAN_LA_OK) {
+    DeviceOperands ops{};
+    SoftmaxMaps& mc = g_sa_maps[device & (kMaxDevices - 1)];
+    const bool hit = use_cache && mc.valid && mc.q == q && mc.k == k && mc.v == v && mc.T == T && mc.H == H;
+    if (hit) {
+      ops = mc.ops;
+    } else {
+      st = encode_map(&ops.q[0], q, T, H, kTileBoxRows, 1);
+      if (st == SPAN_LA_OK) st = encode_map(&ops.k[0], k, T, H, kTileBoxRows, 1);
+      if (st == SPAN_LA_OK) st = encode_map(&ops.v[0], v, T, H, kTileBoxRows, 1);
+      if (st == SPAN_LA_OK && use_cache) {
+        mc.valid = true;
+        mc.q = q;
+        mc.k = k;
+        mc.v = v;
+        mc.T = T;
+        mc.H = H;
+        mc.ops = ops;
+      }
+    }
+    if (st == SPAN_LA_OK) {
+      const float scale_log2e = scale * 1.4426950408889634f;
+      e = counted_launch(kKernelSoftmax, stream, [&] {
+        return launch_softmax_attn(ops.q, ops.k, ops.v, reinterpret_cast<const SaItem*>(block + desc->off_a),
+                                   reinterpret_cast<const int32_t*>(block + desc->off_c), desc->grid,
+                                   block + desc->off_bounds, scale_log2e, scale, out, lse, H, dev->err,
+                                   stream);
+      });
+      if (e != cudaSuccess) st = cuda_fail(e, "softmax attention launch");
+    }
+  }
+  if (ws != nullptr) {
+    cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (st == SPAN_LA_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync");
+  }
+  return st;
+}
+
 span_la_status check_operands(const void* q, const void* k, const void* v, void* out,
                               const span_la_dims& dims) {
   if (dims.total_rows == 0) return SPAN_LA_OK;
@@ -792,6 +892,39 @@ span_la_status span_la_pass(const void* q, const void* k, const void* v, span_la
                      dims.num_heads, dims.dtype == SPAN_LA_BF16);
   };
   return run_plan(key, build, q, k, v, dims, view_state_out, view_state_out, out, stream, dev, device);
+}
+
+span_la_status span_la_softmax_pass(const void* q, const void* k, const void* v, span_la_dims dims,
+                                    const int32_t* view_cu_seqlens, int32_t num_views,
+                                    const int32_t* branch_cu_seqlens, int32_t num_branches,
+                                    const int32_t* branch_parent, float scale, void* out, float* lse_out,
+                                    cudaStream_t stream) {
+  g_detail.clear();
+  span_la_status st = check_dims(dims);
+  if (st != SPAN_LA_OK) return st;
+  if (dims.dtype != SPAN_LA_BF16)
+    return fail(SPAN_LA_ERR_UNSUPPORTED, "the softmax layer takes bf16 inputs only (dtype %d)", dims.dtype);
+  if (!(scale >= 0.f) || !std::isfinite(scale))
+    return fail(SPAN_LA_ERR_INVALID, "scale must be finite and >= 0 (0 selects 1/sqrt(head_dim))");
+  if (scale == 0.f) scale = 1.f / std::sqrt(static_cast<float>(kHeadDim));
+  std::vector<Segment> segs;
+  if ((st = check_cu(view_cu_seqlens, num_views, dims.total_rows, "view_cu_seqlens", &segs, true)) != SPAN_LA_OK) return st;
+  if ((st = check_cu(branch_cu_seqlens, num_branches, dims.total_rows, "branch_cu_seqlens", &segs, false)) != SPAN_LA_OK) return st;
+  if ((st = check_overlap(segs)) != SPAN_LA_OK) return st;
+  if ((st = check_parents(branch_parent, num_branches, num_views)) != SPAN_LA_OK) return st;
+  if (!segs.empty() && (st = check_operands(q, k, v, out, dims)) != SPAN_LA_OK) return st;
+  if (!segs.empty() && lse_out != nullptr && (reinterpret_cast<uintptr_t>(lse_out) & 3u) != 0)
+    return fail(SPAN_LA_ERR_INVALID, "lse_out must be 4-byte aligned");
+  if (segs.empty()) return SPAN_LA_OK;
+
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != SPAN_LA_OK) return st;
+  int device = 0;
+  cudaGetDevice(&device);
+  const std::vector<int32_t> key = plan_key(device, dims.dtype, dims.num_heads, 2, dev->num_sms, view_cu_seqlens,
+                                            num_views, branch_cu_seqlens, num_branches, branch_parent);
+  return run_softmax(key, view_cu_seqlens, num_views, branch_cu_seqlens, num_branches, branch_parent, q, k, v,
+                     dims, scale, out, lse_out, stream, dev, device);
 }
 
 span_la_status span_la_branches_from_state(const float* cached_state, int32_t num_states,

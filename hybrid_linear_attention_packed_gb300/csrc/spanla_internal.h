@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <vector>
 
 namespace spanla {
 
@@ -92,6 +93,46 @@ struct WorkTile {
   uint8_t inl[kInlineBounds];
 };
 static_assert(sizeof(WorkTile) == 48, "WorkTile layout");
+
+// Softmax-attention layer over the packed rows: one work item = up to 128
+// query rows [r0, r0 + nrows) of one segment (or of several whole short
+// branches of one parent) for one head (32 bytes).  Its keys, in processing
+// order, are the prefix rows [ps, ps + pn) (the parent view of branch rows,
+// visible to every query row), then own blocks of 128 rows starting at os,
+// os + 128, ..., r0: all but the last are fully visible, and the last one is
+// the tile itself, causal, where query row i sees key row j (both relative
+// to r0) when seg_start(i) <= j <= i.  seg_start(i) is the largest entry of
+// bounds[seg0 .. seg0 + nseg) not above i (0 when nseg = 0): the start of the
+// packed branch that holds row i.
+struct SaItem {
+  int32_t r0;
+  int32_t nrows;
+  int32_t head;
+  int32_t ps;
+  int32_t pn;
+  int32_t os;
+  int32_t seg0;
+  int32_t nseg;
+};
+static_assert(sizeof(SaItem) == 32, "SaItem layout");
+
+// Host plan of a softmax layer: the items of every head, dealt to CTAs
+// (CTA c runs items [cta_begin[c], cta_begin[c+1]) in that order).
+struct SoftmaxPlan {
+  std::vector<SaItem> items;
+  std::vector<uint8_t> bounds;
+  std::vector<int32_t> cta_begin;
+  int grid = 0;
+  int64_t key_blocks = 0;    // (query tile, 128-key block) products, all heads
+};
+SoftmaxPlan make_softmax_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu, int32_t B,
+                              const int32_t* parent, int H, int max_ctas);
+
+cudaError_t launch_softmax_attn(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                const CUtensorMap* tm_v, const SaItem* items,
+                                const int32_t* cta_begin, int grid, const uint8_t* bounds,
+                                float scale_log2e, float scale, void* out, float* lse, int H,
+                                unsigned* err, cudaStream_t stream);
 
 struct DeviceOperands {
   // TMA descriptors; [0] = bf16 value (or high part), [1] = low part (fp32 inputs).

@@ -32,8 +32,8 @@ EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
             "span_la_profile_reset", "span_la_kernel_name", "span_la_plan_stats",
             "span_la_pass_noalloc", "span_la_cache_create", "span_la_cache_destroy",
             "span_la_cache_put", "span_la_cache_contains", "span_la_cache_branches",
-            "span_la_cache_stats")
-NUM_KERNELS = 6
+            "span_la_cache_stats", "span_la_softmax_pass")
+NUM_KERNELS = 7
 
 
 class SpanLAError(RuntimeError):
@@ -98,6 +98,9 @@ def load_library(path: Optional[str] = None):
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)]
         lib.span_la_plan_stats.restype = ctypes.c_int
+        lib.span_la_softmax_pass.argtypes = [vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
+                                             ctypes.c_int32, i32p, ctypes.c_float, vp, vp, vp]
+        lib.span_la_softmax_pass.restype = ctypes.c_int
         lib.span_la_cache_create.argtypes = [ctypes.c_int32, ctypes.c_int32,
                                              ctypes.POINTER(ctypes.c_void_p)]
         lib.span_la_cache_create.restype = ctypes.c_int
@@ -221,6 +224,34 @@ def span_la_branches_from_state(cached_state: torch.Tensor, q: torch.Tensor, k: 
                                          _iptr(bcu), B, _iptr(par), out.data_ptr(),
                                          _stream_handle(stream))
     _raise(lib, st, "span_la_branches_from_state")
+    return out
+
+
+def span_la_softmax_pass(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                         view_cu_seqlens: Sequence[int], branch_cu_seqlens: Sequence[int],
+                         branch_parent: Sequence[int], scale: float = 0.0,
+                         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """One softmax-attention layer over the packed rows (``span_la_softmax_pass``):
+    views causal, branches over their parent view plus their own causal prefix.
+    ``lse`` (fp32 [T, H], optional) receives the natural-log normaliser."""
+    lib = load_library()
+    dims = _dims_of(q, k, v)
+    vcu, bcu, par = _i32(view_cu_seqlens), _i32(branch_cu_seqlens), _i32(branch_parent)
+    V = max(len(vcu) - 1, 0)
+    B = max(len(bcu) - 1, 0)
+    if out is None:
+        out = torch.empty_like(q)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor like q")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda
+                            or tuple(lse.shape) != (q.shape[0], q.shape[1])):
+        raise ValueError("lse must be contiguous fp32 CUDA [T, H]")
+    st = lib.span_la_softmax_pass(q.data_ptr(), k.data_ptr(), v.data_ptr(), dims, _iptr(vcu), V,
+                                  _iptr(bcu), B, _iptr(par), float(scale), out.data_ptr(),
+                                  lse.data_ptr() if lse is not None else None,
+                                  _stream_handle(stream))
+    _raise(lib, st, "span_la_softmax_pass")
     return out
 
 

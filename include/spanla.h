@@ -224,14 +224,15 @@ span_la_status span_la_plan_stats(const int32_t *view_cu_seqlens, int32_t num_vi
 /*
  * Kernel profiling (tracing hook).  Kernels are numbered
  *   0 split_f32, 1 chunk_state, 3 tile_output (fp32 inputs),
- *   2 segmented_scan (both), 4 span_state, 5 span_output (bf16 inputs).
+ *   2 segmented_scan (both), 4 span_state, 5 span_output (bf16 inputs),
+ *   6 softmax_attn (span_la_softmax_pass).
  * Launches of every kernel are always counted.  While profiling is enabled,
  * every launch is also bracketed by two CUDA events recorded on the call's
  * stream (one device only); span_la_profile_read() waits for the pending
  * events and adds their elapsed times up.  Enabling adds two event records per
  * launch and nothing else to the work on the stream.
  */
-#define SPAN_LA_NUM_KERNELS 6
+#define SPAN_LA_NUM_KERNELS 7
 
 /* Turn event timing on (non-zero) or off. */
 span_la_status span_la_profile_enable(int32_t enable);
@@ -250,6 +251,32 @@ span_la_status span_la_profile_reset(void);
 
 /* Static name of kernel id k, or NULL. */
 const char *span_la_kernel_name(int32_t k);
+
+/*
+ * span_la_softmax_pass -- one softmax-attention layer of the hybrid model over
+ * the same packed rows ("Serving 0.88M TPS from Two RTXs and Mac Minis",
+ * section "The Workload": a branch attends to its view and never to its
+ * siblings; section "Long Requests": the softmax layers' K/V is the other
+ * half of what a view contributes to its branches).  Per head h and row t:
+ *
+ *   o_t = sum_j softmax_j(scale * q_t . k_j) v_j,   lse_t = ln sum_j exp(scale * q_t . k_j),
+ *
+ * where a view row t sees the rows of its view up to and including t, and a
+ * branch row t sees every row of its parent view plus the rows of its own
+ * branch up to and including t.  Same metadata rules and layouts as
+ * span_la_pass: q, k, v, out are device [T][H][64] bf16 (16-byte aligned);
+ * accumulation is fp32 and the probabilities enter the P V product as bf16.
+ *   scale    > 0, or 0 for 1/sqrt(64).  NaN, infinite or negative: INVALID.
+ *   lse_out  device fp32 [T][H] (4-byte aligned) or NULL (not written).
+ * Rows in no segment are not written.  dtype must be SPAN_LA_BF16, else
+ * SPAN_LA_ERR_UNSUPPORTED.  One kernel launch on `stream`, asynchronous;
+ * call span_la_check() to collect device-side wait timeouts.
+ */
+span_la_status span_la_softmax_pass(const void *q, const void *k, const void *v, span_la_dims dims,
+                                    const int32_t *view_cu_seqlens, int32_t num_views,
+                                    const int32_t *branch_cu_seqlens, int32_t num_branches,
+                                    const int32_t *branch_parent, float scale, void *out,
+                                    float *lse_out, cudaStream_t stream);
 
 /*
  * View-state cache ("Serving 0.88M TPS from Two RTXs and Mac Minis", section

@@ -1,0 +1,150 @@
+"""GPU parity of the softmax-attention layer (``span_la_softmax_pass``, through
+the C ABI) against the float64 softmax oracle on the same seeded inputs.
+
+Tolerance (bf16 inputs, written here and applied per call):
+max|o_gpu - o_ref| / max|o_ref| <= 1e-2 over the rows compared, and
+|lse_gpu - lse_ref| <= 1e-2 * max(1, |lse_ref|) elementwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import f64, rel_err, segment_rows, to_device
+from hybrid_linear_attention_packed_gb300 import (SpanLAError, span_la_check, span_la_softmax_pass,
+                                                  workloads)
+from oracle import oracle_softmax_pass, oracle_softmax_rows
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+def _run(w, dev, scale=0.0, with_lse=True):
+    q, k, v = to_device(w, dev)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((w.T, w.H), float("nan"), dtype=torch.float32, device=dev) if with_lse else None
+    span_la_softmax_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, scale=scale, out=out, lse=lse)
+    span_la_check()
+    return out, lse
+
+
+def _check_full(w, dev, scale=0.0):
+    out, lse = _run(w, dev, scale)
+    ref, ref_lse = oracle_softmax_pass(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu,
+                                       w.branch_parent, scale=scale if scale else None)
+    got, got_lse = f64(out), f64(lse)
+    seg = segment_rows(w)
+    assert not np.any(np.isnan(got[seg])), "a segment row was not written"
+    assert np.all(np.isnan(got[~seg])), "a row outside every segment was written"
+    assert np.all(np.isnan(got_lse[~seg]))
+    e = rel_err(got[seg], ref[seg])
+    el = float(np.max(np.abs(got_lse[seg] - ref_lse[seg]) / np.maximum(1.0, np.abs(ref_lse[seg]))))
+    print("%s: out %.2e lse %.2e" % (w.name, e, el))
+    assert e <= TOL and el <= TOL
+    return out
+
+
+def _check_sampled(w, dev, n_rows=96, seed=0):
+    out, lse = _run(w, dev)
+    seg = segment_rows(w)
+    got, got_lse = f64(out), f64(lse)
+    assert not np.any(np.isnan(got[seg]))
+    assert np.all(np.isnan(got[~seg]))
+    rng = np.random.default_rng(seed)
+    segrows = np.flatnonzero(seg)
+    # random rows plus the first and last rows of every tile of the first view
+    rows = set(rng.choice(segrows, size=min(n_rows, segrows.size), replace=False).tolist())
+    a, e = int(w.view_cu[0]), int(w.view_cu[1])
+    for r0 in range(a, e, 128):
+        rows.update({r0, min(r0 + 127, e - 1)})
+    for b in range(min(w.B, 4)):
+        rows.update({int(w.branch_cu[b]), int(w.branch_cu[b + 1]) - 1})
+    rows = sorted(r for r in rows if seg[r])
+    ref, ref_lse = oracle_softmax_rows(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu,
+                                       w.branch_parent, rows)
+    e_o = rel_err(got[rows], ref)
+    e_l = float(np.max(np.abs(got_lse[rows] - ref_lse) / np.maximum(1.0, np.abs(ref_lse))))
+    print("%s (%d sampled rows): out %.2e lse %.2e" % (w.name, len(rows), e_o, e_l))
+    assert e_o <= TOL and e_l <= TOL
+
+
+def test_tiny_case(cuda_device):
+    w = workloads.make_pass([130, 77], [9, 14, 20, 9, 14, 20], [0, 0, 0, 1, 1, 1], H=2,
+                            dtype="bf16", seed=0, q_scale=1.0, k_scale=1.0)
+    _check_full(w, cuda_device)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_single_request_7400_sampled(cuda_device, seed):
+    _check_sampled(workloads.single_request(seed), cuda_device, seed=seed)
+
+
+def test_packed_four_requests_sampled(cuda_device):
+    _check_sampled(workloads.packed_four(0), cuda_device)
+
+
+EDGE = [0, 1, 63, 64, 65, 127, 128, 129, 255, 256, 257]
+
+
+def test_edge_lengths(cuda_device):
+    views = EDGE
+    branches = EDGE + [300, 2, 3] + [1] * 20 + [5, 16, 7]
+    parent = [i % len(views) for i in range(len(branches))]
+    w = workloads.make_pass(views, branches, parent, H=3, dtype="bf16", seed=21, q_scale=1.0,
+                            k_scale=1.0, lead_rows=5, mid_rows=70, tail_rows=130)
+    _check_full(w, cuda_device)
+
+
+def test_many_short_siblings_packed(cuda_device):
+    """Runs of short branches of one parent share tiles; each sees only itself."""
+    lens = [1, 2, 3, 16, 7, 30, 1, 64, 9, 128, 4, 4, 4, 4, 120, 8]
+    parent = [0] * 8 + [1] * 8
+    w = workloads.make_pass([200, 90], lens, parent, H=2, dtype="bf16", seed=25, q_scale=1.0,
+                            k_scale=1.0)
+    _check_full(w, cuda_device)
+
+
+@pytest.mark.parametrize("scale", [0.03, 0.5])
+def test_other_scales(cuda_device, scale):
+    w = workloads.make_pass([300, 129], [40, 100, 5], [0, 1, 0], H=2, dtype="bf16", seed=26,
+                            q_scale=1.0, k_scale=1.0)
+    _check_full(w, cuda_device, scale=scale)
+
+
+def test_gap_rows_with_nan_inputs_do_not_leak(cuda_device):
+    w = workloads.make_pass([100, 64, 1], [20, 44, 7, 200], [0, 0, 1, 2], H=2, dtype="bf16",
+                            seed=22, q_scale=1.0, k_scale=1.0, lead_rows=3, mid_rows=9, tail_rows=64)
+    seg = segment_rows(w)
+    for t in (w.q, w.k, w.v):
+        t[torch.from_numpy(~seg)] = float("nan")
+    _check_full(w, cuda_device)
+
+
+def test_sibling_order_does_not_matter(cuda_device):
+    base = workloads.make_pass([260], [30, 50, 20, 90], [0, 0, 0, 0], H=2, dtype="bf16", seed=27,
+                               q_scale=1.0, k_scale=1.0)
+    out = f64(_run(base, cuda_device)[0])
+    perm = [3, 1, 0, 2]
+    nv = int(base.view_lens.sum())
+    rows = np.concatenate([np.arange(nv)] + [np.arange(base.branch_cu[b], base.branch_cu[b + 1])
+                                             for b in perm])
+    w = workloads.make_pass([260], [base.branch_lens[b] for b in perm], [0] * 4, H=2, dtype="bf16",
+                            seed=27)
+    w.q, w.k, w.v = base.q[rows].contiguous(), base.k[rows].contiguous(), base.v[rows].contiguous()
+    out2 = f64(_run(w, cuda_device)[0])
+    assert np.array_equal(out2[:nv], out[:nv])
+    assert rel_err(out2, out[rows]) <= TOL
+
+
+def test_rejections_and_empty_pass(cuda_device):
+    dev = cuda_device
+    q = torch.zeros((10, 2, 64), dtype=torch.float32, device=dev)
+    with pytest.raises(SpanLAError, match="bf16"):
+        span_la_softmax_pass(q, q, q, [0, 10], None, None)
+    qb = q.to(torch.bfloat16)
+    with pytest.raises(SpanLAError, match="scale"):
+        span_la_softmax_pass(qb, qb, qb, [0, 10], None, None, scale=-1.0)
+    out = torch.full_like(qb, 3.0)
+    span_la_softmax_pass(qb, qb, qb, [0], None, None, out=out)
+    span_la_check()
+    assert torch.all(out == 3.0)
