@@ -23,6 +23,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -47,6 +49,9 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--layer", choices=["linear", "softmax"], default="linear",
+                    help="linear: the packed linear-attention pass (default); softmax: the "
+                         "hybrid model's softmax-attention layer over the same packed rows")
     return ap.parse_args()
 
 
@@ -273,9 +278,212 @@ def workload_config(w, name: str) -> dict:
     return cfg
 
 
+# ---------------------------------------------------------------- softmax layer
+SOFTMAX_METRIC = "packed softmax-layer tokens/s"
+
+
+def visible_pairs(w) -> int:
+    """(query, key) pairs the softmax layer scores, per head: a view row sees its
+    view up to itself, a branch row its parent view and its branch up to itself."""
+    vl = w.view_lens.astype(np.int64) if hasattr(w.view_lens, "astype") else w.view_lens
+    n = int(sum(int(L) * (int(L) + 1) // 2 for L in vl))
+    for b in range(w.B):
+        nb = int(w.branch_lens[b])
+        n += nb * int(w.view_lens[int(w.branch_parent[b])]) + nb * (nb + 1) // 2
+    return n
+
+
+def softmax_oracle_time(w, budget_s: float = 20.0, max_reps: int = 3):
+    from oracle import oracle_softmax_pass
+    q, k, v = (t.double().numpy() for t in (w.q, w.k, w.v))
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < max_reps and (time.perf_counter() - t_all) < budget_s:
+        t0 = time.perf_counter()
+        oracle_softmax_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+        times.append(time.perf_counter() - t0)
+    return statistics.median(times), len(times)
+
+
+def softmax_cpu_line(w, value, reps, args):
+    cores = os.cpu_count() or 1
+    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "the whole workload (%d rows x %d heads), median of %d passes; numpy "
+                      "float64 (matmuls on the BLAS threads, the rest on one thread)"
+                      % (w.rows, w.H, reps),
+            "cpu_model": cpu_model()}
+
+
+def run_softmax_reference(args):
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return 0
+    from hybrid_linear_attention_packed_gb300 import workloads
+    w = workloads.by_name(args.workload, args.seed)
+    med, reps = softmax_oracle_time(w, budget_s=60.0, max_reps=max(1, min(args.steps, 10)))
+    value = w.rows / med
+    cpu = softmax_cpu_line(w, value, reps, args)
+    line = {"impl": "reference", "metric": SOFTMAX_METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": reps, "warmup": 0, "ms_per_step": med * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": dict(workload_config(w, args.workload), layer="softmax"),
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main_softmax(args):
+    """The softmax-attention layer over a packed pass: one span_la_softmax_pass
+    call per step on resident inputs, L2 flushed before every step."""
+    rank, world, local = dist_env()
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    from hybrid_linear_attention_packed_gb300 import build as libbuild
+    if rank == 0:
+        libbuild.build()
+    if pg:
+        pg.barrier()
+    from hybrid_linear_attention_packed_gb300 import spanla, workloads
+    w = workloads.by_name(args.workload, args.seed + rank)
+    if w.dtype != "bf16":
+        raise SystemExit("the softmax layer takes bf16 inputs; workload %s is %s" % (args.workload, w.dtype))
+    q, k, v = (t.to(dev).contiguous() for t in (w.q, w.k, w.v))
+    out = torch.zeros_like(q)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def run_on(qq, kk, vv, oo, strm=None):
+        spanla.span_la_softmax_pass(qq, kk, vv, w.view_cu, w.branch_cu, w.branch_parent, out=oo,
+                                    stream=strm)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        run_on(q, k, v, out)
+    spanla.span_la_check()
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_id_for_smi(torch, local))
+    time.sleep(0.5)
+    spanla.profile_reset()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        run_on(q, k, v, out)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if pg:
+        pg.barrier()
+    launches = spanla.profile_read()
+    spanla.span_la_check()
+    clock_rows = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = statistics.mean(step_ms)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    value = w.rows * world / (ms / 1e3)
+
+    # Kernel time from events around each launch, on the call's stream.
+    spanla.profile_reset()
+    spanla.profile_enable(True)
+    for _ in range(min(K, 300)):
+        flush.zero_()
+        run_on(q, k, v, out)
+    torch.cuda.synchronize()
+    spanla.profile_enable(False)
+    prof = spanla.profile_read()["softmax_attn"]
+    kern_us = prof["ms"] / max(prof["timed"], 1) * 1e3
+    pairs = visible_pairs(w)
+    flops = 4 * 64 * pairs * w.H
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        with open(pk) as f:
+            peaks = json.load(f)
+    peak = peaks.get("bf16_tflops")
+    peak_src = "measured (burst)" if peak else "fallback"
+    peak = peak or 1900.0
+    achieved = flops / (kern_us / 1e6) / 1e12
+    roofline = {"bound": "tensor", "kernel": "softmax_attn", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_source": peak_src, "alg_flops_per_launch": flops,
+                "visible_pairs_per_head": pairs,
+                "exp_per_s": pairs * w.H / (kern_us / 1e6)}
+
+    # End to end with host buffers: copy q, k, v in from pinned memory, run,
+    # read out back, each step in turn on one stream.
+    hq, hk, hv = (t.pin_memory() for t in (w.q, w.k, w.v))
+    hout = torch.empty_like(hq).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        run_on(q, k, v, out)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    KE = max(2, args.e2e_steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    spanla.span_la_check()
+    e2e_ms = e0.elapsed_time(e1) / KE
+    esize = 2
+    h2d = 3 * w.T * w.H * 64 * esize
+    d2h = w.T * w.H * 64 * esize
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        med, reps = softmax_oracle_time(w)
+        cpu = softmax_cpu_line(w, w.rows / med, reps, args)
+    if rank == 0:
+        line = {"metric": SOFTMAX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": dict(workload_config(w, args.workload), layer="softmax",
+                               parallelism="dp%d" % world),
+                "roofline": roofline,
+                "kernels": {"softmax_attn": {"avg_us": kern_us, "launches": prof["launches"]}},
+                "cpu_baseline": cpu,
+                "e2e": {"value": w.rows * world / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE,
+                        "mode": "pinned host buffers, copies and call in turn on one stream"},
+                "gpu_launches": int(sum(p["launches"] for p in launches.values())),
+                "clocks": summarize_clocks(clock_rows, t0, t1),
+                "step_ms_p50": statistics.median(step_ms), "step_ms_min": min(step_ms)}
+        print(json.dumps(line))
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse_args()
+    if args.layer == "softmax":
+        return run_softmax_reference(args) if args.impl == "reference" else main_softmax(args)
     if args.impl == "reference":
         return run_reference(args)
 

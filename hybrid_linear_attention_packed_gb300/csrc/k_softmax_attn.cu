@@ -22,40 +22,53 @@
 //     O_g = P_g V_g                 (tcgen05 with A = P_g from TMEM, M128 N64 K128)
 //     o   = o * exp(scale (m_{g-1} - m_g)) + O_g      (in registers)
 //
-// Persistent CTAs (one per SM) walk a host-built list of items.  6 warps:
+// Persistent CTAs (one per SM) walk a host-built list of items.  11 warps:
 //   warp 0     producer: Q of each item, K and V of each key block, by TMA
 //              (Q double-buffered per item, K/V in a four-stage ring).
-//   warp 1     MMA issuer (one lane): S_g as soon as block g has landed and
-//              its TMEM buffer is free, then O_{g-1} once P_{g-1} is ready;
-//              S/P and O have two TMEM buffers each (g & 1).
-//   warps 2-5  softmax, one warp per TMEM lane quarter, one query row per
-//              thread: mask, running max, exponentials, row sum, P as bf16
-//              in place; then o += O_{g-1}; at the end of an item o / l (and
-//              lse) to global memory.
+//   warp 1     S issuer (one lane): S_g as soon as block g has landed and
+//              its TMEM buffer is free.  S/P has three TMEM buffers (g mod 3),
+//              so S runs up to two blocks ahead of the softmax.
+//   warp 10    O issuer (one lane): O_g as soon as P_g is ready (O has two
+//              TMEM buffers, g & 1); it zeroes the V rows past a partial
+//              block's keys and hands the stage back to the producer.
+//   warps 2-9  softmax: two warps per TMEM lane quarter, one query row per
+//              thread pair, each thread of the pair on one half of the 128
+//              key columns (and one half of the 64 output columns): mask,
+//              running maximum (the pair swaps its halves' maxima through
+//              shared memory), exponentials, row sum, P as bf16 in place;
+//              then o += O_{g-1}; at the end of an item o / l (and lse) to
+//              global memory.
 #include "spanla_internal.h"
 #include "tc_ptx.cuh"
 
 namespace spanla {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 352;
+constexpr int kSoftmaxThreads = 256;
 constexpr int kStages = 4;
 constexpr uint32_t kTileBytes = kTileRows * 128;             // 128 rows x 128 B (bf16 x 64)
 constexpr uint32_t kStageBytes = 2 * kTileBytes;             // K, V
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S/P buffers (128 each), O buffers (64 each).
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 320;
+// TMEM columns: three S/P buffers (128 each), two O buffers (64 each).
+constexpr int kSBufs = 3;
+constexpr uint32_t kColO0 = 384, kColO1 = 448;
+__device__ __forceinline__ uint32_t col_s(int g) { return static_cast<uint32_t>(g % kSBufs) * 128u; }
 
 struct SaSmem {
   static constexpr uint32_t kQ = 0;                              // two Q tiles
   static constexpr uint32_t kStage0 = 2 * kTileBytes;
   static constexpr uint32_t kBar = kStage0 + kStages * kStageBytes;
   static constexpr int kFull = 0, kEmpty = kStages, kQFull = 2 * kStages, kQFree = kQFull + 2,
-                       kSReady = kQFull + 4, kPDone = kQFull + 6, kOReady = kQFull + 8,
-                       kOFree = kQFull + 10, kNumBars = kQFull + 12;
+                       kSReady = kQFull + 4, kPDone = kSReady + kSBufs, kPVDone = kPDone + kSBufs,
+                       kOReady = kPVDone + kSBufs, kOFree = kOReady + 2, kPair = kOFree + 2,
+                       kNumBars = kPair + 4;
   static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
-  static constexpr uint32_t kBytes = kTmemSlot + 8;
+  // Row maxima of the two column halves, [block parity][half][row], and row
+  // sums at the end of an item, [item parity][half][row].
+  static constexpr uint32_t kRedMax = kTmemSlot + 16;
+  static constexpr uint32_t kRedSum = kRedMax + 2 * 2 * 128 * 4;
+  static constexpr uint32_t kBytes = kRedSum + 2 * 2 * 128 * 4;
   static constexpr uint32_t kRequest = kBytes + 1024;
 };
 static_assert(SaSmem::kRequest <= 227 * 1024, "shared memory budget");
@@ -127,11 +140,15 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::kQFull + b), 1);
       mbar_init(bar(L::kQFree + b), 1);
-      mbar_init(bar(L::kSReady + b), 1);
-      mbar_init(bar(L::kPDone + b), kSoftmaxThreads);
       mbar_init(bar(L::kOReady + b), 1);
       mbar_init(bar(L::kOFree + b), kSoftmaxThreads);
     }
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(bar(L::kSReady + b), 1);
+      mbar_init(bar(L::kPDone + b), kSoftmaxThreads);
+      mbar_init(bar(L::kPVDone + b), 1);
+    }
+    for (int q = 0; q < 4; ++q) mbar_init(bar(L::kPair + q), 64);   // the two warps of a lane quarter
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -177,32 +194,10 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mbar_wait_bounded(bar(L::kFull + u % kStages), (u / kStages) & 1, ok ? kWaitLimitNs : 1000000ull);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t id_pv = idesc_bf16_f32(128, 64, 0, 1);
     int g = 0;
-    int prev_stage = -1;   // stage of block g-1, whose P V is still to issue
     bool ok = true;
-    // O_{g-1} = P_{g-1} V_{g-1} once P_{g-1} is bf16 and its O buffer is free.
-    auto issue_pv = [&](int gp) -> bool {
-      const int b = gp & 1;
-      bool w = wait_or_flag(bar(L::kPDone + b), (gp >> 1) & 1, err, kErrTimeoutMma);
-      if (w && gp >= 2) w = wait_or_flag(bar(L::kOFree + b), ((gp - 2) >> 1) & 1, err, kErrTimeoutMma);
-      if (!__all_sync(0xffffffffu, w)) return false;
-      tc_fence_after_sync();
-      if (lane == 0) {
-        const uint32_t st = base + L::kStage0 + prev_stage * kStageBytes;
-        const uint32_t colS = b ? kColS1 : kColS0, colO = b ? kColO1 : kColO0;
-        for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_bf16_tmem_a(tmem + colO, tmem + colS + kk * 8,
-                          smem_desc_sw128(st + kTileBytes + kk * 2048, kTileBytes, 1024), id_pv,
-                          kk > 0 ? 1u : 0u);
-        mma_commit(bar(L::kOReady + b));
-        mma_commit(bar(L::kEmpty + prev_stage));
-      }
-      __syncwarp();
-      return true;
-    };
     for (int i = 0; i < n && ok; ++i) {
       const SaItem it = load_item(list + i);
       const int qb = i & 1;
@@ -210,8 +205,37 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kQFull + qb), (i >> 1) & 1, err, kErrTimeoutTma));
       const int nb = num_blocks(it);
       for (int jb = 0; jb < nb && ok; ++jb, ++g) {
+        const int s = g % kStages, sb = g % kSBufs;
+        const uint32_t st = base + L::kStage0 + s * kStageBytes;
+        bool w = wait_or_flag(bar(L::kFull + s), (g / kStages) & 1, err, kErrTimeoutTma);
+        // S/P buffer sb was last read by P V of block g-3.
+        if (w && g >= kSBufs) w = wait_or_flag(bar(L::kPVDone + sb), ((g - kSBufs) / kSBufs) & 1, err, kErrTimeoutMma);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after_sync();
+        if (lane == 0) {
+          const uint32_t colS = col_s(g);
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            mma_bf16(tmem + colS, smem_desc_sw128(qaddr + kk * 32, 16, 1024),
+                     smem_desc_sw128(st + kk * 32, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
+          mma_commit(bar(L::kSReady + sb));
+          if (jb == nb - 1) mma_commit(bar(L::kQFree + qb));
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == kThreads / 32 - 1) {
+    // ------------------------------------------------------------ O issuer
+    // O_g = P_g V_g once P_g is bf16 and the O buffer is free; then the stage
+    // (K read by S_g, which P_g depends on, and V) goes back to the producer.
+    constexpr uint32_t id_pv = idesc_bf16_f32(128, 64, 0, 1);
+    int g = 0;
+    bool ok = true;
+    for (int i = 0; i < n && ok; ++i) {
+      const SaItem it = load_item(list + i);
+      const int nb = num_blocks(it);
+      for (int jb = 0; jb < nb && ok; ++jb, ++g) {
         const KeyBlock kb = key_block(it, jb);
-        const int s = g % kStages, b = g & 1;
+        const int s = g % kStages, sb = g % kSBufs, b = g & 1;
         const uint32_t st = base + L::kStage0 + s * kStageBytes;
         bool w = wait_or_flag(bar(L::kFull + s), (g / kStages) & 1, err, kErrTimeoutTma);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -224,70 +248,88 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           fence_proxy_async_smem();
         }
         __syncwarp();
-        // S/P buffer b was last read by P V of block g-2.
-        w = true;
-        if (g >= 2) w = wait_or_flag(bar(L::kOReady + b), ((g - 2) >> 1) & 1, err, kErrTimeoutMma);
+        w = wait_or_flag(bar(L::kPDone + sb), (g / kSBufs) & 1, err, kErrTimeoutMma);
+        if (w && g >= 2) w = wait_or_flag(bar(L::kOFree + b), ((g - 2) >> 1) & 1, err, kErrTimeoutMma);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after_sync();
         if (lane == 0) {
-          const uint32_t colS = b ? kColS1 : kColS0;
-          for (int kk = 0; kk < kHeadDim / 16; ++kk)
-            mma_bf16(tmem + colS, smem_desc_sw128(qaddr + kk * 32, 16, 1024),
-                     smem_desc_sw128(st + kk * 32, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
-          mma_commit(bar(L::kSReady + b));
-          if (jb == nb - 1) mma_commit(bar(L::kQFree + qb));
+          const uint32_t colS = col_s(g), colO = b ? kColO1 : kColO0;
+          // P of keys 0..63 is in columns 0..31 of the buffer, of keys
+          // 64..127 in columns 64..95 (one column half per softmax thread).
+          for (int kk = 0; kk < kTileRows / 16; ++kk)
+            mma_bf16_tmem_a(tmem + colO, tmem + colS + kk * 8 + (kk >= 4 ? 32 : 0),
+                            smem_desc_sw128(st + kTileBytes + kk * 2048, kTileBytes, 1024), id_pv,
+                            kk > 0 ? 1u : 0u);
+          mma_commit(bar(L::kPVDone + sb));
+          mma_commit(bar(L::kOReady + b));
+          mma_commit(bar(L::kEmpty + s));
         }
         __syncwarp();
-        if (g >= 1 && !issue_pv(g - 1)) { ok = false; break; }
-        prev_stage = s;
       }
     }
-    if (ok && g >= 1) issue_pv(g - 1);
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
+    const int half = (warp - 2) >> 2;             // key columns [64 half, 64 half + 64)
     const int row = quarter * 32 + lane;          // query row in the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    float o[kHeadDim];
+    // The two threads of a row meet on their lane quarter's mbarrier, one
+    // phase per exchange (bounded waits: a partner that gave up cannot hang
+    // this thread).
+    const uint32_t pair_bar = bar(L::kPair + quarter);
+    uint32_t pair_phase = 0;
+    auto pair_sync = [&]() -> bool {
+      mbar_arrive(pair_bar);
+      const bool w = wait_or_flag(pair_bar, pair_phase & 1, err, kErrTimeoutMma);
+      ++pair_phase;
+      return __all_sync(0xffffffffu, w);
+    };
+    float* red_max = reinterpret_cast<float*>(smem + L::kRedMax);
+    float* red_sum = reinterpret_cast<float*>(smem + L::kRedSum);
+    float o[32];                                  // output columns [32 half, 32 half + 32)
 #pragma unroll
-    for (int c = 0; c < kHeadDim; ++c) o[c] = 0.f;
+    for (int c = 0; c < 32; ++c) o[c] = 0.f;
     float m_run = -INFINITY, l_run = 0.f, alpha_pend = 0.f;
     SaItem done_it{};        // item whose last block is pending
     float m_done = 0.f, l_done = 1.f;
-    int g = 0;
+    int g = 0, items_done = 0;
 
-    // o (of item `it`) / l -> global row; lse = scale * m + log(l).
-    auto finish = [&](const SaItem& it, float m, float l) {
+    // o (of item `it`) / l -> global row; lse = scale * m + log(l).  l is the
+    // sum of the pair's two partial sums.
+    auto finish = [&](const SaItem& it, float m, float l_part) -> bool {
+      float* rs = red_sum + (items_done & 1) * 256;
+      rs[half * 128 + row] = l_part;
+      if (!pair_sync()) return false;
+      const float l = l_part + rs[(half ^ 1) * 128 + row];
+      ++items_done;
       if (row < it.nrows) {
         const float inv = 1.f / l;
-        uint4* dst = reinterpret_cast<uint4*>(out + ((static_cast<int64_t>(it.r0) + row) * H + it.head) * kHeadDim);
+        uint4* dst = reinterpret_cast<uint4*>(out + ((static_cast<int64_t>(it.r0) + row) * H + it.head) * kHeadDim) +
+                     4 * half;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
+        for (int c = 0; c < 4; ++c)
           dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
                               pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
                               pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
                               pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
-        if (lse != nullptr) lse[(static_cast<int64_t>(it.r0) + row) * H + it.head] = scale * m + logf(l);
+        if (lse != nullptr && half == 0) lse[(static_cast<int64_t>(it.r0) + row) * H + it.head] = scale * m + logf(l);
       }
+      return true;
     };
-    // o = o * alpha + O_gp.
+    // o = o * alpha + O_gp (this thread's 32 columns).
     auto accumulate = [&](int gp, float alpha) -> bool {
       const int b = gp & 1;
       if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + b), (gp >> 1) & 1, err, kErrTimeoutMma)))
         return false;
       tc_fence_after_sync();
-      const uint32_t colO = b ? kColO1 : kColO0;
-      uint32_t r0[32], r1[32];
+      const uint32_t colO = (b ? kColO1 : kColO0) + 32 * half;
+      uint32_t r0[32];
       tmem_ld_32cols(tmem + lane_base + colO, r0);
-      tmem_ld_32cols(tmem + lane_base + colO + 32, r1);
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(L::kOFree + b));
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        o[c] = fmaf(o[c], alpha, __uint_as_float(r0[c]));
-        o[32 + c] = fmaf(o[32 + c], alpha, __uint_as_float(r1[c]));
-      }
+      for (int c = 0; c < 32; ++c) o[c] = fmaf(o[c], alpha, __uint_as_float(r0[c]));
       return true;
     };
 
@@ -303,67 +345,75 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int nb = num_blocks(it);
       for (int jb = 0; jb < nb && ok; ++jb, ++g) {
         const KeyBlock kb = key_block(it, jb);
-        const int b = g & 1;
+        const int b = g & 1, sb = g % kSBufs;
         if (jb == 0) {
           m_done = m_run;
           l_done = l_run;
           m_run = -INFINITY;
           l_run = 0.f;
         }
-        if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kSReady + b), (g >> 1) & 1, err, kErrTimeoutMma))) {
+        // Visible key columns of this thread's half: [lo, hi] (relative to 64 half).
+        int lo = 0, hi = 63;
+        if (kb.diag) {
+          lo = seg_start - 64 * half;
+          hi = hi_col - 64 * half;
+        } else if (kb.cnt < kTileRows) {
+          hi = kb.cnt - 1 - 64 * half;
+        }
+        if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kSReady + sb), (g / kSBufs) & 1, err, kErrTimeoutMma))) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t colS = b ? kColS1 : kColS0;
-        uint32_t sr[128];
+        const uint32_t colS = col_s(g) + 64 * half;
+        uint32_t sr[64];
         tmem_ld_32cols(tmem + lane_base + colS, *reinterpret_cast<uint32_t(*)[32]>(sr));
         tmem_ld_32cols(tmem + lane_base + colS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-        tmem_ld_32cols(tmem + lane_base + colS + 64, *reinterpret_cast<uint32_t(*)[32]>(sr + 64));
-        tmem_ld_32cols(tmem + lane_base + colS + 96, *reinterpret_cast<uint32_t(*)[32]>(sr + 96));
         tmem_ld_wait();
-        float s[128];
-        if (kb.diag) {
+        float s[64];
+        if (__all_sync(0xffffffffu, lo <= 0 && hi >= 63)) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            s[c] = (c >= seg_start && c <= hi_col) ? __uint_as_float(sr[c]) : -INFINITY;
-        } else if (kb.cnt < kTileRows) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = c < kb.cnt ? __uint_as_float(sr[c]) : -INFINITY;
+          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
         } else {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+          for (int c = 0; c < 64; ++c) s[c] = (c >= lo && c <= hi) ? __uint_as_float(sr[c]) : -INFINITY;
         }
-        float mx = s[0];
+        float mx0 = s[0], mx1 = s[1];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 2; c < 64; c += 2) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+        }
+        float* rm = red_max + b * 256;
+        rm[half * 128 + row] = fmaxf(mx0, mx1);
+        if (!pair_sync()) { ok = false; break; }
+        const float mx = fmaxf(fmaxf(mx0, mx1), rm[(half ^ 1) * 128 + row]);
         const float m_new = fmaxf(m_run, mx);
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
         const float neg = -m_use * scale_log2e;
         const float alpha = ex2(fmaf(m_run, scale_log2e, neg));   // 0 when m_run = -inf
-        float sum = 0.f;
-        uint32_t pk[64];
+        float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < 32; ++c) {
           const float p0 = ex2(fmaf(s[2 * c], scale_log2e, neg));
           const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2e, neg));
-          sum += p0 + p1;
+          sum0 += p0;
+          sum1 += p1;
           pk[c] = pack_bf16x2(p0, p1);
         }
-        // The 128 bf16 of P go over the first 64 columns of the S buffer
-        // (all of S is in registers already).
-        tmem_st_32cols(tmem + lane_base + colS, *reinterpret_cast<uint32_t(*)[32]>(pk));
-        tmem_st_32cols(tmem + lane_base + colS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        // The 64 bf16 of this half's P go over the first 32 of its columns.
+        tmem_st_32cols(tmem + lane_base + colS, pk);
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(bar(L::kPDone + b));
-        l_run = fmaf(l_run, alpha, sum);
+        mbar_arrive(bar(L::kPDone + sb));
+        l_run = fmaf(l_run, alpha, sum0 + sum1);
         m_run = m_new;
         // Fold in O of the previous block (the previous item's last block when
         // jb == 0, which then completes that item).
         if (g >= 1) {
           if (!accumulate(g - 1, alpha_pend)) { ok = false; break; }
-          if (jb == 0) finish(done_it, m_done, l_done);
+          if (jb == 0 && !finish(done_it, m_done, l_done)) { ok = false; break; }
         }
         alpha_pend = alpha;
         if (jb == nb - 1) done_it = it;
