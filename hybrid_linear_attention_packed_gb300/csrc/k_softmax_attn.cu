@@ -14,13 +14,19 @@
 //
 // Work unit = one SaItem: up to 128 query rows of one head and the sequence
 // of 128-key blocks they attend to (prefix blocks, then own blocks; only the
-// last own block -- the tile itself -- is masked).  Per key block g, with the
-// usual running maximum m and sum l per row (online softmax):
+// last own block -- the tile itself -- is masked).  Per key block g, with a
+// reference maximum m and a running sum l per row (online softmax):
 //
 //     S_g = Q K_g^T                 (tcgen05, M128 N128 K64, fp32 in TMEM)
-//     P_g = exp(scale (S_g - m_g))  (bf16, written back over S_g in TMEM)
-//     O_g = P_g V_g                 (tcgen05 with A = P_g from TMEM, M128 N64 K128)
-//     o   = o * exp(scale (m_{g-1} - m_g)) + O_g      (in registers)
+//     P_g = exp(scale (S_g - m))    (bf16, written back over S_g in TMEM)
+//     O  += P_g V_g                 (tcgen05 with A = P_g from TMEM, M128 N64 K128,
+//                                    accumulated in TMEM over the item's blocks)
+//
+// m is raised only when a row's block maximum exceeds it by more than
+// 8 / (scale log2 e) (a factor of 2^8 in P): then O and l are first scaled by
+// exp(scale (m_old - m_new)).  Below that, P stays within [0, 2^8] and the
+// result is the same; the rescale (and with it a wait for the previous
+// product) is rare.  At the end of an item, o = O / l.
 //
 // Persistent CTAs (one per SM) walk a host-built list of items.  11 warps:
 //   warp 0     producer: Q of each item, K and V of each key block, by TMA
@@ -28,16 +34,16 @@
 //   warp 1     S issuer (one lane): S_g as soon as block g has landed and
 //              its TMEM buffer is free.  S/P has three TMEM buffers (g mod 3),
 //              so S runs up to two blocks ahead of the softmax.
-//   warp 10    O issuer (one lane): O_g as soon as P_g is ready (O has two
-//              TMEM buffers, g & 1); it zeroes the V rows past a partial
-//              block's keys and hands the stage back to the producer.
+//   warp 10    O issuer (one lane): O += P_g V_g as soon as P_g is ready, into
+//              the O buffer of the item (two, by item parity); it zeroes the V
+//              rows past a partial block's keys and hands the stage back to
+//              the producer.
 //   warps 2-9  softmax: two warps per TMEM lane quarter, one query row per
 //              thread pair, each thread of the pair on one half of the 128
 //              key columns (and one half of the 64 output columns): mask,
-//              running maximum (the pair swaps its halves' maxima through
-//              shared memory), exponentials, row sum, P as bf16 in place;
-//              then o += O_{g-1}; at the end of an item o / l (and lse) to
-//              global memory.
+//              block maximum (the pair swaps its halves' maxima through
+//              shared memory), exponentials, row sum, P as bf16 in place; at
+//              the end of an item O / l (and lse) to global memory.
 #include "spanla_internal.h"
 #include "tc_ptx.cuh"
 
@@ -50,7 +56,7 @@ constexpr int kStages = 4;
 constexpr uint32_t kTileBytes = kTileRows * 128;             // 128 rows x 128 B (bf16 x 64)
 constexpr uint32_t kStageBytes = 2 * kTileBytes;             // K, V
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: three S/P buffers (128 each), two O buffers (64 each).
+// TMEM columns: three S/P buffers (128 each), two O accumulators (64 each).
 constexpr int kSBufs = 3;
 constexpr uint32_t kColO0 = 384, kColO1 = 448;
 __device__ __forceinline__ uint32_t col_s(int g) { return static_cast<uint32_t>(g % kSBufs) * 128u; }
@@ -225,7 +231,8 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
   } else if (warp == kThreads / 32 - 1) {
     // ------------------------------------------------------------ O issuer
-    // O_g = P_g V_g once P_g is bf16 and the O buffer is free; then the stage
+    // O += P_g V_g once P_g is bf16 (and, at an item's first block, once the
+    // softmax warps have read the O buffer's previous item); then the stage
     // (K read by S_g, which P_g depends on, and V) goes back to the producer.
     constexpr uint32_t id_pv = idesc_bf16_f32(128, 64, 0, 1);
     int g = 0;
@@ -233,9 +240,11 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     for (int i = 0; i < n && ok; ++i) {
       const SaItem it = load_item(list + i);
       const int nb = num_blocks(it);
+      const int ob = i & 1;
+      const uint32_t colO = ob ? kColO1 : kColO0;
       for (int jb = 0; jb < nb && ok; ++jb, ++g) {
         const KeyBlock kb = key_block(it, jb);
-        const int s = g % kStages, sb = g % kSBufs, b = g & 1;
+        const int s = g % kStages, sb = g % kSBufs;
         const uint32_t st = base + L::kStage0 + s * kStageBytes;
         bool w = wait_or_flag(bar(L::kFull + s), (g / kStages) & 1, err, kErrTimeoutTma);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -249,19 +258,19 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         __syncwarp();
         w = wait_or_flag(bar(L::kPDone + sb), (g / kSBufs) & 1, err, kErrTimeoutMma);
-        if (w && g >= 2) w = wait_or_flag(bar(L::kOFree + b), ((g - 2) >> 1) & 1, err, kErrTimeoutMma);
+        if (w && jb == 0 && i >= 2) w = wait_or_flag(bar(L::kOFree + ob), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after_sync();
         if (lane == 0) {
-          const uint32_t colS = col_s(g), colO = b ? kColO1 : kColO0;
+          const uint32_t colS = col_s(g);
           // P of keys 0..63 is in columns 0..31 of the buffer, of keys
           // 64..127 in columns 64..95 (one column half per softmax thread).
           for (int kk = 0; kk < kTileRows / 16; ++kk)
             mma_bf16_tmem_a(tmem + colO, tmem + colS + kk * 8 + (kk >= 4 ? 32 : 0),
                             smem_desc_sw128(st + kTileBytes + kk * 2048, kTileBytes, 1024), id_pv,
-                            kk > 0 ? 1u : 0u);
+                            (jb > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(L::kPVDone + sb));
-          mma_commit(bar(L::kOReady + b));
+          if (jb == nb - 1) mma_commit(bar(L::kOReady + ob));
           mma_commit(bar(L::kEmpty + s));
         }
         __syncwarp();
@@ -273,6 +282,8 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int half = (warp - 2) >> 2;             // key columns [64 half, 64 half + 64)
     const int row = quarter * 32 + lane;          // query row in the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    float* red_max = reinterpret_cast<float*>(smem + L::kRedMax);
+    float* red_sum = reinterpret_cast<float*>(smem + L::kRedSum);
     // The two threads of a row meet on their lane quarter's mbarrier, one
     // phase per exchange (bounded waits: a partner that gave up cannot hang
     // this thread).
@@ -284,58 +295,50 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       ++pair_phase;
       return __all_sync(0xffffffffu, w);
     };
-    float* red_max = reinterpret_cast<float*>(smem + L::kRedMax);
-    float* red_sum = reinterpret_cast<float*>(smem + L::kRedSum);
-    float o[32];                                  // output columns [32 half, 32 half + 32)
-#pragma unroll
-    for (int c = 0; c < 32; ++c) o[c] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f, alpha_pend = 0.f;
-    SaItem done_it{};        // item whose last block is pending
+    // Raise m only when a block maximum exceeds it by this much (raw score
+    // units): P then stays below 2^8.
+    const float raise_margin = 8.f / scale_log2e;
+    float m_ref = -INFINITY, l_run = 0.f;
     float m_done = 0.f, l_done = 1.f;
-    int g = 0, items_done = 0;
+    SaItem done_it{};        // item whose output is still to be written
+    int done_idx = -1;
+    int g = 0;
 
-    // o (of item `it`) / l -> global row; lse = scale * m + log(l).  l is the
-    // sum of the pair's two partial sums.
-    auto finish = [&](const SaItem& it, float m, float l_part) -> bool {
-      float* rs = red_sum + (items_done & 1) * 256;
+    // O of item `it` (index ii) / l -> global row; lse = scale * m + log(l).
+    // l is the sum of the pair's two partial sums.
+    auto finish = [&](const SaItem& it, int ii, float m, float l_part) -> bool {
+      const int ob = ii & 1;
+      float* rs = red_sum + ob * 256;
       rs[half * 128 + row] = l_part;
       if (!pair_sync()) return false;
       const float l = l_part + rs[(half ^ 1) * 128 + row];
-      ++items_done;
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + ob), (ii >> 1) & 1, err, kErrTimeoutMma)))
+        return false;
+      tc_fence_after_sync();
+      uint32_t r0[32];
+      tmem_ld_32cols(tmem + lane_base + (ob ? kColO1 : kColO0) + 32 * half, r0);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kOFree + ob));
       if (row < it.nrows) {
         const float inv = 1.f / l;
         uint4* dst = reinterpret_cast<uint4*>(out + ((static_cast<int64_t>(it.r0) + row) * H + it.head) * kHeadDim) +
                      4 * half;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
-                              pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                              pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                              pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+          dst[c] = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c]) * inv, __uint_as_float(r0[8 * c + 1]) * inv),
+                              pack_bf16x2(__uint_as_float(r0[8 * c + 2]) * inv, __uint_as_float(r0[8 * c + 3]) * inv),
+                              pack_bf16x2(__uint_as_float(r0[8 * c + 4]) * inv, __uint_as_float(r0[8 * c + 5]) * inv),
+                              pack_bf16x2(__uint_as_float(r0[8 * c + 6]) * inv, __uint_as_float(r0[8 * c + 7]) * inv));
         if (lse != nullptr && half == 0) lse[(static_cast<int64_t>(it.r0) + row) * H + it.head] = scale * m + logf(l);
       }
-      return true;
-    };
-    // o = o * alpha + O_gp (this thread's 32 columns).
-    auto accumulate = [&](int gp, float alpha) -> bool {
-      const int b = gp & 1;
-      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + b), (gp >> 1) & 1, err, kErrTimeoutMma)))
-        return false;
-      tc_fence_after_sync();
-      const uint32_t colO = (b ? kColO1 : kColO0) + 32 * half;
-      uint32_t r0[32];
-      tmem_ld_32cols(tmem + lane_base + colO, r0);
-      tmem_ld_wait();
-      tc_fence_before_sync();
-      mbar_arrive(bar(L::kOFree + b));
-#pragma unroll
-      for (int c = 0; c < 32; ++c) o[c] = fmaf(o[c], alpha, __uint_as_float(r0[c]));
       return true;
     };
 
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
       const SaItem it = load_item(list + i);
+      const int ob = i & 1;
       int seg_start = 0;
       for (int q = 0; q < it.nseg; ++q) {
         const int sb = bounds[it.seg0 + q];
@@ -347,9 +350,9 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const KeyBlock kb = key_block(it, jb);
         const int b = g & 1, sb = g % kSBufs;
         if (jb == 0) {
-          m_done = m_run;
+          m_done = m_ref;
           l_done = l_run;
-          m_run = -INFINITY;
+          m_ref = -INFINITY;
           l_run = 0.f;
         }
         // Visible key columns of this thread's half: [lo, hi] (relative to 64 half).
@@ -388,10 +391,31 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         rm[half * 128 + row] = fmaxf(mx0, mx1);
         if (!pair_sync()) { ok = false; break; }
         const float mx = fmaxf(fmaxf(mx0, mx1), rm[(half ^ 1) * 128 + row]);
-        const float m_new = fmaxf(m_run, mx);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        if (jb == 0) {
+          m_ref = mx;   // the item's O starts from this block (no rescale)
+        } else if (__any_sync(0xffffffffu, mx > m_ref + raise_margin)) {
+          // Raise m for the rows that need it: O (after the previous block's
+          // product has landed) and l scale by exp(scale (m_old - m_new)).
+          const int gp = g - 1, sp = gp % kSBufs;
+          if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kPVDone + sp), (gp / kSBufs) & 1, err, kErrTimeoutMma))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const float m_new = fmaxf(m_ref, mx);
+          const float alpha = m_new == m_ref ? 1.f : ex2((m_ref - m_new) * scale_log2e);   // 0 when m_ref = -inf
+          const uint32_t colO = (ob ? kColO1 : kColO0) + 32 * half;
+          uint32_t r0[32];
+          tmem_ld_32cols(tmem + lane_base + colO, r0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r0[c] = __float_as_uint(__uint_as_float(r0[c]) * alpha);
+          tmem_st_32cols(tmem + lane_base + colO, r0);
+          l_run *= alpha;
+          m_ref = m_new;
+        }
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         const float neg = -m_use * scale_log2e;
-        const float alpha = ex2(fmaf(m_run, scale_log2e, neg));   // 0 when m_run = -inf
         float sum0 = 0.f, sum1 = 0.f;
         uint32_t pk[32];
 #pragma unroll
@@ -407,19 +431,20 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(bar(L::kPDone + sb));
-        l_run = fmaf(l_run, alpha, sum0 + sum1);
-        m_run = m_new;
-        // Fold in O of the previous block (the previous item's last block when
-        // jb == 0, which then completes that item).
-        if (g >= 1) {
-          if (!accumulate(g - 1, alpha_pend)) { ok = false; break; }
-          if (jb == 0 && !finish(done_it, m_done, l_done)) { ok = false; break; }
+        l_run += sum0 + sum1;
+        // The previous item is complete once its last product has landed:
+        // write it out now that this item's first block is under way.
+        if (jb == 0 && done_idx >= 0) {
+          if (!finish(done_it, done_idx, m_done, l_done)) { ok = false; break; }
+          done_idx = -1;
         }
-        alpha_pend = alpha;
-        if (jb == nb - 1) done_it = it;
+        if (jb == nb - 1) {
+          done_it = it;
+          done_idx = i;
+        }
       }
     }
-    if (ok && g >= 1 && accumulate(g - 1, alpha_pend)) finish(done_it, m_run, l_run);
+    if (ok && done_idx >= 0) finish(done_it, done_idx, m_ref, l_run);
   }
 
   tc_fence_before_sync();
