@@ -183,7 +183,8 @@ def chunked_method_bytes(w, esize: int) -> int:
 def kernel_sha(name: str) -> str:
     files = {"tile_output": "k_tile_output.cu", "chunk_state": "k_chunk_state.cu",
              "segmented_scan": "k_scan.cu", "split_f32": "k_misc.cu",
-             "span_state": "k_span_state.cu", "span_output": "k_span_output.cu"}
+             "span_state": "k_span_state.cu", "span_output": "k_span_output.cu",
+             "softmax_attn": "k_softmax_attn.cu"}
     p = os.path.join(ROOT, "hybrid_linear_attention_packed_gb300", "csrc", files[name])
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -419,7 +420,8 @@ def main_softmax(args):
     peak = peak or 1900.0
     achieved = flops / (kern_us / 1e6) / 1e12
     roofline = {"bound": "tensor", "kernel": "softmax_attn", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": recorded_traffic("softmax_attn", args.workload),
                 "peak_source": peak_src, "alg_flops_per_launch": flops,
                 "visible_pairs_per_head": pairs,
                 "exp_per_s": pairs * w.H / (kern_us / 1e6)}
