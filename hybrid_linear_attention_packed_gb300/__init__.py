@@ -10,6 +10,7 @@ from .spanla import (  # noqa: F401
     span_la_branches_from_state,
     span_la_check,
     span_la_pass,
+    span_la_softmax_branches_from_kv,
     span_la_softmax_pass,
     ViewStateCache,
 )

@@ -14,7 +14,9 @@
 //
 // Work unit = one SaItem: up to 128 query rows of one head and the sequence
 // of 128-key blocks they attend to (prefix blocks, then own blocks; only the
-// last own block -- the tile itself -- is masked).  Per key block g, with a
+// last own block -- the tile itself -- is masked).  Prefix blocks are read
+// through their own pair of tensor maps: the pass's K and V for branches of
+// views in the same pass, or K and V kept from the pass that ran the views.  Per key block g, with a
 // reference maximum m and a running sum l per row (online softmax):
 //
 //     S_g = Q K_g^T                 (tcgen05, M128 N128 K64, fp32 in TMEM)
@@ -122,7 +124,8 @@ __device__ __forceinline__ KeyBlock key_block(const SaItem& it, int32_t jb) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const SaItem* __restrict__ items,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_pk,
+                    const __grid_constant__ CUtensorMap tm_pv, const SaItem* __restrict__ items,
                     const int32_t* __restrict__ cta_begin, const uint8_t* __restrict__ bounds,
                     float scale_log2e, float scale, __nv_bfloat16* __restrict__ out,
                     float* __restrict__ lse, int H, unsigned* __restrict__ err) {
@@ -159,6 +162,8 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_pk);
+    tma_prefetch_desc(&tm_pv);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -191,8 +196,11 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           if (!wait_or_flag(bar(L::kEmpty + s), ((g / kStages) & 1) ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
           const uint32_t st = base + L::kStage0 + s * kStageBytes;
           mbar_arrive_expect_tx(bar(L::kFull + s), kStageBytes);
-          tma_load_3d(st, &tm_k, bar(L::kFull + s), 0, kb.kr0, it.head);
-          tma_load_3d(st + kTileBytes, &tm_v, bar(L::kFull + s), 0, kb.kr0, it.head);
+          // Prefix blocks come from the prefix arrays (the pass's own K and V,
+          // or a parent view's K and V kept from an earlier pass).
+          const bool pre = jb < (it.pn + kTileRows - 1) / kTileRows;
+          tma_load_3d(st, pre ? &tm_pk : &tm_k, bar(L::kFull + s), 0, kb.kr0, it.head);
+          tma_load_3d(st + kTileBytes, pre ? &tm_pv : &tm_v, bar(L::kFull + s), 0, kb.kr0, it.head);
         }
       }
       // Wait (bounded) for the loads in flight before the CTA can exit.
@@ -456,7 +464,8 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 }  // namespace
 
 cudaError_t launch_softmax_attn(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                                const CUtensorMap* tm_v, const SaItem* items,
+                                const CUtensorMap* tm_v, const CUtensorMap* tm_pk,
+                                const CUtensorMap* tm_pv, const SaItem* items,
                                 const int32_t* cta_begin, int grid, const uint8_t* bounds,
                                 float scale_log2e, float scale, void* out, float* lse, int H,
                                 unsigned* err, cudaStream_t stream) {
@@ -465,7 +474,8 @@ cudaError_t launch_softmax_attn(const CUtensorMap* tm_q, const CUtensorMap* tm_k
   static std::atomic<uint64_t> done{0};
   cudaError_t e = set_smem_limit_once(softmax_attn_kernel, bytes, done);
   if (e != cudaSuccess) return e;
-  softmax_attn_kernel<<<grid, kThreads, bytes, stream>>>(tm_q[0], tm_k[0], tm_v[0], items, cta_begin, bounds,
+  softmax_attn_kernel<<<grid, kThreads, bytes, stream>>>(tm_q[0], tm_k[0], tm_v[0], tm_pk[0], tm_pv[0], items,
+                                                         cta_begin, bounds,
                                                          scale_log2e, scale,
                                                          static_cast<__nv_bfloat16*>(out), lse, H, err);
   return cudaGetLastError();

@@ -766,23 +766,32 @@ struct SoftmaxMaps {
   const void* q = nullptr;
   const void* k = nullptr;
   const void* v = nullptr;
+  const void* pk = nullptr;
+  const void* pv = nullptr;
   int64_t T = 0;
+  int64_t prefix_rows = 0;
   int H = 0;
-  DeviceOperands ops{};
+  DeviceOperands ops{};   // q[0], k[0], v[0]; prefix K in k[1], prefix V in v[1]
 };
 SoftmaxMaps g_sa_maps[kMaxDevices];
 
+// One softmax-layer launch.  The items' prefix rows index pk / pv
+// ([prefix_rows][H][64]): the pass's own k / v, or the K and V of views kept
+// from an earlier pass (branches_only: the views get no tiles).
 span_la_status run_softmax(const std::vector<int32_t>& key, const int32_t* view_cu, int32_t V,
                            const int32_t* branch_cu, int32_t B, const int32_t* parent, const void* q,
-                           const void* k, const void* v, const span_la_dims& dims, float scale, void* out,
-                           float* lse, cudaStream_t stream, DeviceState* dev, int device) {
+                           const void* k, const void* v, const void* pk, const void* pv, int64_t prefix_rows,
+                           bool branches_only, const span_la_dims& dims, float scale, void* out, float* lse,
+                           cudaStream_t stream, DeviceState* dev, int device) {
   const int H = dims.num_heads;
   const int64_t T = dims.total_rows;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   cudaError_t e = cudaStreamIsCapturing(stream, &cap);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
   const bool use_cache = cap == cudaStreamCaptureStatusNone;
-  auto build = [&] { return make_softmax_desc(make_softmax_plan(view_cu, V, branch_cu, B, parent, H, dev->num_sms)); };
+  auto build = [&] {
+    return make_softmax_desc(make_softmax_plan(view_cu, V, branch_cu, B, parent, H, dev->num_sms, branches_only));
+  };
   std::unique_lock<std::mutex> cache_lock(g_cache_mu, std::defer_lock);
   DescBlock local;
   const DescBlock* desc = nullptr;
@@ -810,19 +819,36 @@ span_la_status run_softmax(const std::vector<int32_t>& key, const int32_t* view_
   if (st == SPAN_LA_OK) {
     DeviceOperands ops{};
     SoftmaxMaps& mc = g_sa_maps[device & (kMaxDevices - 1)];
-    const bool hit = use_cache && mc.valid && mc.q == q && mc.k == k && mc.v == v && mc.T == T && mc.H == H;
+    const bool hit = use_cache && mc.valid && mc.q == q && mc.k == k && mc.v == v && mc.pk == pk &&
+                     mc.pv == pv && mc.T == T && mc.prefix_rows == prefix_rows && mc.H == H;
     if (hit) {
       ops = mc.ops;
     } else {
       st = encode_map(&ops.q[0], q, T, H, kTileBoxRows, 1);
       if (st == SPAN_LA_OK) st = encode_map(&ops.k[0], k, T, H, kTileBoxRows, 1);
       if (st == SPAN_LA_OK) st = encode_map(&ops.v[0], v, T, H, kTileBoxRows, 1);
+      if (st == SPAN_LA_OK) {
+        if (pk == k && pv == v && prefix_rows == T) {
+          ops.k[1] = ops.k[0];
+          ops.v[1] = ops.v[0];
+        } else if (prefix_rows > 0) {
+          st = encode_map(&ops.k[1], pk, prefix_rows, H, kTileBoxRows, 1);
+          if (st == SPAN_LA_OK) st = encode_map(&ops.v[1], pv, prefix_rows, H, kTileBoxRows, 1);
+        } else {
+          // No prefix rows anywhere (every parent view is empty): never read.
+          ops.k[1] = ops.k[0];
+          ops.v[1] = ops.v[0];
+        }
+      }
       if (st == SPAN_LA_OK && use_cache) {
         mc.valid = true;
         mc.q = q;
         mc.k = k;
         mc.v = v;
+        mc.pk = pk;
+        mc.pv = pv;
         mc.T = T;
+        mc.prefix_rows = prefix_rows;
         mc.H = H;
         mc.ops = ops;
       }
@@ -830,7 +856,8 @@ span_la_status run_softmax(const std::vector<int32_t>& key, const int32_t* view_
     if (st == SPAN_LA_OK) {
       const float scale_log2e = scale * 1.4426950408889634f;
       e = counted_launch(kKernelSoftmax, stream, [&] {
-        return launch_softmax_attn(ops.q, ops.k, ops.v, reinterpret_cast<const SaItem*>(block + desc->off_a),
+        return launch_softmax_attn(ops.q, ops.k, ops.v, &ops.k[1], &ops.v[1],
+                                   reinterpret_cast<const SaItem*>(block + desc->off_a),
                                    reinterpret_cast<const int32_t*>(block + desc->off_c), desc->grid,
                                    block + desc->off_bounds, scale_log2e, scale, out, lse, H, dev->err,
                                    stream);
@@ -924,7 +951,45 @@ span_la_status span_la_softmax_pass(const void* q, const void* k, const void* v,
   const std::vector<int32_t> key = plan_key(device, dims.dtype, dims.num_heads, 2, dev->num_sms, view_cu_seqlens,
                                             num_views, branch_cu_seqlens, num_branches, branch_parent);
   return run_softmax(key, view_cu_seqlens, num_views, branch_cu_seqlens, num_branches, branch_parent, q, k, v,
-                     dims, scale, out, lse_out, stream, dev, device);
+                     k, v, dims.total_rows, false, dims, scale, out, lse_out, stream, dev, device);
+}
+
+span_la_status span_la_softmax_branches_from_kv(const void* view_k, const void* view_v, int64_t view_rows,
+                                                const int32_t* view_cu_seqlens, int32_t num_views,
+                                                const void* q, const void* k, const void* v, span_la_dims dims,
+                                                const int32_t* branch_cu_seqlens, int32_t num_branches,
+                                                const int32_t* branch_parent, float scale, void* out,
+                                                float* lse_out, cudaStream_t stream) {
+  g_detail.clear();
+  span_la_status st = check_dims(dims);
+  if (st != SPAN_LA_OK) return st;
+  if (dims.dtype != SPAN_LA_BF16)
+    return fail(SPAN_LA_ERR_UNSUPPORTED, "the softmax layer takes bf16 inputs only (dtype %d)", dims.dtype);
+  if (!(scale >= 0.f) || !std::isfinite(scale))
+    return fail(SPAN_LA_ERR_INVALID, "scale must be finite and >= 0 (0 selects 1/sqrt(head_dim))");
+  if (scale == 0.f) scale = 1.f / std::sqrt(static_cast<float>(kHeadDim));
+  if (view_rows < 0 || view_rows > INT32_MAX) return fail(SPAN_LA_ERR_INVALID, "view_rows %lld out of range", (long long)view_rows);
+  std::vector<Segment> vsegs, segs;
+  if ((st = check_cu(view_cu_seqlens, num_views, view_rows, "view_cu_seqlens", &vsegs, true)) != SPAN_LA_OK) return st;
+  if ((st = check_cu(branch_cu_seqlens, num_branches, dims.total_rows, "branch_cu_seqlens", &segs, false)) != SPAN_LA_OK) return st;
+  if ((st = check_overlap(segs)) != SPAN_LA_OK) return st;
+  if ((st = check_parents(branch_parent, num_branches, num_views)) != SPAN_LA_OK) return st;
+  if (segs.empty()) return SPAN_LA_OK;
+  if ((st = check_operands(q, k, v, out, dims)) != SPAN_LA_OK) return st;
+  if (!vsegs.empty() && (view_k == nullptr || view_v == nullptr || !aligned16(view_k) || !aligned16(view_v)))
+    return fail(SPAN_LA_ERR_INVALID, "view_k and view_v must be non-NULL and 16-byte aligned");
+  if (lse_out != nullptr && (reinterpret_cast<uintptr_t>(lse_out) & 3u) != 0)
+    return fail(SPAN_LA_ERR_INVALID, "lse_out must be 4-byte aligned");
+
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != SPAN_LA_OK) return st;
+  int device = 0;
+  cudaGetDevice(&device);
+  const std::vector<int32_t> key = plan_key(device, dims.dtype, dims.num_heads, 3, dev->num_sms, view_cu_seqlens,
+                                            num_views, branch_cu_seqlens, num_branches, branch_parent);
+  return run_softmax(key, view_cu_seqlens, num_views, branch_cu_seqlens, num_branches, branch_parent, q, k, v,
+                     view_k, view_v, vsegs.empty() ? 0 : view_rows, true, dims, scale, out, lse_out, stream, dev,
+                     device);
 }
 
 span_la_status span_la_branches_from_state(const float* cached_state, int32_t num_states,

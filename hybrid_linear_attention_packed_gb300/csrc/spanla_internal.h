@@ -97,8 +97,8 @@ static_assert(sizeof(WorkTile) == 48, "WorkTile layout");
 // Softmax-attention layer over the packed rows: one work item = up to 128
 // query rows [r0, r0 + nrows) of one segment (or of several whole short
 // branches of one parent) for one head (32 bytes).  Its keys, in processing
-// order, are the prefix rows [ps, ps + pn) (the parent view of branch rows,
-// visible to every query row), then own blocks of 128 rows starting at os,
+// order, are the prefix rows [ps, ps + pn) of the prefix arrays (the parent
+// view of branch rows, visible to every query row), then own blocks of 128 rows starting at os,
 // os + 128, ..., r0: all but the last are fully visible, and the last one is
 // the tile itself, causal, where query row i sees key row j (both relative
 // to r0) when seg_start(i) <= j <= i.  seg_start(i) is the largest entry of
@@ -125,11 +125,16 @@ struct SoftmaxPlan {
   int grid = 0;
   int64_t key_blocks = 0;    // (query tile, 128-key block) products, all heads
 };
+// With branches_only, views get no tiles (their K and V are a prefix source
+// only: branches over K and V kept from an earlier pass).
 SoftmaxPlan make_softmax_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu, int32_t B,
-                              const int32_t* parent, int H, int max_ctas);
+                              const int32_t* parent, int H, int max_ctas, bool branches_only = false);
 
+// tm_pk / tm_pv: the arrays the items' prefix rows index (ps) -- the same as
+// tm_k / tm_v within one pass.
 cudaError_t launch_softmax_attn(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                                const CUtensorMap* tm_v, const SaItem* items,
+                                const CUtensorMap* tm_v, const CUtensorMap* tm_pk,
+                                const CUtensorMap* tm_pv, const SaItem* items,
                                 const int32_t* cta_begin, int grid, const uint8_t* bounds,
                                 float scale_log2e, float scale, void* out, float* lse, int H,
                                 unsigned* err, cudaStream_t stream);

@@ -28,14 +28,15 @@ int32_t blocks_of(const SaItem& it) {
 }  // namespace
 
 SoftmaxPlan make_softmax_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu, int32_t B,
-                              const int32_t* parent, int H, int max_ctas) {
+                              const int32_t* parent, int H, int max_ctas, bool branches_only) {
   SoftmaxPlan plan;
   std::vector<SaItem> tiles;   // head 0; replicated per head below
   auto add_segment = [&](int32_t a, int32_t e, int32_t ps, int32_t pn) {
     for (int32_t r0 = a; r0 < e; r0 += kTileRows)
       tiles.push_back({r0, std::min<int32_t>(kTileRows, e - r0), 0, ps, pn, a, 0, 0});
   };
-  for (int32_t s = 0; s < V; ++s) add_segment(view_cu[s], view_cu[s + 1], 0, 0);
+  if (!branches_only)
+    for (int32_t s = 0; s < V; ++s) add_segment(view_cu[s], view_cu[s + 1], 0, 0);
   for (int32_t b = 0; b < B;) {
     const int32_t a = branch_cu[b], e = branch_cu[b + 1];
     const int32_t p = parent[b];

@@ -32,7 +32,7 @@ EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
             "span_la_profile_reset", "span_la_kernel_name", "span_la_plan_stats",
             "span_la_pass_noalloc", "span_la_cache_create", "span_la_cache_destroy",
             "span_la_cache_put", "span_la_cache_contains", "span_la_cache_branches",
-            "span_la_cache_stats", "span_la_softmax_pass")
+            "span_la_cache_stats", "span_la_softmax_pass", "span_la_softmax_branches_from_kv")
 NUM_KERNELS = 7
 
 
@@ -101,6 +101,10 @@ def load_library(path: Optional[str] = None):
         lib.span_la_softmax_pass.argtypes = [vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
                                              ctypes.c_int32, i32p, ctypes.c_float, vp, vp, vp]
         lib.span_la_softmax_pass.restype = ctypes.c_int
+        lib.span_la_softmax_branches_from_kv.argtypes = [vp, vp, ctypes.c_int64, i32p, ctypes.c_int32,
+                                                         vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
+                                                         ctypes.c_float, vp, vp, vp]
+        lib.span_la_softmax_branches_from_kv.restype = ctypes.c_int
         lib.span_la_cache_create.argtypes = [ctypes.c_int32, ctypes.c_int32,
                                              ctypes.POINTER(ctypes.c_void_p)]
         lib.span_la_cache_create.restype = ctypes.c_int
@@ -252,6 +256,41 @@ def span_la_softmax_pass(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                   lse.data_ptr() if lse is not None else None,
                                   _stream_handle(stream))
     _raise(lib, st, "span_la_softmax_pass")
+    return out
+
+
+def span_la_softmax_branches_from_kv(view_k: torch.Tensor, view_v: torch.Tensor,
+                                     view_cu_seqlens: Sequence[int], q: torch.Tensor, k: torch.Tensor,
+                                     v: torch.Tensor, branch_cu_seqlens: Sequence[int],
+                                     branch_parent: Sequence[int], scale: float = 0.0,
+                                     out: Optional[torch.Tensor] = None,
+                                     lse: Optional[torch.Tensor] = None,
+                                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Softmax-layer branches over their parent views' K and V kept from an
+    earlier pass (``span_la_softmax_branches_from_kv``)."""
+    lib = load_library()
+    dims = _dims_of(q, k, v)
+    for name, t in (("view_k", view_k), ("view_v", view_v)):
+        if (not t.is_cuda or t.dtype != q.dtype or not t.is_contiguous() or t.dim() != 3
+                or tuple(t.shape[1:]) != tuple(q.shape[1:])):
+            raise ValueError("%s must be a contiguous CUDA tensor [rows, H, 64] like q" % name)
+    if view_k.shape != view_v.shape:
+        raise ValueError("view_k and view_v must share shape")
+    vcu, bcu, par = _i32(view_cu_seqlens), _i32(branch_cu_seqlens), _i32(branch_parent)
+    V = max(len(vcu) - 1, 0)
+    B = max(len(bcu) - 1, 0)
+    if out is None:
+        out = torch.empty_like(q)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor like q")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda
+                            or tuple(lse.shape) != (q.shape[0], q.shape[1])):
+        raise ValueError("lse must be contiguous fp32 CUDA [T, H]")
+    st = lib.span_la_softmax_branches_from_kv(
+        view_k.data_ptr(), view_v.data_ptr(), view_k.shape[0], _iptr(vcu), V, q.data_ptr(),
+        k.data_ptr(), v.data_ptr(), dims, _iptr(bcu), B, _iptr(par), float(scale), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None, _stream_handle(stream))
+    _raise(lib, st, "span_la_softmax_branches_from_kv")
     return out
 
 

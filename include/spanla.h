@@ -279,6 +279,30 @@ span_la_status span_la_softmax_pass(const void *q, const void *k, const void *v,
                                     float *lse_out, cudaStream_t stream);
 
 /*
+ * span_la_softmax_branches_from_kv -- the softmax layer for branches only,
+ * each attending to its parent view's K and V kept from an earlier pass (the
+ * softmax half of the view cache: "Serving 0.88M TPS from Two RTXs and Mac
+ * Minis", section "Long Requests") and to its own branch's rows up to itself.
+ * Equals the branch rows of span_la_softmax_pass over the views and branches
+ * together; the branches of one long request can be run as several calls
+ * (shards) over the same view K/V.
+ *   view_k, view_v   device bf16 [view_rows][H][64], 16-byte aligned; view p
+ *                    is rows [view_cu_seqlens[p], view_cu_seqlens[p+1]) of them.
+ *   q, k, v, out     device bf16 [T][H][64] (T = dims.total_rows) holding the
+ *                    branch rows at branch_cu_seqlens; branch b's parent is
+ *                    view branch_parent[b] of view_cu_seqlens.
+ *   scale, lse_out   as span_la_softmax_pass.
+ * Rows of out outside the branches are not written.
+ */
+span_la_status span_la_softmax_branches_from_kv(const void *view_k, const void *view_v, int64_t view_rows,
+                                                const int32_t *view_cu_seqlens, int32_t num_views,
+                                                const void *q, const void *k, const void *v,
+                                                span_la_dims dims, const int32_t *branch_cu_seqlens,
+                                                int32_t num_branches, const int32_t *branch_parent,
+                                                float scale, void *out, float *lse_out,
+                                                cudaStream_t stream);
+
+/*
  * View-state cache ("Serving 0.88M TPS from Two RTXs and Mac Minis", section
  * "Long Requests": the shards of a long request reuse the view's cached state
  * instead of recomputing the view, 3.4x faster than without the cache).

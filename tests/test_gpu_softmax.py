@@ -148,3 +148,63 @@ def test_rejections_and_empty_pass(cuda_device):
     span_la_softmax_pass(qb, qb, qb, [0], None, None, out=out)
     span_la_check()
     assert torch.all(out == 3.0)
+
+
+def test_branches_from_kept_view_kv_equal_in_pass_branches(cuda_device):
+    """The long-request procedure for the softmax layer: the view's K and V are
+    kept (copied away) from the pass that ran it; the 256 branches then run over
+    them, as one call and as 4 shard calls, from a buffer of branch rows only."""
+    from hybrid_linear_attention_packed_gb300 import span_la_softmax_branches_from_kv
+    w = workloads.cached_long(0)
+    q, k, v = to_device(w, cuda_device)
+    whole = torch.full_like(q, float("nan"))
+    span_la_softmax_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, out=whole)
+    nv = int(w.view_cu[-1])
+    view_k, view_v = k[:nv].clone(), v[:nv].clone()
+    qb, kb, vb = q[nv:].contiguous(), k[nv:].contiguous(), v[nv:].contiguous()
+    bcu = (w.branch_cu - nv).astype(np.int32)
+    one = torch.full_like(qb, float("nan"))
+    lse = torch.full((qb.shape[0], w.H), float("nan"), dtype=torch.float32, device=cuda_device)
+    span_la_softmax_branches_from_kv(view_k, view_v, w.view_cu, qb, kb, vb, bcu, w.branch_parent,
+                                     out=one, lse=lse)
+    shards = torch.full_like(qb, float("nan"))
+    for cu in workloads.shards(w, 4):
+        cu = (cu - nv).astype(np.int32)
+        span_la_softmax_branches_from_kv(view_k, view_v, w.view_cu, qb, kb, vb, cu,
+                                         np.zeros(len(cu) - 1, np.int32), out=shards)
+    span_la_check()
+    # same tiles, same keys: bit for bit the branch rows of the whole pass
+    assert torch.equal(one, whole[nv:])
+    assert not torch.isnan(shards).any()
+    rows = np.random.default_rng(3).choice(qb.shape[0], size=64, replace=False)
+    rows = sorted(set(rows.tolist()) | {0, qb.shape[0] - 1})
+    ref, ref_lse = oracle_softmax_rows(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu,
+                                       w.branch_parent, [nv + r for r in rows])
+    e1 = rel_err(f64(one)[rows], ref)
+    e4 = rel_err(f64(shards)[rows], ref)
+    el = float(np.max(np.abs(f64(lse)[rows] - ref_lse) / np.maximum(1.0, np.abs(ref_lse))))
+    print("branches from kept K/V: one call %.2e, 4 shards %.2e, lse %.2e" % (e1, e4, el))
+    assert max(e1, e4, el) <= TOL
+
+
+def test_branches_from_kv_several_views_and_rejections(cuda_device):
+    from hybrid_linear_attention_packed_gb300 import span_la_softmax_branches_from_kv
+    w = workloads.make_pass([129, 0, 300], [5, 130, 64, 1], [2, 0, 1, 2], H=2, dtype="bf16", seed=31,
+                            q_scale=1.0, k_scale=1.0)
+    q, k, v = to_device(w, cuda_device)
+    whole = torch.full_like(q, float("nan"))
+    span_la_softmax_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, out=whole)
+    nv = int(w.view_cu[-1])
+    out = torch.full_like(q, float("nan"))
+    # the pass's own arrays as the kept K/V: branch rows in place
+    span_la_softmax_branches_from_kv(k[:nv].clone(), v[:nv].clone(), w.view_cu, q, k, v, w.branch_cu,
+                                     w.branch_parent, out=out)
+    span_la_check()
+    assert torch.equal(out[nv:], whole[nv:])
+    assert torch.isnan(out[:nv]).all()
+    with pytest.raises(SpanLAError):
+        span_la_softmax_branches_from_kv(k[:nv], v[:nv], [0, nv + 1], q, k, v, w.branch_cu[:2], [0],
+                                         out=out)
+    with pytest.raises(SpanLAError, match="branch_parent"):
+        span_la_softmax_branches_from_kv(k[:nv], v[:nv], w.view_cu, q, k, v, w.branch_cu[:2], [3],
+                                         out=out)
