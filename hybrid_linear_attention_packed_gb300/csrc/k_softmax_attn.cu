@@ -103,6 +103,33 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Paired fp32 arithmetic (one instruction for two lanes of a 64-bit register
+// pair) and the three-input maximum, which halve the per-element instruction
+// count of the softmax loops.
+__device__ __forceinline__ uint64_t pair_f32(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpair_f32(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Key block jb of an item: first key row, valid keys, and whether it is the
 // item's own (masked) diagonal block.
 struct KeyBlock {
@@ -389,11 +416,11 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
           for (int c = 0; c < 64; ++c) s[c] = (c >= lo && c <= hi) ? __uint_as_float(sr[c]) : -INFINITY;
         }
-        float mx0 = s[0], mx1 = s[1];
+        float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
 #pragma unroll
-        for (int c = 2; c < 64; c += 2) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
+        for (int c = 4; c < 64; c += 4) {
+          mx0 = max3(mx0, s[c], s[c + 1]);
+          mx1 = max3(mx1, s[c + 2], s[c + 3]);
         }
         float* rm = red_max + b * 256;
         rm[half * 128 + row] = fmaxf(mx0, mx1);
@@ -424,16 +451,23 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         const float neg = -m_use * scale_log2e;
-        float sum0 = 0.f, sum1 = 0.f;
+        // p = 2^(s c - m c) two lanes at a time; two paired partial sums.
+        const uint64_t c2 = pair_f32(scale_log2e, scale_log2e), n2 = pair_f32(neg, neg);
+        uint64_t acc0 = pair_f32(0.f, 0.f), acc1 = acc0;
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float p0 = ex2(fmaf(s[2 * c], scale_log2e, neg));
-          const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2e, neg));
-          sum0 += p0;
-          sum1 += p1;
+          float x0, x1;
+          unpair_f32(fma_f32x2(pair_f32(s[2 * c], s[2 * c + 1]), c2, n2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          if (c & 1) acc1 = add_f32x2(acc1, pair_f32(p0, p1));
+          else acc0 = add_f32x2(acc0, pair_f32(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
         }
+        float a0, a1, b0, b1;
+        unpair_f32(acc0, a0, a1);
+        unpair_f32(acc1, b0, b1);
+        const float sum0 = a0 + b0, sum1 = a1 + b1;
         // The 64 bf16 of this half's P go over the first 32 of its columns.
         tmem_st_32cols(tmem + lane_base + colS, pk);
         tmem_st_wait();
