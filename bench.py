@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--per-request", action="store_true",
+                    help="run each request of the workload (a view and its branches) as its own "
+                         "pass instead of one shared pass (the page's shared-branch-pass lever)")
     ap.add_argument("--layer", choices=["linear", "softmax"], default="linear",
                     help="linear: the packed linear-attention pass (default); softmax: the "
                          "hybrid model's softmax-attention layer over the same packed rows")
@@ -276,6 +279,13 @@ def workload_config(w, name: str) -> dict:
     if name == "cached_long":
         cfg["step"] = ("span_la_branches_from_state over the view's cached final state, 4 shards "
                        "of 64 branches; tokens/s counts branch rows")
+    return cfg
+
+
+def add_mode(cfg: dict, args) -> dict:
+    if getattr(args, "per_request", False):
+        cfg = dict(cfg, step="one span_la_pass per request (view + its branches) over the same "
+                             "buffers, instead of one shared pass")
     return cfg
 
 
@@ -531,6 +541,25 @@ def main():
         def run_on(qq, kk, vv, oo, ss, strm=None):
             for cu, par in zip(shard_cu, shard_par):
                 spanla.span_la_branches_from_state(cached, qq, kk, vv, cu, par, out=oo, stream=strm)
+    elif args.per_request:
+        # One pass per request over the same buffers: view v and its branches
+        # (contiguous in the branch list, grouped by parent).
+        rows_per_step = w.rows
+        row_lo = 0
+        req_calls = []
+        for vi in range(w.V):
+            bsel = np.flatnonzero(w.branch_parent == vi)
+            if bsel.size and bsel[-1] - bsel[0] + 1 != bsel.size:
+                raise SystemExit("--per-request needs each view's branches listed together")
+            bcu_r = (np.ascontiguousarray(w.branch_cu[bsel[0]:bsel[-1] + 2], dtype=np.int32)
+                     if bsel.size else np.zeros(0, np.int32))
+            req_calls.append((np.ascontiguousarray(w.view_cu[vi:vi + 2], dtype=np.int32), bcu_r,
+                              np.zeros(bsel.size, np.int32), vi))
+
+        def run_on(qq, kk, vv, oo, ss, strm=None):
+            for vcu_r, bcu_r, par_r, vi in req_calls:
+                spanla.span_la_pass(qq, kk, vv, vcu_r, bcu_r, par_r, out=oo,
+                                    view_state_out=ss[vi:vi + 1], stream=strm)
     else:
         rows_per_step = w.rows
         row_lo = 0
@@ -598,6 +627,11 @@ def main():
         plan = None
         for cu, par in zip(shard_cu, shard_par):
             st_ = spanla.plan_stats([], cu, par, w.H, w.dtype, num_parents=1, from_state=True)
+            plan = st_ if plan is None else {key: plan[key] + st_[key] for key in plan}
+    elif args.per_request:
+        plan = None
+        for vcu_r, bcu_r, par_r, _ in req_calls:
+            st_ = spanla.plan_stats(vcu_r, bcu_r, par_r, w.H, w.dtype)
             plan = st_ if plan is None else {key: plan[key] + st_[key] for key in plan}
     else:
         plan = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H, w.dtype)
@@ -721,6 +755,12 @@ def main():
         raw = [(cached.data_ptr(), 1, q.data_ptr(), k.data_ptr(), v.data_ptr(), dims, cu.ctypes.data,
                 len(cu) - 1, par.ctypes.data, out.data_ptr(), sh) for cu, par in zip(shard_cu, shard_par)]
         fn = lib.span_la_branches_from_state
+    elif args.per_request:
+        raw = [(q.data_ptr(), k.data_ptr(), v.data_ptr(), dims, vcu_r.ctypes.data, 1,
+                bcu_r.ctypes.data if len(bcu_r) else None, max(len(bcu_r) - 1, 0),
+                par_r.ctypes.data if len(par_r) else None, out.data_ptr(),
+                state[vi:vi + 1].data_ptr(), sh) for vcu_r, bcu_r, par_r, vi in req_calls]
+        fn = lib.span_la_pass
     else:
         vcu, bcu, par = (np.ascontiguousarray(a, dtype=np.int32) for a in (w.view_cu, w.branch_cu, w.branch_parent))
         raw = [(q.data_ptr(), k.data_ptr(), v.data_ptr(), dims, vcu.ctypes.data, len(vcu) - 1,
@@ -767,7 +807,7 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": vs, "dtype": w.dtype, "data": "synthetic",
-                "config": dict(workload_config(w, args.workload), parallelism="dp%d" % world),
+                "config": dict(add_mode(workload_config(w, args.workload), args), parallelism="dp%d" % world),
                 "roofline": roofline, "pass_roofline": pass_roofline,
                 "kernels": kernels, "plan": plan,
                 "cpu_baseline": cpu,
