@@ -153,3 +153,48 @@ def test_view_cache_validation_without_a_device(lib):
         assert lib.span_la_cache_destroy(handle) == 0
     else:
         assert st == 3 and handle.value is None
+
+
+def _softmax(lib, vcu, bcu, par, dims=None, scale=0.0, lse=None, q=FAKE):
+    dims = dims or _dims()
+    (va, vp), (ba, bp), (pa, pp) = _arr(vcu), _arr(bcu), _arr(par)
+    V, B = max(len(va) - 1, 0), max(len(ba) - 1, 0)
+    st = lib.span_la_softmax_pass(q, q, q, dims, vp if V else None, V, bp if B else None, B,
+                                  pp if B else None, scale, q, lse, None)
+    return st, lib.span_la_last_error_detail().decode()
+
+
+def test_softmax_layer_validation(lib):
+    """The softmax layer checks its arguments on the host before any CUDA call."""
+    st, detail = _softmax(lib, [0, 10], [], [], dims=_dims(dtype=1))
+    assert st == 2 and "bf16" in detail
+    st, detail = _softmax(lib, [0, 10], [], [], scale=-0.5)
+    assert st == 1 and "scale" in detail
+    st, detail = _softmax(lib, [0, 10], [], [], scale=float("nan"))
+    assert st == 1 and "scale" in detail
+    st, detail = _softmax(lib, [0, 10], [], [], lse=FAKE + 2)
+    assert st == 1 and "lse_out" in detail
+    st, detail = _softmax(lib, [0, 50], [40, 60], [0])
+    assert st == 1 and "overlap" in detail
+    st, detail = _softmax(lib, [0, 50], [50, 60], [1])
+    assert st == 1 and "branch_parent" in detail
+    st, detail = _softmax(lib, [0, 10], [], [], q=FAKE + 8)
+    assert st == 1 and "aligned" in detail
+    st, detail = _softmax(lib, [0], [], [], q=0)
+    assert st == 0     # nothing to do: no CUDA call
+
+
+def test_softmax_branches_from_kv_validation(lib):
+    (va, vp), (ba, bp), (pa, pp) = _arr([0, 30]), _arr([0, 10, 20]), _arr([0, 1])
+    st = lib.span_la_softmax_branches_from_kv(FAKE, FAKE, 30, vp, 1, FAKE, FAKE, FAKE, _dims(), bp, 2,
+                                              pp, 0.0, FAKE, None, None)
+    assert st == 1 and "branch_parent" in lib.span_la_last_error_detail().decode()
+    (va, vp) = _arr([0, 31])
+    (pa, pp) = _arr([0, 0])
+    st = lib.span_la_softmax_branches_from_kv(FAKE, FAKE, 30, vp, 1, FAKE, FAKE, FAKE, _dims(), bp, 2,
+                                              pp, 0.0, FAKE, None, None)
+    assert st == 1 and "view_cu_seqlens" in lib.span_la_last_error_detail().decode()
+    (va, vp) = _arr([0, 30])
+    st = lib.span_la_softmax_branches_from_kv(0, FAKE, 30, vp, 1, FAKE, FAKE, FAKE, _dims(), bp, 2,
+                                              pp, 0.0, FAKE, None, None)
+    assert st == 1 and "view_k" in lib.span_la_last_error_detail().decode()
