@@ -83,6 +83,12 @@ def test_packed_four_requests_sampled(cuda_device):
     _check_sampled(workloads.packed_four(0), cuda_device)
 
 
+@pytest.mark.parametrize("n_views", [4, 16])
+def test_sweep_sampled(cuda_device, n_views):
+    """Full-size sweep passes (views log-U[500,18000], log-U[1,300] branches each)."""
+    _check_sampled(workloads.sweep(n_views, 0), cuda_device, n_rows=128, seed=n_views)
+
+
 EDGE = [0, 1, 63, 64, 65, 127, 128, 129, 255, 256, 257]
 
 
