@@ -361,7 +361,7 @@ def main_softmax(args):
         libbuild.build()
     if pg:
         pg.barrier()
-    from hybrid_linear_attention_packed_gb300 import spanla, workloads
+    from hybrid_linear_attention_packed_gb300 import sharding, spanla, workloads
     w = workloads.by_name(args.workload, args.seed + rank)
     if w.dtype != "bf16":
         raise SystemExit("the softmax layer takes bf16 inputs; workload %s is %s" % (args.workload, w.dtype))
@@ -401,11 +401,7 @@ def main_softmax(args):
     spanla.span_la_check()
     clock_rows = sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    ms = statistics.mean(step_ms)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = sharding.max_over_ranks(statistics.mean(step_ms), pg, dev)
     value = w.rows * world / (ms / 1e3)
 
     # Kernel time from events around each launch, on the call's stream.
@@ -515,7 +511,7 @@ def main():
         libbuild.build()
     if pg:
         pg.barrier()
-    from hybrid_linear_attention_packed_gb300 import spanla, workloads
+    from hybrid_linear_attention_packed_gb300 import sharding, spanla, workloads
 
     # Weak scaling: every rank runs its own pass (independent requests).
     w = workloads.by_name(args.workload, args.seed + rank)
@@ -600,11 +596,7 @@ def main():
     clock_rows = sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = statistics.mean(step_ms)
-    ms_max = ms
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = sharding.max_over_ranks(ms, pg, dev)
     rows_total = rows_per_step * world
     value = rows_total / (ms_max / 1e3)
 
@@ -729,11 +721,7 @@ def main():
     e_end.record(s_in)
     torch.cuda.synchronize()
     spanla.span_la_check()
-    e2e_ms = e_start.elapsed_time(e_end) / KE
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = sharding.max_over_ranks(e_start.elapsed_time(e_end) / KE, pg, dev)
     # Host time to enqueue one call (the device kept busy so that no launch
     # waits on it), and the device time per call with the L2 warm: calls
     # enqueued back to back with no flush between them.
