@@ -43,6 +43,18 @@ span_la_status cuda_fail(cudaError_t e, const char* what) {
   return fail(SPAN_LA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Fault injection (span_la_fault_inject): the next g_fail_allocs device
+// allocations of the library fail as if the device were out of memory.
+std::atomic<int32_t> g_fail_allocs{0};
+
+bool injected_alloc_failure() {
+  int32_t n = g_fail_allocs.load(std::memory_order_relaxed);
+  while (n > 0) {
+    if (g_fail_allocs.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) return true;
+  }
+  return false;
+}
+
 // ------------------------------------------------------------------ per-device state
 constexpr int kMaxDevices = 64;
 
@@ -579,6 +591,8 @@ span_la_status cached_block(const std::vector<int32_t>& key, int device, cudaStr
   en.key = key;
   en.desc = build();
   const size_t bytes = std::max<size_t>(en.desc.host.size(), 256);
+  if (injected_alloc_failure())
+    return fail(SPAN_LA_ERR_NOMEM, "cudaMalloc(descriptors, %zu): injected failure", bytes);
   cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&en.d_block), bytes);
   if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMalloc(descriptors, %zu): %s", bytes, cudaGetErrorString(e));
   if (!en.desc.host.empty())
@@ -637,6 +651,7 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
   const size_t total = std::max<size_t>(off_parts + (split ? 6 * part_bytes : 0), 256);
 
   uint8_t* ws = nullptr;
+  if (injected_alloc_failure()) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): injected failure", total);
   e = cudaMallocAsync(reinterpret_cast<void**>(&ws), total, stream);
   if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): %s", total, cudaGetErrorString(e));
   do {
@@ -810,6 +825,7 @@ span_la_status run_softmax(const std::vector<int32_t>& key, const int32_t* view_
   uint8_t* ws = nullptr;
   if (!use_cache) {
     const size_t bytes = std::max<size_t>(desc->host.size(), 256);
+    if (injected_alloc_failure()) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): injected failure", bytes);
     e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
     if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): %s", bytes, cudaGetErrorString(e));
     e = cudaMemcpyAsync(ws, desc->host.data(), desc->host.size(), cudaMemcpyHostToDevice, stream);
@@ -1245,6 +1261,14 @@ span_la_status span_la_pass_noalloc(const void* q, const void* k, const void* v,
     });
     if (e != cudaSuccess) return cuda_fail(e, "span-output launch");
   }
+  return SPAN_LA_OK;
+}
+
+span_la_status span_la_fault_inject(int32_t kind, int32_t count) {
+  g_detail.clear();
+  if (kind != SPAN_LA_FAULT_ALLOC) return fail(SPAN_LA_ERR_INVALID, "unknown fault kind %d", kind);
+  if (count < 0) return fail(SPAN_LA_ERR_INVALID, "count %d < 0", count);
+  g_fail_allocs.store(count, std::memory_order_relaxed);
   return SPAN_LA_OK;
 }
 

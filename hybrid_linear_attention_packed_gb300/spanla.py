@@ -32,7 +32,8 @@ EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
             "span_la_profile_reset", "span_la_kernel_name", "span_la_plan_stats",
             "span_la_pass_noalloc", "span_la_cache_create", "span_la_cache_destroy",
             "span_la_cache_put", "span_la_cache_contains", "span_la_cache_branches",
-            "span_la_cache_stats", "span_la_softmax_pass", "span_la_softmax_branches_from_kv")
+            "span_la_cache_stats", "span_la_softmax_pass", "span_la_softmax_branches_from_kv",
+            "span_la_fault_inject")
 NUM_KERNELS = 7
 
 
@@ -101,6 +102,8 @@ def load_library(path: Optional[str] = None):
         lib.span_la_softmax_pass.argtypes = [vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
                                              ctypes.c_int32, i32p, ctypes.c_float, vp, vp, vp]
         lib.span_la_softmax_pass.restype = ctypes.c_int
+        lib.span_la_fault_inject.argtypes = [ctypes.c_int32, ctypes.c_int32]
+        lib.span_la_fault_inject.restype = ctypes.c_int
         lib.span_la_softmax_branches_from_kv.argtypes = [vp, vp, ctypes.c_int64, i32p, ctypes.c_int32,
                                                          vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
                                                          ctypes.c_float, vp, vp, vp]
@@ -388,6 +391,15 @@ def span_la_check(stream: Optional[torch.cuda.Stream] = None) -> None:
     """Synchronise the stream and raise on a CUDA error or a device wait timeout."""
     lib = load_library()
     _raise(lib, lib.span_la_check(_stream_handle(stream)), "span_la_check")
+
+
+FAULT_ALLOC = 1
+
+
+def fault_inject(kind: int, count: int) -> None:
+    """Make the library's next `count` device allocations fail (kind FAULT_ALLOC)."""
+    lib = load_library()
+    _raise(lib, lib.span_la_fault_inject(int(kind), int(count)), "span_la_fault_inject")
 
 
 def span_la_selftest_wait_timeout(limit_us: int, stream=None) -> None:

@@ -200,6 +200,17 @@ int32_t span_la_version(void);
 span_la_status span_la_selftest_wait_timeout(int32_t limit_us, cudaStream_t stream);
 
 /*
+ * span_la_fault_inject -- failure-detection hook on the host: with kind
+ * SPAN_LA_FAULT_ALLOC, the library's next `count` device allocations
+ * (workspace, descriptor blocks) fail as if the device were out of memory,
+ * so the calls that make them return SPAN_LA_ERR_NOMEM before enqueueing any
+ * kernel.  count = 0 clears it.  Process-wide; meant for tests.  Unknown kind
+ * or count < 0: SPAN_LA_ERR_INVALID.
+ */
+#define SPAN_LA_FAULT_ALLOC 1
+span_la_status span_la_fault_inject(int32_t kind, int32_t count);
+
+/*
  * span_la_plan_stats -- host only, no CUDA call: the work units a call with
  * this metadata, head count and dtype would launch (used to count the
  * algorithmic bytes of each kernel).

@@ -109,6 +109,31 @@ def test_bounded_wait_times_out_without_trapping(cuda_device):
     assert not torch.isnan(out[: w.rows]).any()
 
 
+def test_injected_allocation_failure_enqueues_nothing(cuda_device):
+    """A workspace allocation that fails (host-side injection) makes the call
+    return SPAN_LA_ERR_NOMEM with nothing enqueued and nothing written; the
+    next call runs normally."""
+    w = workloads.make_pass([300, 70], [20, 9], [0, 1], H=2, dtype="bf16", seed=44)
+    q, k, v = to_device(w, cuda_device)
+    out = torch.full_like(q, float("nan"))
+    state = torch.full((w.V, w.H, 64, 64), float("nan"), dtype=torch.float32, device=cuda_device)
+    spanla.profile_reset()
+    spanla.fault_inject(spanla.FAULT_ALLOC, 1)
+    try:
+        with pytest.raises(SpanLAError) as exc:
+            span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, out=out,
+                         view_state_out=state)
+    finally:
+        spanla.fault_inject(spanla.FAULT_ALLOC, 0)
+    assert exc.value.status == 4 and "injected" in str(exc.value)
+    span_la_check()
+    assert torch.isnan(out).all() and torch.isnan(state).all()
+    assert all(p["launches"] == 0 for p in spanla.profile_read().values())
+    span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, out=out, view_state_out=state)
+    span_la_check()
+    assert not torch.isnan(out[: w.rows]).any() and not torch.isnan(state).any()
+
+
 def test_profiler_counts_and_times_every_launch(cuda_device):
     w = workloads.single_request(0)
     q, k, v = to_device(w, cuda_device)

@@ -198,3 +198,10 @@ def test_softmax_branches_from_kv_validation(lib):
     st = lib.span_la_softmax_branches_from_kv(0, FAKE, 30, vp, 1, FAKE, FAKE, FAKE, _dims(), bp, 2,
                                               pp, 0.0, FAKE, None, None)
     assert st == 1 and "view_k" in lib.span_la_last_error_detail().decode()
+
+
+def test_fault_injection_knob(lib):
+    assert lib.span_la_fault_inject(7, 1) == 1
+    assert lib.span_la_fault_inject(spanla.FAULT_ALLOC, -1) == 1
+    assert lib.span_la_fault_inject(spanla.FAULT_ALLOC, 2) == 0
+    assert lib.span_la_fault_inject(spanla.FAULT_ALLOC, 0) == 0
