@@ -12,6 +12,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <queue>
 #include <string>
@@ -508,6 +509,25 @@ DescBlock make_desc(const Plan& plan, int H, int num_sms) {
   return d;
 }
 
+// ------------------------------------------------------------------ graph capture
+// A host-to-device copy recorded while a stream is captured into a CUDA graph
+// reads its host source every time the graph is launched.  The descriptor
+// bytes of such a call are therefore moved into this registry and kept for the
+// life of the process (a few KB per captured call).
+std::mutex g_graph_mu;
+std::vector<std::unique_ptr<std::vector<uint8_t>>> g_graph_bytes;
+
+// Copy `bytes` to device `dst` on `stream`; when the stream is being captured,
+// the bytes are first moved to storage that outlives the graph.
+cudaError_t upload_descriptors(void* dst, std::vector<uint8_t>&& bytes, bool capturing, cudaStream_t stream) {
+  if (bytes.empty()) return cudaSuccess;
+  if (!capturing) return cudaMemcpyAsync(dst, bytes.data(), bytes.size(), cudaMemcpyHostToDevice, stream);
+  std::lock_guard<std::mutex> lock(g_graph_mu);
+  g_graph_bytes.push_back(std::make_unique<std::vector<uint8_t>>(std::move(bytes)));
+  const std::vector<uint8_t>& kept = *g_graph_bytes.back();
+  return cudaMemcpyAsync(dst, kept.data(), kept.size(), cudaMemcpyHostToDevice, stream);
+}
+
 // ------------------------------------------------------------------ plan cache
 // Passes with the same metadata (every layer of a model step, for instance)
 // reuse one uploaded descriptor block: the plan depends on the metadata, the
@@ -656,7 +676,7 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
   if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): %s", total, cudaGetErrorString(e));
   do {
     if (!use_cache) {
-      e = cudaMemcpyAsync(ws, desc->host.data(), desc->host.size(), cudaMemcpyHostToDevice, stream);
+      e = upload_descriptors(ws, std::move(local.host), true, stream);
       if (e != cudaSuccess) { st = cuda_fail(e, "cudaMemcpyAsync(descriptors)"); break; }
       block = ws;
     }
@@ -828,7 +848,7 @@ span_la_status run_softmax(const std::vector<int32_t>& key, const int32_t* view_
     if (injected_alloc_failure()) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): injected failure", bytes);
     e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
     if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): %s", bytes, cudaGetErrorString(e));
-    e = cudaMemcpyAsync(ws, desc->host.data(), desc->host.size(), cudaMemcpyHostToDevice, stream);
+    e = upload_descriptors(ws, std::move(local.host), true, stream);
     if (e != cudaSuccess) st = cuda_fail(e, "cudaMemcpyAsync(descriptors)");
     block = ws;
   }
@@ -1221,8 +1241,10 @@ span_la_status span_la_pass_noalloc(const void* q, const void* k, const void* v,
 
   // The error word starts each call at zero; everything else in the scratch
   // is written before it is read.
-  e = cudaMemsetAsync(err, 0, sizeof(unsigned), stream);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cap);
+  if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(unsigned), stream);
+  if (e == cudaSuccess) e = upload_descriptors(ws, std::move(host), cap != cudaStreamCaptureStatusNone, stream);
   if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
   DeviceOperands tile_ops{}, chunk_ops{};
   const void* ops[3] = {q, k, v};

@@ -126,6 +126,17 @@ void release_events(span_la_view_cache* c) {
   c->spare_events.clear();
 }
 
+// The cache's cross-stream events are host-side state of each call, so its
+// calls are not recorded into CUDA graphs.
+span_la_status refuse_capture(cudaStream_t stream) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cache_fail(SPAN_LA_ERR_CUDA, "cudaStreamIsCapturing: %s", cudaGetErrorString(e));
+  if (cap != cudaStreamCaptureStatusNone)
+    return cache_fail(SPAN_LA_ERR_UNSUPPORTED, "view-state cache calls cannot be captured into a CUDA graph");
+  return SPAN_LA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -192,6 +203,8 @@ span_la_status span_la_cache_put(span_la_view_cache* cache, const uint64_t* keys
     return cache_fail(SPAN_LA_ERR_INVALID, "states must be 16-byte aligned");
   std::unordered_set<uint64_t> keep(keys, keys + n);
   if (static_cast<int32_t>(keep.size()) != n) return cache_fail(SPAN_LA_ERR_INVALID, "keys are not distinct");
+  span_la_status cst = refuse_capture(stream);
+  if (cst != SPAN_LA_OK) return cst;
   std::lock_guard<std::mutex> lock(cache->mu);
   const size_t state_bytes = static_cast<size_t>(cache->heads) * kStateBytesPerHead;
   for (int32_t i = 0; i < n; ++i) {
@@ -249,6 +262,8 @@ span_la_status span_la_cache_branches(span_la_view_cache* cache, const uint64_t*
                       cache->heads);
   if (num_branches < 0 || (num_branches > 0 && parent_keys == nullptr))
     return cache_fail(SPAN_LA_ERR_INVALID, "bad parent key array");
+  span_la_status cst = refuse_capture(stream);
+  if (cst != SPAN_LA_OK) return cst;
   std::vector<int32_t> slots(num_branches);
   {
     std::lock_guard<std::mutex> lock(cache->mu);

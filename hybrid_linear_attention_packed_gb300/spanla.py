@@ -179,7 +179,8 @@ def span_la_pass(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                  branch_parent: Optional[Sequence[int]],
                  out: Optional[torch.Tensor] = None,
                  view_state_out: Optional[torch.Tensor] = None,
-                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                 stream: Optional[torch.cuda.Stream] = None,
+                 _entry: str = "span_la_pass") -> Tuple[torch.Tensor, torch.Tensor]:
     """One packed pass (see ``span_la_pass`` in ``include/spanla.h``).
 
     Returns ``(out [T,H,64], view_state_out [V,H,64,64] fp32)``.  ``out`` is
@@ -201,11 +202,23 @@ def span_la_pass(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if (view_state_out.dtype != torch.float32 or not view_state_out.is_contiguous()
             or view_state_out.numel() < V * H * 4096):
         raise ValueError("view_state_out must be contiguous fp32 [V, H, 64, 64]")
-    st = lib.span_la_pass(q.data_ptr(), k.data_ptr(), v.data_ptr(), dims,
-                          _iptr(vcu), V, _iptr(bcu), B, _iptr(par),
-                          out.data_ptr(), view_state_out.data_ptr(), _stream_handle(stream))
-    _raise(lib, st, "span_la_pass")
+    st = getattr(lib, _entry)(q.data_ptr(), k.data_ptr(), v.data_ptr(), dims,
+                              _iptr(vcu), V, _iptr(bcu), B, _iptr(par),
+                              out.data_ptr(), view_state_out.data_ptr(), _stream_handle(stream))
+    _raise(lib, st, _entry)
     return out, view_state_out
+
+
+def span_la_pass_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                         view_cu_seqlens: Sequence[int], branch_cu_seqlens: Optional[Sequence[int]],
+                         branch_parent: Optional[Sequence[int]],
+                         out: Optional[torch.Tensor] = None,
+                         view_state_out: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """As :func:`span_la_pass`, with the workspace in the library's fixed
+    scratch instead of a per-call allocation (``span_la_pass_noalloc``)."""
+    return span_la_pass(q, k, v, view_cu_seqlens, branch_cu_seqlens, branch_parent, out=out,
+                        view_state_out=view_state_out, stream=stream, _entry="span_la_pass_noalloc")
 
 
 def span_la_branches_from_state(cached_state: torch.Tensor, q: torch.Tensor, k: torch.Tensor,

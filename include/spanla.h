@@ -41,6 +41,11 @@
  * Asynchrony.  A call only enqueues work on `stream` (a cudaStream_t on the
  *   current device; 0 = legacy default stream).  Outputs are valid once the
  *   stream has reached the call; inputs must stay unchanged until then.
+ * Graphs.  The pass, branch and softmax calls may be recorded while `stream`
+ *   is being captured into a CUDA graph: the recorded work replays on the
+ *   buffers of the recorded call (their current contents), with its own
+ *   workspace allocations in the graph.  The descriptor bytes of a recorded
+ *   call are kept by the library for the life of the process.
  * Precision.  bf16 or fp32 inputs; the state and every accumulation are fp32.
  *   fp32 operands (and the fp32 state and P tiles fed to the tensor cores) are
  *   split into two bf16 parts whose cross products are summed.  Outputs are
@@ -329,7 +334,9 @@ span_la_status span_la_softmax_branches_from_kv(const void *view_k, const void *
  * on whatever streams they were enqueued.  The caller still orders the
  * states a put copies from (normally by putting on the stream of the pass
  * that wrote them).  A cache object may be used from several host threads
- * (calls are serialised by a lock); it is not tied to a stream.
+ * (calls are serialised by a lock); it is not tied to a stream.  Puts and
+ * branch calls on a stream that is being captured into a CUDA graph return
+ * SPAN_LA_ERR_UNSUPPORTED (the ordering events are per-call host state).
  */
 typedef struct span_la_view_cache span_la_view_cache;
 

@@ -171,3 +171,84 @@ def test_plan_reused_across_calls_and_streams(cuda_device):
         seg = segment_rows(w)
         assert rel_err(f64(out)[seg], ref[seg]) <= TOL["bf16"]
         assert rel_err(f64(state), ref_state) <= TOL["bf16"]
+
+
+def _graph_replay_equals_eager(dev, record, w_a, w_b):
+    """Record `record(q, k, v, outs)` into a CUDA graph on inputs A, replay it
+    after copying inputs B into the same buffers, and compare with an eager
+    call on B, bit for bit."""
+    qa, ka, va = to_device(w_a, dev)
+    qb, kb, vb = to_device(w_b, dev)
+    eager = record(qb, kb, vb)
+    span_la_check()
+    q, k, v = qa.clone(), ka.clone(), va.clone()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        outs = record(q, k, v)
+    for _ in range(2):
+        q.copy_(qb)
+        k.copy_(kb)
+        v.copy_(vb)
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        span_la_check()
+        for got, want in zip(outs, eager):
+            assert torch.equal(got, want)
+
+
+def test_cuda_graph_replays_the_pass(cuda_device):
+    shape = dict(view_lens=[700, 129], branch_lens=[40, 9, 100], parent=[0, 0, 1])
+    w_a, w_b = (workloads.make_pass(shape["view_lens"], shape["branch_lens"], shape["parent"], H=4,
+                                    dtype="bf16", seed=s) for s in (50, 51))
+
+    def record(q, k, v):
+        out = torch.zeros_like(q)
+        state = torch.zeros((w_a.V, w_a.H, 64, 64), dtype=torch.float32, device=q.device)
+        span_la_pass(q, k, v, w_a.view_cu, w_a.branch_cu, w_a.branch_parent, out=out,
+                     view_state_out=state)
+        return out, state
+    _graph_replay_equals_eager(cuda_device, record, w_a, w_b)
+
+
+def test_cuda_graph_replays_the_noalloc_pass(cuda_device):
+    w_a, w_b = (workloads.make_pass([300, 64], [20, 70], [1, 0], H=2, dtype="bf16", seed=s)
+                for s in (52, 53))
+
+    def record(q, k, v):
+        out = torch.zeros_like(q)
+        state = torch.zeros((w_a.V, w_a.H, 64, 64), dtype=torch.float32, device=q.device)
+        spanla.span_la_pass_noalloc(q, k, v, w_a.view_cu, w_a.branch_cu, w_a.branch_parent,
+                                    out=out, view_state_out=state)
+        return out, state
+    _graph_replay_equals_eager(cuda_device, record, w_a, w_b)
+
+
+def test_cuda_graph_replays_the_softmax_layer(cuda_device):
+    from hybrid_linear_attention_packed_gb300 import span_la_softmax_pass
+    w_a, w_b = (workloads.make_pass([500, 130], [33, 7, 128], [0, 1, 1], H=2, dtype="bf16", seed=s,
+                                    q_scale=1.0, k_scale=1.0) for s in (54, 55))
+
+    def record(q, k, v):
+        out = torch.zeros_like(q)
+        span_la_softmax_pass(q, k, v, w_a.view_cu, w_a.branch_cu, w_a.branch_parent, out=out)
+        return (out,)
+    _graph_replay_equals_eager(cuda_device, record, w_a, w_b)
+
+
+def test_cache_calls_refuse_graph_capture(cuda_device):
+    from hybrid_linear_attention_packed_gb300 import ViewStateCache
+    state = torch.zeros((1, 2, 64, 64), dtype=torch.float32, device=cuda_device)
+    with ViewStateCache(2, capacity=2) as cache:
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with pytest.raises(SpanLAError) as exc:
+            with torch.cuda.graph(g):
+                cache.put([1], state)
+        assert exc.value.status == 2
+        torch.cuda.synchronize()
+        cache.put([1], state)
+        span_la_check()
+        assert cache.contains([1]).tolist() == [True]
