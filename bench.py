@@ -773,6 +773,34 @@ def main():
     spanla.span_la_check()
     warm_us = w_start.elapsed_time(w_end) * 1e3 / NW
 
+    # The same step recorded once into a CUDA graph and replayed (L2 flushed
+    # before each replay, outside the graph).
+    graph_us = None
+    try:
+        gstream = torch.cuda.Stream(device=dev)
+        gstream.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gstream):
+            run_on(q, k, v, out, state)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            flush.zero_()
+            g.replay()
+        torch.cuda.synchronize()
+        gs = [torch.cuda.Event(enable_timing=True) for _ in range(50)]
+        ge = [torch.cuda.Event(enable_timing=True) for _ in range(50)]
+        for i in range(50):
+            flush.zero_()
+            gs[i].record(stream)
+            g.replay()
+            ge[i].record(stream)
+        torch.cuda.synchronize()
+        spanla.span_la_check()
+        graph_us = statistics.mean(a.elapsed_time(b) for a, b in zip(gs, ge)) * 1e3
+        del g
+    except (RuntimeError, spanla.SpanLAError) as exc:   # report, do not fail the bench
+        graph_us = "unavailable: %s" % exc
+
     h2d = 3 * (w.T - row_lo) * w.H * 64 * esize
     d2h = (w.T - row_lo) * w.H * 64 * esize + (0 if shards_mode else w.V * w.H * STATE_BYTES)
 
@@ -810,6 +838,7 @@ def main():
                 "profiled_kernel_us_sum": profiled_step_us,
                 "step_ms_min": min(step_ms),
                 "host_enqueue_us": statistics.median(host_us),
+                "graph_us_per_step": graph_us,
                 "warm_l2_us_per_step": warm_us}
         print(json.dumps(line))
     if pg:
