@@ -1,11 +1,16 @@
 // Host side of libspanla: argument validation, the packed-pass descriptor
-// build, the stream-ordered workspace, TMA descriptors and the launches.
+// build, the plan cache, the stream-ordered workspace, TMA descriptors and the
+// launches, for the linear-attention pass and the softmax layer; also the
+// diagnostics (status text, profiling counters, fault injection).
 //
 // A pass ("Serving 0.88M TPS from Two RTXs and Mac Minis", section "Kernels":
 // one scan per pass in three launches) is enqueued as
-//   chunk-state  -> segmented scan -> tile output (view chunks + branch fork)
-// over descriptor tables built here from the host metadata, so that each step
-// is one launch for the whole pass however many views and branches it holds.
+//   span state -> segmented scan -> span output (views + branch fork)
+// for bf16 inputs (chunk state -> scan -> tile output for fp32 inputs), over
+// descriptor tables built here from the host metadata, so that each kernel is
+// one launch for the whole pass however many views and branches it holds.
+// The softmax layer over the same rows is one launch (section "Softmax
+// layer" below).
 #include <algorithm>
 #include <cmath>
 #include <atomic>
