@@ -41,11 +41,16 @@
 //              rows past a partial block's keys and hands the stage back to
 //              the producer.
 //   warps 2-9  softmax: two warps per TMEM lane quarter, one query row per
-//              thread pair, each thread of the pair on one half of the 128
-//              key columns (and one half of the 64 output columns): mask,
-//              block maximum (the pair swaps its halves' maxima through
-//              shared memory), exponentials, row sum, P as bf16 in place; at
-//              the end of an item O / l (and lse) to global memory.
+//              thread in each; the warp of role g & 1 takes key block g whole
+//              (all 128 columns of its rows): mask, block maximum, the raise
+//              decision -- which needs the previous block's reference maximum,
+//              handed over by the other warp through shared memory and
+//              published again at once -- then exponentials, row sum and P
+//              as bf16 in place.  So consecutive blocks' exponentials run in
+//              the two warps at the same time, and only the short maximum /
+//              decision step is ordered between them.  Each warp keeps its
+//              own partial row sum; at the end of an item the two combine
+//              and each writes half of the output columns (and lse).
 #include "spanla_internal.h"
 #include "tc_ptx.cuh"
 
@@ -70,13 +75,15 @@ struct SaSmem {
   static constexpr int kFull = 0, kEmpty = kStages, kQFull = 2 * kStages, kQFree = kQFull + 2,
                        kSReady = kQFull + 4, kPDone = kSReady + kSBufs, kPVDone = kPDone + kSBufs,
                        kOReady = kPVDone + kSBufs, kOFree = kOReady + 2, kPair = kOFree + 2,
-                       kNumBars = kPair + 4;
+                       kDec = kPair + 4, kNumBars = kDec + 8;
   static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
-  // Row maxima of the two column halves, [block parity][half][row], and row
-  // sums at the end of an item, [item parity][half][row].
-  static constexpr uint32_t kRedMax = kTmemSlot + 16;
-  static constexpr uint32_t kRedSum = kRedMax + 2 * 2 * 128 * 4;
-  static constexpr uint32_t kBytes = kRedSum + 2 * 2 * 128 * 4;
+  // Reference maximum after block g, [g & 1][row]; each role's partial row
+  // sum and the maximum it is relative to at the end of an item,
+  // [item parity][role][row].
+  static constexpr uint32_t kDecM = kTmemSlot + 16;
+  static constexpr uint32_t kRedL = kDecM + 2 * 128 * 4;
+  static constexpr uint32_t kRedM = kRedL + 2 * 2 * 128 * 4;
+  static constexpr uint32_t kBytes = kRedM + 2 * 2 * 128 * 4;
   static constexpr uint32_t kRequest = kBytes + 1024;
 };
 static_assert(SaSmem::kRequest <= 227 * 1024, "shared memory budget");
@@ -181,10 +188,14 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(bar(L::kSReady + b), 1);
-      mbar_init(bar(L::kPDone + b), kSoftmaxThreads);
+      mbar_init(bar(L::kPDone + b), kSoftmaxThreads / 2);   // the warps of the block's role
       mbar_init(bar(L::kPVDone + b), 1);
     }
-    for (int q = 0; q < 4; ++q) mbar_init(bar(L::kPair + q), 64);   // the two warps of a lane quarter
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(bar(L::kPair + q), 64);                       // the two warps of a lane quarter
+      mbar_init(bar(L::kDec + 2 * q), 32);                    // decision of an even block
+      mbar_init(bar(L::kDec + 2 * q + 1), 32);                // decision of an odd block
+    }
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -299,7 +310,7 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (lane == 0) {
           const uint32_t colS = col_s(g);
           // P of keys 0..63 is in columns 0..31 of the buffer, of keys
-          // 64..127 in columns 64..95 (one column half per softmax thread).
+          // 64..127 in columns 64..95 (each written over its own scores).
           for (int kk = 0; kk < kTileRows / 16; ++kk)
             mma_bf16_tmem_a(tmem + colO, tmem + colS + kk * 8 + (kk >= 4 ? 32 : 0),
                             smem_desc_sw128(st + kTileBytes + kk * 2048, kTileBytes, 1024), id_pv,
@@ -314,14 +325,14 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
-    const int half = (warp - 2) >> 2;             // key columns [64 half, 64 half + 64)
+    const int role = (warp - 2) >> 2;             // takes the key blocks g with g & 1 == role
     const int row = quarter * 32 + lane;          // query row in the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    float* red_max = reinterpret_cast<float*>(smem + L::kRedMax);
-    float* red_sum = reinterpret_cast<float*>(smem + L::kRedSum);
-    // The two threads of a row meet on their lane quarter's mbarrier, one
-    // phase per exchange (bounded waits: a partner that gave up cannot hang
-    // this thread).
+    float* dec_m = reinterpret_cast<float*>(smem + L::kDecM);
+    float* red_l = reinterpret_cast<float*>(smem + L::kRedL);
+    float* red_m = reinterpret_cast<float*>(smem + L::kRedM);
+    // The two warps of a lane quarter meet at the end of an item (bounded
+    // waits: a partner that gave up cannot hang this thread).
     const uint32_t pair_bar = bar(L::kPair + quarter);
     uint32_t pair_phase = 0;
     auto pair_sync = [&]() -> bool {
@@ -333,41 +344,93 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // Raise m only when a block maximum exceeds it by this much (raw score
     // units): P then stays below 2^8.
     const float raise_margin = 8.f / scale_log2e;
-    float m_ref = -INFINITY, l_run = 0.f;
-    float m_done = 0.f, l_done = 1.f;
+    // This warp's partial row sum over its blocks of the current item, and the
+    // reference maximum it is relative to.
+    float l_w = 0.f, m_w = -INFINITY;
+    float l_done = 0.f, m_done = -INFINITY;
     SaItem done_it{};        // item whose output is still to be written
     int done_idx = -1;
     int g = 0;
 
-    // O of item `it` (index ii) / l -> global row; lse = scale * m + log(l).
-    // l is the sum of the pair's two partial sums.
-    auto finish = [&](const SaItem& it, int ii, float m, float l_part) -> bool {
+    // Bring l_w to reference maximum m.
+    auto rebase = [&](float m) {
+      if (m != m_w) {
+        l_w = m_w == -INFINITY ? 0.f : l_w * ex2((m_w - m) * scale_log2e);
+        m_w = m;
+      }
+    };
+
+    // O of item `it` (index ii) / l -> global row (this role's 32 output
+    // columns); lse = scale * m + log(l).  l combines both roles' sums.
+    auto finish = [&](const SaItem& it, int ii, float m_part, float l_part) -> bool {
       const int ob = ii & 1;
-      float* rs = red_sum + ob * 256;
-      rs[half * 128 + row] = l_part;
+      red_l[(ob * 2 + role) * 128 + row] = l_part;
+      red_m[(ob * 2 + role) * 128 + row] = m_part;
       if (!pair_sync()) return false;
-      const float l = l_part + rs[(half ^ 1) * 128 + row];
+      const float l_o = red_l[(ob * 2 + (role ^ 1)) * 128 + row];
+      const float m_o = red_m[(ob * 2 + (role ^ 1)) * 128 + row];
+      const float m = fmaxf(m_part, m_o);
+      const float l = (m_part == -INFINITY ? 0.f : l_part * ex2((m_part - m) * scale_log2e)) +
+                      (m_o == -INFINITY ? 0.f : l_o * ex2((m_o - m) * scale_log2e));
       if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + ob), (ii >> 1) & 1, err, kErrTimeoutMma)))
         return false;
       tc_fence_after_sync();
       uint32_t r0[32];
-      tmem_ld_32cols(tmem + lane_base + (ob ? kColO1 : kColO0) + 32 * half, r0);
+      tmem_ld_32cols(tmem + lane_base + (ob ? kColO1 : kColO0) + 32 * role, r0);
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(L::kOFree + ob));
       if (row < it.nrows) {
         const float inv = 1.f / l;
         uint4* dst = reinterpret_cast<uint4*>(out + ((static_cast<int64_t>(it.r0) + row) * H + it.head) * kHeadDim) +
-                     4 * half;
+                     4 * role;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           dst[c] = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c]) * inv, __uint_as_float(r0[8 * c + 1]) * inv),
                               pack_bf16x2(__uint_as_float(r0[8 * c + 2]) * inv, __uint_as_float(r0[8 * c + 3]) * inv),
                               pack_bf16x2(__uint_as_float(r0[8 * c + 4]) * inv, __uint_as_float(r0[8 * c + 5]) * inv),
                               pack_bf16x2(__uint_as_float(r0[8 * c + 6]) * inv, __uint_as_float(r0[8 * c + 7]) * inv));
-        if (lse != nullptr && half == 0) lse[(static_cast<int64_t>(it.r0) + row) * H + it.head] = scale * m + logf(l);
+        if (lse != nullptr && role == 0) lse[(static_cast<int64_t>(it.r0) + row) * H + it.head] = scale * m + logf(l);
       }
       return true;
+    };
+
+    // 64 scores (key columns [c0, c0 + 64) of block g) with keys outside
+    // [lo, hi] masked to -inf.
+    auto load_half = [&](uint32_t colS, int c0, int lo, int hi, float (&x)[64]) {
+      uint32_t sr[64];
+      tmem_ld_32cols(tmem + lane_base + colS + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
+      tmem_ld_32cols(tmem + lane_base + colS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+      tmem_ld_wait();
+      if (__all_sync(0xffffffffu, lo <= c0 && hi >= c0 + 63)) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = (c0 + c >= lo && c0 + c <= hi) ? __uint_as_float(sr[c]) : -INFINITY;
+      }
+    };
+    // P of 64 scores against reference maximum m, as bf16 into the first 32
+    // of their columns; returns their sum.
+    auto exp_store = [&](uint32_t colS, int c0, float m, const float (&x)[64]) -> float {
+      const float neg = -(m == -INFINITY ? 0.f : m) * scale_log2e;
+      const uint64_t c2 = pair_f32(scale_log2e, scale_log2e), n2 = pair_f32(neg, neg);
+      uint64_t acc0 = pair_f32(0.f, 0.f), acc1 = acc0;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float x0, x1;
+        unpair_f32(fma_f32x2(pair_f32(x[2 * c], x[2 * c + 1]), c2, n2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        if (c & 1) acc1 = add_f32x2(acc1, pair_f32(p0, p1));
+        else acc0 = add_f32x2(acc0, pair_f32(p0, p1));
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      tmem_st_32cols(tmem + lane_base + colS + c0, pk);
+      float a0, a1, b0, b1;
+      unpair_f32(acc0, a0, a1);
+      unpair_f32(acc1, b0, b1);
+      return (a0 + b0) + (a1 + b1);
     };
 
     bool ok = true;
@@ -382,55 +445,72 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int hi_col = row < it.nrows ? row : -1;   // last visible key of the diagonal block
       const int nb = num_blocks(it);
       for (int jb = 0; jb < nb && ok; ++jb, ++g) {
-        const KeyBlock kb = key_block(it, jb);
-        const int b = g & 1, sb = g % kSBufs;
         if (jb == 0) {
-          m_done = m_ref;
-          l_done = l_run;
-          m_ref = -INFINITY;
-          l_run = 0.f;
+          // A new item: this warp's partial sum starts again; the previous
+          // item (whose last product lands soon) is written out.
+          l_done = l_w;
+          m_done = m_w;
+          l_w = 0.f;
+          m_w = -INFINITY;
+          if (done_idx >= 0) {
+            if (!finish(done_it, done_idx, m_done, l_done)) { ok = false; break; }
+            done_idx = -1;
+          }
         }
-        // Visible key columns of this thread's half: [lo, hi] (relative to 64 half).
-        int lo = 0, hi = 63;
+        if (jb == nb - 1) {
+          done_it = it;
+          done_idx = i;
+        }
+        if ((g & 1) != role) continue;
+        const KeyBlock kb = key_block(it, jb);
+        const int sb = g % kSBufs;
+        // Visible key columns of the row: [lo, hi] (0..127).
+        int lo = 0, hi = 127;
         if (kb.diag) {
-          lo = seg_start - 64 * half;
-          hi = hi_col - 64 * half;
+          lo = seg_start;
+          hi = hi_col;
         } else if (kb.cnt < kTileRows) {
-          hi = kb.cnt - 1 - 64 * half;
+          hi = kb.cnt - 1;
         }
         if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kSReady + sb), (g / kSBufs) & 1, err, kErrTimeoutMma))) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t colS = col_s(g) + 64 * half;
-        uint32_t sr[64];
-        tmem_ld_32cols(tmem + lane_base + colS, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_ld_32cols(tmem + lane_base + colS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-        tmem_ld_wait();
-        float s[64];
-        if (__all_sync(0xffffffffu, lo <= 0 && hi >= 63)) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = (c >= lo && c <= hi) ? __uint_as_float(sr[c]) : -INFINITY;
-        }
-        float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+        const uint32_t colS = col_s(g);
+        float x[64];
+        load_half(colS, 0, lo, hi, x);
+        float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]);
 #pragma unroll
         for (int c = 4; c < 64; c += 4) {
-          mx0 = max3(mx0, s[c], s[c + 1]);
-          mx1 = max3(mx1, s[c + 2], s[c + 3]);
+          mx0 = max3(mx0, x[c], x[c + 1]);
+          mx1 = max3(mx1, x[c + 2], x[c + 3]);
         }
-        float* rm = red_max + b * 256;
-        rm[half * 128 + row] = fmaxf(mx0, mx1);
-        if (!pair_sync()) { ok = false; break; }
-        const float mx = fmaxf(fmaxf(mx0, mx1), rm[(half ^ 1) * 128 + row]);
+        load_half(colS, 64, lo, hi, x);
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          mx0 = max3(mx0, x[c], x[c + 1]);
+          mx1 = max3(mx1, x[c + 2], x[c + 3]);
+        }
+        const float mx = fmaxf(mx0, mx1);
+        // The reference maximum after block g-1, handed over by the other
+        // warp (every block hands one over, so the two stay in step).
+        float m_ref = -INFINITY;
+        if (g >= 1) {
+          const int gp = g - 1;
+          if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kDec + 2 * quarter + (gp & 1)), (gp >> 1) & 1, err,
+                                                    kErrTimeoutMma))) {
+            ok = false;
+            break;
+          }
+          m_ref = dec_m[(gp & 1) * 128 + row];
+        }
         if (jb == 0) {
           m_ref = mx;   // the item's O starts from this block (no rescale)
         } else if (__any_sync(0xffffffffu, mx > m_ref + raise_margin)) {
           // Raise m for the rows that need it: O (after the previous block's
-          // product has landed) and l scale by exp(scale (m_old - m_new)).
+          // product has landed) scales by exp(scale (m_old - m_new)); the
+          // partial sums follow when they are next used.
           const int gp = g - 1, sp = gp % kSBufs;
           if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kPVDone + sp), (gp / kSBufs) & 1, err, kErrTimeoutMma))) {
             ok = false;
@@ -439,54 +519,33 @@ softmax_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           tc_fence_after_sync();
           const float m_new = fmaxf(m_ref, mx);
           const float alpha = m_new == m_ref ? 1.f : ex2((m_ref - m_new) * scale_log2e);   // 0 when m_ref = -inf
-          const uint32_t colO = (ob ? kColO1 : kColO0) + 32 * half;
-          uint32_t r0[32];
-          tmem_ld_32cols(tmem + lane_base + colO, r0);
-          tmem_ld_wait();
+          const uint32_t colO = ob ? kColO1 : kColO0;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) r0[c] = __float_as_uint(__uint_as_float(r0[c]) * alpha);
-          tmem_st_32cols(tmem + lane_base + colO, r0);
-          l_run *= alpha;
+          for (int h = 0; h < 2; ++h) {
+            uint32_t r0[32];
+            tmem_ld_32cols(tmem + lane_base + colO + 32 * h, r0);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r0[c] = __float_as_uint(__uint_as_float(r0[c]) * alpha);
+            tmem_st_32cols(tmem + lane_base + colO + 32 * h, r0);
+          }
           m_ref = m_new;
         }
-        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        const float neg = -m_use * scale_log2e;
-        // p = 2^(s c - m c) two lanes at a time; two paired partial sums.
-        const uint64_t c2 = pair_f32(scale_log2e, scale_log2e), n2 = pair_f32(neg, neg);
-        uint64_t acc0 = pair_f32(0.f, 0.f), acc1 = acc0;
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float x0, x1;
-          unpair_f32(fma_f32x2(pair_f32(s[2 * c], s[2 * c + 1]), c2, n2), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          if (c & 1) acc1 = add_f32x2(acc1, pair_f32(p0, p1));
-          else acc0 = add_f32x2(acc0, pair_f32(p0, p1));
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        float a0, a1, b0, b1;
-        unpair_f32(acc0, a0, a1);
-        unpair_f32(acc1, b0, b1);
-        const float sum0 = a0 + b0, sum1 = a1 + b1;
-        // The 64 bf16 of this half's P go over the first 32 of its columns.
-        tmem_st_32cols(tmem + lane_base + colS, pk);
+        // Hand the decision to the other warp before the exponentials.
+        dec_m[(g & 1) * 128 + row] = m_ref;
+        mbar_arrive(bar(L::kDec + 2 * quarter + (g & 1)));
+        rebase(m_ref);
+        // Keys 64..127 are in registers; keys 0..63 are read again.
+        float sum = exp_store(colS, 64, m_ref, x);
+        load_half(colS, 0, lo, hi, x);
+        sum += exp_store(colS, 0, m_ref, x);
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(bar(L::kPDone + sb));
-        l_run += sum0 + sum1;
-        // The previous item is complete once its last product has landed:
-        // write it out now that this item's first block is under way.
-        if (jb == 0 && done_idx >= 0) {
-          if (!finish(done_it, done_idx, m_done, l_done)) { ok = false; break; }
-          done_idx = -1;
-        }
-        if (jb == nb - 1) {
-          done_it = it;
-          done_idx = i;
-        }
+        l_w += sum;
       }
     }
-    if (ok && done_idx >= 0) finish(done_it, done_idx, m_ref, l_run);
+    if (ok && done_idx >= 0) finish(done_it, done_idx, m_w, l_w);
   }
 
   tc_fence_before_sync();
