@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cache", action="store_true",
+                    help="cached_long: run the shards through the view-state cache API "
+                         "(span_la_cache_branches by key) instead of span_la_branches_from_state")
     ap.add_argument("--per-request", action="store_true",
                     help="run each request of the workload (a view and its branches) as its own "
                          "pass instead of one shared pass (the page's shared-branch-pass lever)")
@@ -283,6 +286,9 @@ def workload_config(w, name: str) -> dict:
 
 
 def add_mode(cfg: dict, args) -> dict:
+    if getattr(args, "cache", False) and args.workload == "cached_long":
+        cfg = dict(cfg, step="span_la_cache_branches by key over the view-state cache, 4 shards of "
+                             "64 branches; tokens/s counts branch rows")
     if getattr(args, "per_request", False):
         cfg = dict(cfg, step="one span_la_pass per request (view + its branches) over the same "
                              "buffers, instead of one shared pass")
@@ -432,31 +438,55 @@ def main_softmax(args):
                 "visible_pairs_per_head": pairs,
                 "exp_per_s": pairs * w.H / (kern_us / 1e6)}
 
-    # End to end with host buffers: copy q, k, v in from pinned memory, run,
-    # read out back, each step in turn on one stream.
+    # End to end with host buffers: every step copies its q, k, v in from
+    # pinned memory, runs the call and reads out back, pipelined over two
+    # device buffer sets and three streams (copies in, the call, copies out)
+    # as for the linear pass; the value is the steps' rows over the time from
+    # the first copy-in to the last read-back.
     hq, hk, hv = (t.pin_memory() for t in (w.q, w.k, w.v))
     hout = torch.empty_like(hq).pin_memory()
+    sets = [(q, k, v, out), (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                             torch.empty_like(out))]
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        run_on(q, k, v, out)
-        hout.copy_(out, non_blocking=True)
+    def e2e_run(n_steps):
+        ready, ran, read = [None, None], [None, None], [None, None]
+        for i in range(n_steps):
+            b = i & 1
+            dq, dk, dv, dout = sets[b]
+            with torch.cuda.stream(s_in):
+                if ran[b] is not None:
+                    s_in.wait_event(ran[b])
+                dq.copy_(hq, non_blocking=True)
+                dk.copy_(hk, non_blocking=True)
+                dv.copy_(hv, non_blocking=True)
+                ready[b] = torch.cuda.Event()
+                ready[b].record(s_in)
+            with torch.cuda.stream(s_run):
+                s_run.wait_event(ready[b])
+                if read[b] is not None:
+                    s_run.wait_event(read[b])
+                run_on(dq, dk, dv, dout, s_run)
+                ran[b] = torch.cuda.Event()
+                ran[b].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ran[b])
+                hout.copy_(dout, non_blocking=True)
+                read[b] = torch.cuda.Event()
+                read[b].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    e2e_run(4)
     torch.cuda.synchronize()
     KE = max(2, args.e2e_steps)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(KE):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    e2e_run(KE)
+    s_in.wait_stream(s_out)
+    e1.record(s_in)
     torch.cuda.synchronize()
     spanla.span_la_check()
-    e2e_ms = e0.elapsed_time(e1) / KE
+    e2e_ms = sharding.max_over_ranks(e0.elapsed_time(e1) / KE, pg, dev)
     esize = 2
     h2d = 3 * w.T * w.H * 64 * esize
     d2h = w.T * w.H * 64 * esize
@@ -476,7 +506,8 @@ def main_softmax(args):
                 "cpu_baseline": cpu,
                 "e2e": {"value": w.rows * world / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE,
-                        "mode": "pinned host buffers, copies and call in turn on one stream"},
+                        "mode": "pinned host buffers; copies of step i+1 overlap the call and "
+                                "read-back of step i (two device buffer sets, three streams)"},
                 "gpu_launches": int(sum(p["launches"] for p in launches.values())),
                 "clocks": summarize_clocks(clock_rows, t0, t1),
                 "step_ms_p50": statistics.median(step_ms), "step_ms_min": min(step_ms)}
@@ -534,9 +565,18 @@ def main():
         rows_per_step = int(w.branch_lens.sum())
         row_lo = int(w.branch_cu[0])     # rows a step reads and writes: [row_lo, T)
 
-        def run_on(qq, kk, vv, oo, ss, strm=None):
-            for cu, par in zip(shard_cu, shard_par):
-                spanla.span_la_branches_from_state(cached, qq, kk, vv, cu, par, out=oo, stream=strm)
+        if args.cache:
+            view_cache = spanla.ViewStateCache(w.H, capacity=4)
+            view_cache.put([0x5EED], cached)
+            shard_keys = [np.full(len(c) - 1, 0x5EED, dtype=np.uint64) for c in shard_cu]
+
+            def run_on(qq, kk, vv, oo, ss, strm=None):
+                for cu, keys in zip(shard_cu, shard_keys):
+                    view_cache.branches(keys, qq, kk, vv, cu, out=oo, stream=strm)
+        else:
+            def run_on(qq, kk, vv, oo, ss, strm=None):
+                for cu, par in zip(shard_cu, shard_par):
+                    spanla.span_la_branches_from_state(cached, qq, kk, vv, cu, par, out=oo, stream=strm)
     elif args.per_request:
         # One pass per request over the same buffers: view v and its branches
         # (contiguous in the branch list, grouped by parent).
@@ -739,7 +779,11 @@ def main():
     lib = spanla.load_library()
     dims = spanla.Dims(q.shape[0], q.shape[1], 64, spanla.SPAN_LA_BF16 if w.dtype == "bf16" else spanla.SPAN_LA_F32)
     sh = stream.cuda_stream
-    if shards_mode:
+    if shards_mode and args.cache:
+        raw = [(view_cache._handle, keys.ctypes.data, q.data_ptr(), k.data_ptr(), v.data_ptr(), dims,
+                cu.ctypes.data, len(cu) - 1, out.data_ptr(), sh) for cu, keys in zip(shard_cu, shard_keys)]
+        fn = lib.span_la_cache_branches
+    elif shards_mode:
         raw = [(cached.data_ptr(), 1, q.data_ptr(), k.data_ptr(), v.data_ptr(), dims, cu.ctypes.data,
                 len(cu) - 1, par.ctypes.data, out.data_ptr(), sh) for cu, par in zip(shard_cu, shard_par)]
         fn = lib.span_la_branches_from_state
