@@ -74,6 +74,8 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_k0, const __grid_const
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();                 // the bf16 parts from the split kernel
+  griddep_launch_dependents();    // the scan waits for this grid itself
 
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_tma, 2 * SPLIT * kOperandBytes);
@@ -175,25 +177,31 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_k0, const __grid_const
 
 cudaError_t launch_chunk_state(bool split, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                const ChunkDesc* chunks, int n_chunks, int H, float* ws,
-                               unsigned* err, cudaStream_t stream) {
+                               unsigned* err, cudaStream_t stream, bool pdl) {
   if (n_chunks <= 0) return cudaSuccess;
-  const dim3 grid(n_chunks, (H + kChunkBoxHeads - 1) / kChunkBoxHeads);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_chunks, (H + kChunkBoxHeads - 1) / kChunkBoxHeads);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
   if (split) {
     auto kern = chunk_state_kernel<2>;
-    const uint32_t bytes = ChunkSmem<2>::kRequest;
+    cfg.dynamicSmemBytes = ChunkSmem<2>::kRequest;
     static std::atomic<uint64_t> done{0};
-    cudaError_t e = set_smem_limit_once(kern, bytes, done);
+    cudaError_t e = set_smem_limit_once(kern, static_cast<uint32_t>(cfg.dynamicSmemBytes), done);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, bytes, stream>>>(tm_k[0], tm_k[1], tm_v[0], tm_v[1], chunks, H, ws, err);
-  } else {
-    auto kern = chunk_state_kernel<1>;
-    const uint32_t bytes = ChunkSmem<1>::kRequest;
-    static std::atomic<uint64_t> done{0};
-    cudaError_t e = set_smem_limit_once(kern, bytes, done);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, bytes, stream>>>(tm_k[0], tm_k[0], tm_v[0], tm_v[0], chunks, H, ws, err);
+    return cudaLaunchKernelEx(&cfg, kern, tm_k[0], tm_k[1], tm_v[0], tm_v[1], chunks, H, ws, err);
   }
-  return cudaGetLastError();
+  auto kern = chunk_state_kernel<1>;
+  cfg.dynamicSmemBytes = ChunkSmem<1>::kRequest;
+  static std::atomic<uint64_t> done{0};
+  cudaError_t e = set_smem_limit_once(kern, static_cast<uint32_t>(cfg.dynamicSmemBytes), done);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, kern, tm_k[0], tm_k[0], tm_v[0], tm_v[0], chunks, H, ws, err);
 }
 
 }  // namespace spanla

@@ -11,6 +11,9 @@ namespace {
 __global__ void split_f32_kernel(const float4* __restrict__ q, const float4* __restrict__ k,
                                  const float4* __restrict__ v, int64_t n4,
                                  uint2* __restrict__ parts) {
+  // The chunk-state kernel may be scheduled now; it waits for this grid's
+  // completion before it reads the parts.
+  griddep_launch_dependents();
   const float4* src[3] = {q, k, v};
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {

@@ -95,6 +95,7 @@ tile_output_kernel(const __grid_constant__ CUtensorMap tm_q0, const __grid_const
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();   // prefix states from the scan (and, through it, the bf16 parts)
 
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_tma, 3 * SPLIT * kRowTileBytes);
@@ -336,27 +337,33 @@ tile_output_kernel(const __grid_constant__ CUtensorMap tm_q0, const __grid_const
 cudaError_t launch_tile_output(bool split, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                const CUtensorMap* tm_v, const TileDesc* tiles, int n_tiles,
                                const uint8_t* bounds, const float* stateA, const float* stateB,
-                               void* out, int H, unsigned* err, cudaStream_t stream) {
+                               void* out, int H, unsigned* err, cudaStream_t stream, bool pdl) {
   if (n_tiles <= 0) return cudaSuccess;
-  const dim3 grid(n_tiles, H);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_tiles, H);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
   if (split) {
     auto kern = tile_output_kernel<2>;
-    const uint32_t bytes = TileSmem<2>::kRequest;
+    cfg.dynamicSmemBytes = TileSmem<2>::kRequest;
     static std::atomic<uint64_t> done{0};
-    cudaError_t e = set_smem_limit_once(kern, bytes, done);
+    cudaError_t e = set_smem_limit_once(kern, static_cast<uint32_t>(cfg.dynamicSmemBytes), done);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, bytes, stream>>>(tm_q[0], tm_q[1], tm_k[0], tm_k[1], tm_v[0], tm_v[1],
-                                            tiles, bounds, stateA, stateB, out, H, err);
-  } else {
-    auto kern = tile_output_kernel<1>;
-    const uint32_t bytes = TileSmem<1>::kRequest;
-    static std::atomic<uint64_t> done{0};
-    cudaError_t e = set_smem_limit_once(kern, bytes, done);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, bytes, stream>>>(tm_q[0], tm_q[0], tm_k[0], tm_k[0], tm_v[0], tm_v[0],
-                                            tiles, bounds, stateA, stateB, out, H, err);
+    return cudaLaunchKernelEx(&cfg, kern, tm_q[0], tm_q[1], tm_k[0], tm_k[1], tm_v[0], tm_v[1], tiles, bounds,
+                              stateA, stateB, static_cast<void*>(out), H, err);
   }
-  return cudaGetLastError();
+  auto kern = tile_output_kernel<1>;
+  cfg.dynamicSmemBytes = TileSmem<1>::kRequest;
+  static std::atomic<uint64_t> done{0};
+  cudaError_t e = set_smem_limit_once(kern, static_cast<uint32_t>(cfg.dynamicSmemBytes), done);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, kern, tm_q[0], tm_q[0], tm_k[0], tm_k[0], tm_v[0], tm_v[0], tiles, bounds,
+                            stateA, stateB, static_cast<void*>(out), H, err);
 }
 
 }  // namespace spanla

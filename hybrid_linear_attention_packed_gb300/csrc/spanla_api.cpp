@@ -749,7 +749,7 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
               : counted_launch(kKernelChunk, stream, [&] {
                   return launch_chunk_state(split, chunk_ops.k, chunk_ops.v,
                                             reinterpret_cast<const ChunkDesc*>(block + desc->off_a),
-                                            desc->n_chunks, H, states, dev->err, stream);
+                                            desc->n_chunks, H, states, dev->err, stream, kernel_before);
                 });
       if (e != cudaSuccess) { st = cuda_fail(e, "chunk/span-state launch"); break; }
       kernel_before = true;
@@ -773,10 +773,11 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
                                     block + desc->off_bounds, stateA, states, out, H, dev->err, stream, pdl);
         });
       } else {
+        const bool pdl = kernel_before;
         e = counted_launch(kKernelTile, stream, [&] {
           return launch_tile_output(split, tile_ops.q, tile_ops.k, tile_ops.v,
                                     reinterpret_cast<const TileDesc*>(block + desc->off_b), desc->n_tiles,
-                                    block + desc->off_bounds, stateA, states, out, H, dev->err, stream);
+                                    block + desc->off_bounds, stateA, states, out, H, dev->err, stream, pdl);
         });
       }
       if (e != cudaSuccess) { st = cuda_fail(e, "output launch"); break; }

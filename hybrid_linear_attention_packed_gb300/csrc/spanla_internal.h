@@ -167,7 +167,7 @@ cudaError_t launch_split_f32(const float* q, const float* k, const float* v, int
 
 cudaError_t launch_chunk_state(bool split, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                const ChunkDesc* chunks, int n_chunks, int H, float* ws,
-                               unsigned* err, cudaStream_t stream);
+                               unsigned* err, cudaStream_t stream, bool pdl);
 
 cudaError_t launch_scan(const ScanDesc* scan, int n_scan, int H, float* ws, float* final_out,
                         cudaStream_t stream, bool pdl);
@@ -189,7 +189,7 @@ constexpr int kMaxSpanTiles = 8;
 cudaError_t launch_tile_output(bool split, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                const CUtensorMap* tm_v, const TileDesc* tiles, int n_tiles,
                                const uint8_t* bounds, const float* stateA, const float* stateB,
-                               void* out, int H, unsigned* err, cudaStream_t stream);
+                               void* out, int H, unsigned* err, cudaStream_t stream, bool pdl);
 
 cudaError_t launch_wait_timeout_probe(unsigned limit_us, unsigned* err, cudaStream_t stream);
 
