@@ -128,6 +128,17 @@ void release_events(span_la_view_cache* c) {
 
 // The cache's cross-stream events are host-side state of each call, so its
 // calls are not recorded into CUDA graphs.
+// Calls run on the device the cache was created on.
+span_la_status check_device(const span_la_view_cache* c) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cache_fail(SPAN_LA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev != c->device)
+    return cache_fail(SPAN_LA_ERR_INVALID, "the current device is %d; the cache lives on device %d", dev,
+                      c->device);
+  return SPAN_LA_OK;
+}
+
 span_la_status refuse_capture(cudaStream_t stream) {
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   cudaError_t e = cudaStreamIsCapturing(stream, &cap);
@@ -203,7 +214,8 @@ span_la_status span_la_cache_put(span_la_view_cache* cache, const uint64_t* keys
     return cache_fail(SPAN_LA_ERR_INVALID, "states must be 16-byte aligned");
   std::unordered_set<uint64_t> keep(keys, keys + n);
   if (static_cast<int32_t>(keep.size()) != n) return cache_fail(SPAN_LA_ERR_INVALID, "keys are not distinct");
-  span_la_status cst = refuse_capture(stream);
+  span_la_status cst = check_device(cache);
+  if (cst == SPAN_LA_OK) cst = refuse_capture(stream);
   if (cst != SPAN_LA_OK) return cst;
   std::lock_guard<std::mutex> lock(cache->mu);
   const size_t state_bytes = static_cast<size_t>(cache->heads) * kStateBytesPerHead;
@@ -262,7 +274,8 @@ span_la_status span_la_cache_branches(span_la_view_cache* cache, const uint64_t*
                       cache->heads);
   if (num_branches < 0 || (num_branches > 0 && parent_keys == nullptr))
     return cache_fail(SPAN_LA_ERR_INVALID, "bad parent key array");
-  span_la_status cst = refuse_capture(stream);
+  span_la_status cst = check_device(cache);
+  if (cst == SPAN_LA_OK) cst = refuse_capture(stream);
   if (cst != SPAN_LA_OK) return cst;
   std::vector<int32_t> slots(num_branches);
   {

@@ -334,7 +334,9 @@ span_la_status span_la_softmax_branches_from_kv(const void *view_k, const void *
  * on whatever streams they were enqueued.  The caller still orders the
  * states a put copies from (normally by putting on the stream of the pass
  * that wrote them).  A cache object may be used from several host threads
- * (calls are serialised by a lock); it is not tied to a stream.  Puts and
+ * (calls are serialised by a lock); it is not tied to a stream, but puts and
+ * branch calls must be made with its device current (else
+ * SPAN_LA_ERR_INVALID).  Puts and
  * branch calls on a stream that is being captured into a CUDA graph return
  * SPAN_LA_ERR_UNSUPPORTED (the ordering events are per-call host state).
  */
