@@ -80,3 +80,26 @@ def test_random_softmax_passes(cuda_device, seed):
     print("seed %d scale %g: V=%d B=%d H=%d rows=%d out %.2e lse %.2e"
           % (seed, scale, w.V, w.B, w.H, w.rows, e, el))
     assert e <= TOL["bf16"] and el <= TOL["bf16"]
+
+
+def test_many_heads_both_layers(cuda_device):
+    """48 heads: the head index runs through TMA coordinates, the schedules and
+    the state layout [n][H][64][64]."""
+    w = workloads.make_pass([300, 129], [40, 1, 130], [0, 1, 1], H=48, dtype="bf16", seed=91,
+                            q_scale=1.0, k_scale=1.0)
+    q, k, v = to_device(w, cuda_device)
+    out, state = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
+                              out=torch.full_like(q, float("nan")))
+    sm = span_la_softmax_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
+                              out=torch.full_like(q, float("nan")))
+    span_la_check()
+    ref, ref_state = oracle_pass(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu,
+                                 w.branch_parent)
+    sref, _ = oracle_softmax_pass(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu,
+                                  w.branch_parent)
+    seg = segment_rows(w)
+    e = rel_err(f64(out)[seg], ref[seg])
+    es = rel_err(f64(state), ref_state)
+    e_sm = rel_err(f64(sm)[seg], sref[seg])
+    print("48 heads: linear out %.2e state %.2e; softmax out %.2e" % (e, es, e_sm))
+    assert e <= TOL["bf16"] and es <= TOL["bf16"] and e_sm <= TOL["bf16"]
