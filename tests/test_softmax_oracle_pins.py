@@ -213,3 +213,43 @@ def test_bad_metadata_is_rejected():
         oracle_softmax_pass(q, q, q, [0, 5], [5, 3], [0])
     with pytest.raises(ValueError):
         oracle_softmax_pass(q, q, q, [0, 5], [5, 8], [1])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_packed_passes_equal_library_attention(seed):
+    """Whole random packed passes (views, branches, rows in no segment) against
+    the library routine with the visibility of every row over the whole buffer
+    written out from the rule."""
+    rng = np.random.default_rng([seed, 5])
+    V = int(rng.integers(1, 4))
+    vl = [int(x) for x in rng.integers(0, 90, size=V)]
+    bl, par = [], []
+    for v in range(V):
+        for _ in range(int(rng.integers(0, 4))):
+            bl.append(int(rng.integers(0, 40)))
+            par.append(v)
+    lead = int(rng.integers(0, 5))
+    vcu = _cu(vl, lead)
+    bcu = _cu(bl, int(vcu[-1]) + int(rng.integers(0, 5)))
+    T = int(bcu[-1]) + int(rng.integers(0, 5))
+    H, D = 2, 16
+    q, k, v = _rand(rng, T, H, D), _rand(rng, T, H, D), _rand(rng, T, H, D)
+    scale = float(rng.choice([0.1, 0.25, 0.6]))
+    out, _ = oracle_softmax_pass(q, k, v, vcu, bcu, par, scale=scale, fill=7.0)
+    mask = np.zeros((T, T), dtype=bool)
+    seg = np.zeros(T, dtype=bool)
+    for s in range(V):
+        for t in range(vcu[s], vcu[s + 1]):
+            mask[t, vcu[s]:t + 1] = True
+            seg[t] = True
+    for b in range(len(bl)):
+        p = par[b]
+        for t in range(bcu[b], bcu[b + 1]):
+            mask[t, vcu[p]:vcu[p + 1]] = True
+            mask[t, bcu[b]:t + 1] = True
+            seg[t] = True
+    rows = np.flatnonzero(seg)
+    if rows.size:
+        ref = _sdpa(q[rows], k, v, mask=mask[rows], scale=scale)
+        assert np.max(np.abs(out[rows] - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+    assert np.all(out[~seg] == 7.0)
