@@ -292,3 +292,43 @@ def test_rows_outside_segments_untouched_and_bad_metadata_rejected():
         oracle_pass(q, k, v, [5, 2], [5], [])
     with pytest.raises(ValueError):
         oracle_pass(q, k, v, [0, 5], [5, 8], [1])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_packed_passes_equal_quadratic_forms(seed):
+    """Whole random packed passes through the C recurrence against the masked
+    quadratic form per segment, each branch started from its parent's final
+    state written in closed form (K_p^T V_p by einsum), rows of no segment
+    untouched."""
+    rng = np.random.default_rng([seed, 9])
+    V = int(rng.integers(1, 4))
+    vl = [int(x) for x in rng.integers(0, 150, size=V)]
+    bl, par = [], []
+    for v in range(V):
+        for _ in range(int(rng.integers(0, 4))):
+            bl.append(int(rng.integers(0, 80)))
+            par.append(v)
+    vcu = _cu(vl, int(rng.integers(0, 5)))
+    bcu = _cu(bl, int(vcu[-1]) + int(rng.integers(0, 5)))
+    T = int(bcu[-1]) + int(rng.integers(0, 5))
+    H, D = 2, 8
+    q, k, v = _rand(rng, T, H, D), _rand(rng, T, H, D), _rand(rng, T, H, D)
+    out, state = oracle_pass(q, k, v, vcu, bcu, par, fill=5.0)
+    seg = np.zeros(T, dtype=bool)
+    for s in range(V):
+        a, e = vcu[s], vcu[s + 1]
+        seg[a:e] = True
+        final = np.einsum("thi,thj->hij", k[a:e], v[a:e])
+        assert np.max(np.abs(state[s] - final)) <= 1e-12 * max(1.0, np.max(np.abs(final)))
+        if e > a:
+            ref, _ = segment_quadratic(q[a:e], k[a:e], v[a:e])
+            assert _rel(out[a:e], ref) <= 1e-12
+    for b in range(len(bl)):
+        a, e = bcu[b], bcu[b + 1]
+        seg[a:e] = True
+        pa, pe = vcu[par[b]], vcu[par[b] + 1]
+        S0 = np.einsum("thi,thj->hij", k[pa:pe], v[pa:pe])
+        if e > a:
+            ref, _ = segment_quadratic(q[a:e], k[a:e], v[a:e], S0)
+            assert _rel(out[a:e], ref) <= 1e-12
+    assert np.all(out[~seg] == 5.0)
