@@ -205,3 +205,22 @@ def test_fault_injection_knob(lib):
     assert lib.span_la_fault_inject(spanla.FAULT_ALLOC, -1) == 1
     assert lib.span_la_fault_inject(spanla.FAULT_ALLOC, 2) == 0
     assert lib.span_la_fault_inject(spanla.FAULT_ALLOC, 0) == 0
+
+
+def test_c_client_builds_against_the_header(lib, tmp_path):
+    """The plain C client compiles and links against include/spanla.h and
+    libspanla.so (it runs in the GPU tests)."""
+    import shutil
+    import subprocess
+    cuda = next((c for c in (os.environ.get("CUDA_HOME"), "/usr/local/cuda")
+                 if c and os.path.exists(os.path.join(c, "include", "cuda_runtime_api.h"))), None)
+    if cuda is None or shutil.which("gcc") is None:
+        pytest.skip("no CUDA headers or gcc")
+    lib_path = spanla_build.build()
+    exe = str(tmp_path / "spanla_client")
+    r = subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-Werror", "-o", exe,
+                        os.path.join(ROOT, "tests", "c_client", "spanla_client.c"),
+                        "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include"),
+                        "-L", os.path.dirname(lib_path), "-lspanla", "-L", os.path.join(cuda, "lib64"),
+                        "-lcudart"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
