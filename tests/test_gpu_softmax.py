@@ -142,6 +142,23 @@ def test_sibling_order_does_not_matter(cuda_device):
     assert rel_err(out2, out[rows]) <= TOL
 
 
+@pytest.mark.parametrize("growth", [0.02, 0.1])
+def test_rising_scores_take_the_rescale_path(cuda_device, growth):
+    """Key norms grow along each segment, so a later key block's maximum keeps
+    exceeding the reference maximum by more than the 2^8 margin: O and the
+    partial row sums are rescaled many times (by both warps of a row) and the
+    result must still match the oracle; lse too."""
+    w = workloads.make_pass([1000, 300], [60, 200, 9], [0, 0, 1], H=2, dtype="bf16", seed=33,
+                            q_scale=1.0, k_scale=1.0)
+    ramp = torch.ones(w.T)
+    for cu in (w.view_cu, w.branch_cu):
+        for s in range(len(cu) - 1):
+            n = int(cu[s + 1] - cu[s])
+            ramp[int(cu[s]):int(cu[s + 1])] = 1.0 + growth * torch.arange(n, dtype=torch.float32)
+    w.k = (w.k.float() * ramp[:, None, None]).to(torch.bfloat16)
+    _check_full(w, cuda_device)
+
+
 def test_rejections_and_empty_pass(cuda_device):
     dev = cuda_device
     q = torch.zeros((10, 2, 64), dtype=torch.float32, device=dev)
