@@ -186,3 +186,30 @@ def test_empty_and_degenerate_passes(cuda_device):
     out, state = span_la_pass(z, z, z, [0, 0], [0, 0], [0])
     span_la_check()
     assert state.shape == (1, 2, 64, 64) and torch.all(state == 0)
+
+
+def test_packed_pass_equals_one_pass_per_request(cuda_device):
+    """A shared pass of four requests against each request run as its own pass
+    over the same buffers (the page, "Kernels": shared branch passes): both
+    match the oracle and each other within the bf16 tolerance."""
+    w = workloads.packed_four(2)
+    q, k, v = to_device(w, cuda_device)
+    shared, shared_state = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
+                                        out=torch.full_like(q, float("nan")))
+    alone = torch.full_like(q, float("nan"))
+    alone_state = torch.zeros_like(shared_state)
+    for vi in range(w.V):
+        bsel = np.flatnonzero(w.branch_parent == vi)
+        bcu = w.branch_cu[bsel[0]:bsel[-1] + 2] if bsel.size else np.zeros(0, np.int32)
+        span_la_pass(q, k, v, w.view_cu[vi:vi + 2], bcu, np.zeros(bsel.size, np.int32), out=alone,
+                     view_state_out=alone_state[vi:vi + 1])
+    span_la_check()
+    ref, ref_state = _oracle(w)
+    seg = segment_rows(w)
+    e_shared = rel_err(f64(shared)[seg], ref[seg])
+    e_alone = rel_err(f64(alone)[seg], ref[seg])
+    e_pair = rel_err(f64(alone)[seg], f64(shared)[seg])
+    e_state = rel_err(f64(alone_state), f64(shared_state))
+    print("shared %.2e, per request %.2e, between %.2e, states %.2e" % (e_shared, e_alone, e_pair, e_state))
+    assert max(e_shared, e_alone, e_pair, e_state) <= TOL["bf16"]
+    assert torch.isnan(alone[torch.from_numpy(~seg).to(cuda_device)]).all()
