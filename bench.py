@@ -431,12 +431,22 @@ def main_softmax(args):
     peak_src = "measured (burst)" if peak else "fallback"
     peak = peak or 1900.0
     achieved = flops / (kern_us / 1e6) / 1e12
+    # The tensor work the kernel issues: one 128x128x64 Q K^T and one 128x64x128
+    # P V per (query tile, key block), masked or not.
+    sa_plan = spanla.softmax_plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H,
+                                        torch.cuda.get_device_properties(dev).multi_processor_count)
+    mma_flops = sa_plan["key_blocks"] * 2 * (2 * 128 * 128 * 64)
+    roofline_mma = {"issued_flops_per_launch": mma_flops,
+                    "issued_tflops": mma_flops / (kern_us / 1e6) / 1e12,
+                    "issued_frac": mma_flops / (kern_us / 1e6) / 1e12 / peak,
+                    "plan": sa_plan}
     roofline = {"bound": "tensor", "kernel": "softmax_attn", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": recorded_traffic("softmax_attn", args.workload),
                 "peak_source": peak_src, "alg_flops_per_launch": flops,
                 "visible_pairs_per_head": pairs,
-                "exp_per_s": pairs * w.H / (kern_us / 1e6)}
+                "exp_per_s": pairs * w.H / (kern_us / 1e6),
+                "tensor_issued": roofline_mma}
 
     # End to end with host buffers: every step copies its q, k, v in from
     # pinned memory, runs the call and reads out back, pipelined over two

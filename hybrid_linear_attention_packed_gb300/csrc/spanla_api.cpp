@@ -1099,6 +1099,31 @@ const char* span_la_last_error_detail(void) { return g_detail.c_str(); }
 
 int32_t span_la_version(void) { return 100; }
 
+span_la_status span_la_softmax_plan_stats(const int32_t* view_cu_seqlens, int32_t num_views,
+                                          const int32_t* branch_cu_seqlens, int32_t num_branches,
+                                          const int32_t* branch_parent, int32_t num_heads, int32_t num_sms,
+                                          int64_t* stats) {
+  g_detail.clear();
+  if (stats == nullptr) return fail(SPAN_LA_ERR_INVALID, "stats is NULL");
+  if (num_heads < 1) return fail(SPAN_LA_ERR_INVALID, "num_heads %d < 1", num_heads);
+  if (num_sms < 1) return fail(SPAN_LA_ERR_INVALID, "num_sms %d < 1", num_sms);
+  std::vector<Segment> segs;
+  span_la_status st = SPAN_LA_OK;
+  if ((st = check_cu(view_cu_seqlens, num_views, INT32_MAX, "view_cu_seqlens", &segs, true)) != SPAN_LA_OK) return st;
+  if ((st = check_cu(branch_cu_seqlens, num_branches, INT32_MAX, "branch_cu_seqlens", &segs, false)) != SPAN_LA_OK) return st;
+  if ((st = check_overlap(segs)) != SPAN_LA_OK) return st;
+  if ((st = check_parents(branch_parent, num_branches, num_views)) != SPAN_LA_OK) return st;
+  const SoftmaxPlan plan = make_softmax_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
+                                             branch_parent, num_heads, num_sms);
+  int64_t rows = 0;
+  for (const SaItem& it : plan.items) rows += it.nrows;
+  stats[0] = static_cast<int64_t>(plan.items.size());
+  stats[1] = rows;
+  stats[2] = plan.key_blocks;
+  stats[3] = plan.grid;
+  return SPAN_LA_OK;
+}
+
 span_la_status span_la_plan_stats(const int32_t* view_cu_seqlens, int32_t num_views,
                                   const int32_t* branch_cu_seqlens, int32_t num_branches,
                                   const int32_t* branch_parent, int32_t num_parents,

@@ -33,7 +33,7 @@ EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
             "span_la_pass_noalloc", "span_la_cache_create", "span_la_cache_destroy",
             "span_la_cache_put", "span_la_cache_contains", "span_la_cache_branches",
             "span_la_cache_stats", "span_la_softmax_pass", "span_la_softmax_branches_from_kv",
-            "span_la_fault_inject")
+            "span_la_fault_inject", "span_la_softmax_plan_stats")
 NUM_KERNELS = 7
 
 
@@ -102,6 +102,10 @@ def load_library(path: Optional[str] = None):
         lib.span_la_softmax_pass.argtypes = [vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
                                              ctypes.c_int32, i32p, ctypes.c_float, vp, vp, vp]
         lib.span_la_softmax_pass.restype = ctypes.c_int
+        lib.span_la_softmax_plan_stats.argtypes = [i32p, ctypes.c_int32, i32p, ctypes.c_int32, i32p,
+                                                   ctypes.c_int32, ctypes.c_int32,
+                                                   ctypes.POINTER(ctypes.c_int64)]
+        lib.span_la_softmax_plan_stats.restype = ctypes.c_int
         lib.span_la_fault_inject.argtypes = [ctypes.c_int32, ctypes.c_int32]
         lib.span_la_fault_inject.restype = ctypes.c_int
         lib.span_la_softmax_branches_from_kv.argtypes = [vp, vp, ctypes.c_int64, i32p, ctypes.c_int32,
@@ -438,6 +442,22 @@ def plan_stats(view_cu_seqlens, branch_cu_seqlens, branch_parent, num_heads: int
                                        1 if from_state else 0, int(num_heads), dt, stats),
            "span_la_plan_stats")
     return dict(zip(PLAN_FIELDS, (int(x) for x in stats)))
+
+
+SOFTMAX_PLAN_FIELDS = ("items", "rows", "key_blocks", "grid")
+
+
+def softmax_plan_stats(view_cu_seqlens, branch_cu_seqlens, branch_parent, num_heads: int,
+                       num_sms: int = 152) -> dict:
+    """Work units of the softmax layer for this metadata (host only)."""
+    lib = load_library()
+    vcu, bcu, par = _i32(view_cu_seqlens), _i32(branch_cu_seqlens), _i32(branch_parent)
+    V = max(len(vcu) - 1, 0)
+    B = max(len(bcu) - 1, 0)
+    stats = (ctypes.c_int64 * len(SOFTMAX_PLAN_FIELDS))()
+    _raise(lib, lib.span_la_softmax_plan_stats(_iptr(vcu), V, _iptr(bcu), B, _iptr(par), int(num_heads),
+                                               int(num_sms), stats), "span_la_softmax_plan_stats")
+    return dict(zip(SOFTMAX_PLAN_FIELDS, (int(x) for x in stats)))
 
 
 def profile_enable(on: bool = True) -> None:

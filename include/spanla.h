@@ -216,6 +216,22 @@ span_la_status span_la_selftest_wait_timeout(int32_t limit_us, cudaStream_t stre
 span_la_status span_la_fault_inject(int32_t kind, int32_t count);
 
 /*
+ * span_la_softmax_plan_stats -- host only, no CUDA call: the work units of
+ * span_la_softmax_pass for this metadata, head count and number of CTAs
+ * (normally the SM count), into stats[0..3]:
+ *   stats[0] work items: (query tile of <= 128 rows, head) pairs
+ *   stats[1] query rows those items cover (summed over heads)
+ *   stats[2] key blocks the items process: each is one 128 x 128 x 64 Q K^T
+ *            and one 128 x 64 x 128 P V product on the tensor cores
+ *   stats[3] CTAs the launch uses
+ * Returns SPAN_LA_ERR_INVALID on bad metadata, like the entry point.
+ */
+span_la_status span_la_softmax_plan_stats(const int32_t *view_cu_seqlens, int32_t num_views,
+                                          const int32_t *branch_cu_seqlens, int32_t num_branches,
+                                          const int32_t *branch_parent, int32_t num_heads,
+                                          int32_t num_sms, int64_t *stats);
+
+/*
  * span_la_plan_stats -- host only, no CUDA call: the work units a call with
  * this metadata, head count and dtype would launch (used to count the
  * algorithmic bytes of each kernel).

@@ -224,3 +224,21 @@ def test_c_client_builds_against_the_header(lib, tmp_path):
                         "-L", os.path.dirname(lib_path), "-lspanla", "-L", os.path.join(cuda, "lib64"),
                         "-lcudart"], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_softmax_plan_covers_every_segment_row_once(lib):
+    """Host-only plan of the softmax layer: the items cover every segment row of
+    every head once; a view tile j of a view sees j + 1 key blocks, a branch
+    tile its parent's blocks plus its own."""
+    from hybrid_linear_attention_packed_gb300 import workloads
+    w = workloads.make_pass([300, 129, 0], [40, 9, 130, 1], [0, 0, 1, 2], H=3, dtype="bf16", seed=1)
+    st = spanla.softmax_plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H, num_sms=152)
+    assert st["rows"] == w.rows * w.H
+    # views: 300 rows -> tiles with 1, 2, 3 blocks; 129 -> 1, 2.  Branches of view 0 (40 + 9 rows,
+    # one packed tile): 3 prefix blocks + 1; branch 130 of view 1: two tiles, 2 prefix blocks + 1 or
+    # 2 own; branch 1 of the empty view 2: 1 block.
+    per_head = (1 + 2 + 3) + (1 + 2) + (3 + 1) + (2 + 1) + (2 + 2) + 1
+    assert st["key_blocks"] == per_head * w.H
+    assert st["items"] == (3 + 2 + 1 + 2 + 1) * w.H
+    assert st["grid"] == min(152, st["items"])
+    assert lib.span_la_softmax_plan_stats(None, 1, None, 0, None, 1, 152, None) == 1
