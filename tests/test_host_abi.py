@@ -242,3 +242,35 @@ def test_softmax_plan_covers_every_segment_row_once(lib):
     assert st["items"] == (3 + 2 + 1 + 2 + 1) * w.H
     assert st["grid"] == min(152, st["items"])
     assert lib.span_la_softmax_plan_stats(None, 1, None, 0, None, 1, 152, None) == 1
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_metadata_plans_cover_every_row(lib, seed):
+    """Random packed-pass metadata (host only): both planners cover every segment
+    row of every head exactly once, the softmax plan needs at least one key
+    block per query tile, and a branch naming a view that does not exist is
+    rejected by both."""
+    rng = np.random.default_rng([seed, 3])
+    V = int(rng.integers(1, 8))
+    vl = rng.integers(0, 3000, size=V)
+    counts = rng.integers(0, 12, size=V)
+    bl = rng.integers(0, 300, size=int(counts.sum()))
+    par = np.repeat(np.arange(V), counts).astype(np.int32)
+    vcu = np.concatenate([[0], np.cumsum(vl)]).astype(np.int32)
+    bcu = (np.concatenate([[0], np.cumsum(bl)]) + vcu[-1]).astype(np.int32)
+    H = int(rng.integers(1, 17))
+    rows = int(vl.sum() + bl.sum())
+    for dtype in ("bf16", "f32"):
+        st = spanla.plan_stats(vcu, bcu, par, H, dtype)
+        assert st["tile_rows"] == rows
+    sa = spanla.softmax_plan_stats(vcu, bcu, par, H, num_sms=152)
+    assert sa["rows"] == rows * H
+    assert sa["key_blocks"] >= sa["items"]
+    assert sa["grid"] == (min(152, sa["items"]) if sa["items"] else 0)
+    if len(par):
+        bad = par.copy()
+        bad[-1] = V
+        with pytest.raises(spanla.SpanLAError):
+            spanla.plan_stats(vcu, bcu, bad, H)
+        with pytest.raises(spanla.SpanLAError):
+            spanla.softmax_plan_stats(vcu, bcu, bad, H)
