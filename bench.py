@@ -225,16 +225,32 @@ def cpu_model() -> str:
 
 def oracle_time(w, budget_s: float = 8.0, max_reps: int = 50, nthreads: int = 0):
     """Time the float64 oracle on the whole workload, repeated within ~budget_s
-    (nthreads = 0: every host core)."""
+    (nthreads = 0: every host core); also returns its last result."""
     from oracle import oracle_max_threads, oracle_pass
     q, k, v = (t.double().numpy() for t in (w.q, w.k, w.v))
     times = []
+    result = None
     t_all = time.perf_counter()
     while len(times) < max_reps and (time.perf_counter() - t_all) < budget_s:
         t0 = time.perf_counter()
-        oracle_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, nthreads=nthreads)
+        result = oracle_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, nthreads=nthreads)
         times.append(time.perf_counter() - t0)
-    return statistics.median(times), len(times), (nthreads or oracle_max_threads())
+    return statistics.median(times), len(times), (nthreads or oracle_max_threads()), result
+
+
+def segment_mask(w):
+    m = np.zeros(w.T, dtype=bool)
+    for cu in (w.view_cu, w.branch_cu):
+        for s_ in range(len(cu) - 1):
+            m[int(cu[s_]):int(cu[s_ + 1])] = True
+    return m
+
+
+def max_rel_err(got, ref):
+    """max |got - ref| / max |ref| (the parity tests' measure)."""
+    den = float(np.max(np.abs(ref))) if ref.size else 0.0
+    diff = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    return diff / den if den > 0 else diff
 
 
 def run_reference(args):
@@ -314,12 +330,13 @@ def softmax_oracle_time(w, budget_s: float = 20.0, max_reps: int = 3):
     from oracle import oracle_softmax_pass
     q, k, v = (t.double().numpy() for t in (w.q, w.k, w.v))
     times = []
+    result = None
     t_all = time.perf_counter()
     while len(times) < max_reps and (time.perf_counter() - t_all) < budget_s:
         t0 = time.perf_counter()
-        oracle_softmax_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+        result = oracle_softmax_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
         times.append(time.perf_counter() - t0)
-    return statistics.median(times), len(times)
+    return statistics.median(times), len(times), result
 
 
 def softmax_cpu_line(w, value, reps, args):
@@ -337,7 +354,7 @@ def run_softmax_reference(args):
         return 0
     from hybrid_linear_attention_packed_gb300 import workloads
     w = workloads.by_name(args.workload, args.seed)
-    med, reps = softmax_oracle_time(w, budget_s=60.0, max_reps=max(1, min(args.steps, 10)))
+    med, reps, _ = softmax_oracle_time(w, budget_s=60.0, max_reps=max(1, min(args.steps, 10)))
     value = w.rows / med
     cpu = softmax_cpu_line(w, value, reps, args)
     line = {"impl": "reference", "metric": SOFTMAX_METRIC, "value": value, "unit": UNIT,
@@ -503,8 +520,12 @@ def main_softmax(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        med, reps = softmax_oracle_time(w)
+        med, reps, (ref, _) = softmax_oracle_time(w)
         cpu = softmax_cpu_line(w, w.rows / med, reps, args)
+        # The benchmarked output against the oracle's (the parity tests' measure).
+        seg = segment_mask(w)
+        got = out.detach().double().cpu().numpy()
+        cpu["max_rel_err_vs_gpu"] = max_rel_err(got[seg], ref[seg])
     if rank == 0:
         line = {"metric": SOFTMAX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -860,14 +881,21 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not shards_mode:
-        med, reps, cores = oracle_time(w)
-        med1, reps1, _ = oracle_time(w, budget_s=6.0, max_reps=3, nthreads=1)
+        med, reps, cores, (ref, ref_state) = oracle_time(w)
+        med1, reps1, _, _ = oracle_time(w, budget_s=6.0, max_reps=3, nthreads=1)
         cpu = {"value": w.rows / med, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "the whole workload (%d rows x %d heads), median of %d passes"
                          % (w.rows, w.H, reps),
                "one_thread": {"value": w.rows / med1, "unit": UNIT, "cores": 1,
                               "sample": "median of %d passes" % reps1},
                "cpu_model": cpu_model()}
+        # The benchmarked pass's output and view states against the oracle's
+        # (the parity tests' measure).
+        seg = segment_mask(w)
+        got = out.detach().double().cpu().numpy()
+        cpu["max_rel_err_vs_gpu"] = {
+            "out": max_rel_err(got[seg], ref[seg]),
+            "view_states": max_rel_err(state.detach().double().cpu().numpy(), ref_state)}
 
     vs = None
     if args.workload == "single":
