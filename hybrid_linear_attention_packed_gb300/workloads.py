@@ -129,6 +129,32 @@ def make_pass(view_lens: Sequence[int], branch_lens: Sequence[int],
                     view_cu, branch_cu, q, k, v)
 
 
+def pass_layout(view_lens: Sequence[int], branch_lens: Sequence[int]):
+    """int32 (view_cu, branch_cu) of a pass packed with no gaps (views, then
+    branches), for passes whose inputs are drawn on the device."""
+    view_cu = _cu(np.asarray(view_lens, dtype=np.int64).reshape(-1), 0)
+    branch_cu = _cu(np.asarray(branch_lens, dtype=np.int64).reshape(-1), int(view_cu[-1]))
+    return view_cu, branch_cu
+
+
+def draw_qkv_device(seed: int, T: int, H: int, device, q_scale: float = 1.0 / 8,
+                    k_scale: float = 1.0 / 8, v_scale: float = 1.0, D: int = HEAD_DIM):
+    """q, k, v [T, H, D] bf16 drawn on ``device`` by torch's generator for that
+    device, seeded with ``seed`` (q, k, v in that order, each a standard normal
+    times its scale): passes of billions of elements that host generation
+    would take minutes to draw and copy.  Tests read back only the rows they
+    check."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out = []
+    for scale in (q_scale, k_scale, v_scale):
+        x = torch.randn((T, H, D), generator=g, device=device, dtype=torch.bfloat16)
+        if scale != 1.0:
+            x.mul_(scale)
+        out.append(x)
+    return tuple(out)
+
+
 def tiny_oracle_case(seed: int = 0) -> Workload:
     """1 head, d=64, fp32, q,k,v ~ N(0,1)/8; views of 130 and 77 tokens; three
     branches of 9, 14 and 20 tokens per view, each forking from its view."""
