@@ -536,12 +536,16 @@ cudaError_t upload_descriptors(void* dst, std::vector<uint8_t>&& bytes, bool cap
 // ------------------------------------------------------------------ plan cache
 // Passes with the same metadata (every layer of a model step, for instance)
 // reuse one uploaded descriptor block: the plan depends on the metadata, the
-// head count, the dtype and the SM count only.  A block is uploaded on the
-// calling stream; a call on another stream first waits for that upload.  At
-// most kCacheEntries blocks are kept per process; evicting one synchronises
-// the device before freeing it.  Calls made while their stream is being
-// captured into a graph bypass the cache.
+// head count, the dtype and the SM count only.  A block is a stream-ordered
+// allocation uploaded on the calling stream; a call on another stream first
+// waits for that upload.  At most kCacheEntries blocks are kept per device.
+// Every call that reads a block records an event on its stream afterwards
+// (one event per stream, at most kMaxReaders streams per block), so that
+// evicting a block frees it in stream order behind its last reads, without
+// synchronising the host.  Calls made while their stream is being captured
+// into a graph bypass the cache.
 constexpr int kCacheEntries = 16;
+constexpr size_t kMaxReaders = 8;
 
 struct CacheEntry {
   int device = -1;
@@ -550,8 +554,55 @@ struct CacheEntry {
   uint8_t* d_block = nullptr;
   cudaEvent_t uploaded = nullptr;
   cudaStream_t upload_stream = nullptr;
+  std::vector<std::pair<cudaStream_t, cudaEvent_t>> readers;   // last read per stream
+  bool sync_on_evict = false;   // a read could not be recorded: synchronise before freeing
   uint64_t last_use = 0;
 };
+
+// Records on `stream` that the launches just enqueued there read `en`'s
+// block.  A new stream beyond kMaxReaders takes over the oldest reader: it
+// first waits for that reader's event, so its own event covers both.
+cudaError_t note_reader(CacheEntry& en, cudaStream_t stream) {
+  for (auto& r : en.readers)
+    if (r.first == stream) return cudaEventRecord(r.second, stream);
+  if (en.readers.size() >= kMaxReaders) {
+    auto& oldest = en.readers.front();
+    cudaError_t e = cudaStreamWaitEvent(stream, oldest.second, 0);
+    if (e != cudaSuccess) return e;
+    oldest.first = stream;
+    e = cudaEventRecord(oldest.second, stream);
+    std::rotate(en.readers.begin(), en.readers.begin() + 1, en.readers.end());
+    return e;
+  }
+  cudaEvent_t ev = nullptr;
+  cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return e;
+  e = cudaEventRecord(ev, stream);
+  if (e != cudaSuccess) {
+    cudaEventDestroy(ev);
+    return e;
+  }
+  en.readers.emplace_back(stream, ev);
+  return cudaSuccess;
+}
+
+// Frees `en`'s block on `stream` behind its upload and every recorded read.
+// On failure the block is left allocated (and the entry is kept).
+cudaError_t release_entry(CacheEntry& en, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (en.sync_on_evict) {
+    e = cudaDeviceSynchronize();
+  } else {
+    e = cudaStreamWaitEvent(stream, en.uploaded, 0);
+    for (const auto& r : en.readers)
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, r.second, 0);
+  }
+  if (e == cudaSuccess) e = cudaFreeAsync(en.d_block, stream);
+  if (e != cudaSuccess) return e;
+  for (const auto& r : en.readers) cudaEventDestroy(r.second);
+  cudaEventDestroy(en.uploaded);
+  return cudaSuccess;
+}
 
 std::mutex g_cache_mu;
 std::vector<CacheEntry> g_cache;
@@ -584,11 +635,13 @@ std::vector<int32_t> plan_key(int device, int dtype, int H, int from_state, int 
 }
 
 // The device block for `key` (built by `build` on a miss), usable on `stream`.
-// The caller holds g_cache_mu until its launches are enqueued, so that no
-// other call evicts the block meanwhile.
+// The caller holds g_cache_mu until its launches are enqueued and recorded
+// with note_reader on `*entry`, so that no other call evicts the block (or
+// moves the entry) meanwhile.
 template <typename Build>
 span_la_status cached_block(const std::vector<int32_t>& key, int device, cudaStream_t stream,
-                            Build&& build, const DescBlock** desc, const uint8_t** block) {
+                            Build&& build, const DescBlock** desc, const uint8_t** block,
+                            CacheEntry** entry) {
   for (CacheEntry& en : g_cache) {
     if (en.device == device && en.key == key) {
       if (en.upload_stream != stream) {
@@ -598,17 +651,20 @@ span_la_status cached_block(const std::vector<int32_t>& key, int device, cudaStr
       en.last_use = ++g_cache_clock;
       *desc = &en.desc;
       *block = en.d_block;
+      *entry = &en;
       return SPAN_LA_OK;
     }
   }
-  if (static_cast<int>(g_cache.size()) >= kCacheEntries) {
-    size_t victim = 0;
-    for (size_t i = 1; i < g_cache.size(); ++i)
-      if (g_cache[i].last_use < g_cache[victim].last_use) victim = i;
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize(plan cache eviction)");
-    cudaFree(g_cache[victim].d_block);
-    cudaEventDestroy(g_cache[victim].uploaded);
+  int on_device = 0;
+  size_t victim = g_cache.size();
+  for (size_t i = 0; i < g_cache.size(); ++i) {
+    if (g_cache[i].device != device) continue;
+    ++on_device;
+    if (victim == g_cache.size() || g_cache[i].last_use < g_cache[victim].last_use) victim = i;
+  }
+  if (on_device >= kCacheEntries) {
+    cudaError_t e = release_entry(g_cache[victim], stream);
+    if (e != cudaSuccess) return cuda_fail(e, "plan cache eviction");
     g_cache.erase(g_cache.begin() + victim);
   }
   CacheEntry en;
@@ -617,15 +673,17 @@ span_la_status cached_block(const std::vector<int32_t>& key, int device, cudaStr
   en.desc = build();
   const size_t bytes = std::max<size_t>(en.desc.host.size(), 256);
   if (injected_alloc_failure())
-    return fail(SPAN_LA_ERR_NOMEM, "cudaMalloc(descriptors, %zu): injected failure", bytes);
-  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&en.d_block), bytes);
-  if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMalloc(descriptors, %zu): %s", bytes, cudaGetErrorString(e));
+    return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(descriptors, %zu): injected failure", bytes);
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&en.d_block), bytes, stream);
+  if (e != cudaSuccess)
+    return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(descriptors, %zu): %s", bytes, cudaGetErrorString(e));
   if (!en.desc.host.empty())
     e = cudaMemcpyAsync(en.d_block, en.desc.host.data(), en.desc.host.size(), cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&en.uploaded, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventRecord(en.uploaded, stream);
   if (e != cudaSuccess) {
-    cudaFree(en.d_block);
+    if (en.uploaded != nullptr) cudaEventDestroy(en.uploaded);
+    cudaFreeAsync(en.d_block, stream);
     return cuda_fail(e, "descriptor upload");
   }
   en.upload_stream = stream;
@@ -633,7 +691,17 @@ span_la_status cached_block(const std::vector<int32_t>& key, int device, cudaStr
   g_cache.push_back(std::move(en));
   *desc = &g_cache.back().desc;
   *block = g_cache.back().d_block;
+  *entry = &g_cache.back();
   return SPAN_LA_OK;
+}
+
+// After a call's launches: record the read of its cached block on `stream`.
+span_la_status finish_read(CacheEntry* entry, cudaStream_t stream, span_la_status st) {
+  if (entry == nullptr) return st;
+  const cudaError_t e = note_reader(*entry, stream);
+  if (e == cudaSuccess) return st;
+  entry->sync_on_evict = true;
+  return st == SPAN_LA_OK ? cuda_fail(e, "cudaEventRecord(descriptor read)") : st;
 }
 
 // Common tail of both entry points: descriptors (cached, or uploaded into the
@@ -654,11 +722,12 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
   DescBlock local;
   const DescBlock* desc = nullptr;
   const uint8_t* block = nullptr;
+  CacheEntry* entry = nullptr;
   span_la_status st = SPAN_LA_OK;
   if (use_cache) {
     cache_lock.lock();
     st = cached_block(key, device, stream, [&] { return make_desc(build_plan(), H, dev->num_sms); }, &desc,
-                      &block);
+                      &block, &entry);
     if (st != SPAN_LA_OK) return st;
   } else {
     local = make_desc(build_plan(), H, dev->num_sms);
@@ -783,6 +852,7 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
       if (e != cudaSuccess) { st = cuda_fail(e, "output launch"); break; }
     }
   } while (false);
+  st = finish_read(entry, stream, st);
   cudaError_t ef = cudaFreeAsync(ws, stream);
   if (st == SPAN_LA_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync");
   return st;
@@ -837,10 +907,11 @@ span_la_status run_softmax(const std::vector<int32_t>& key, const int32_t* view_
   DescBlock local;
   const DescBlock* desc = nullptr;
   const uint8_t* block = nullptr;
+  CacheEntry* entry = nullptr;
   span_la_status st = SPAN_LA_OK;
   if (use_cache) {
     cache_lock.lock();
-    st = cached_block(key, device, stream, build, &desc, &block);
+    st = cached_block(key, device, stream, build, &desc, &block, &entry);
     if (st != SPAN_LA_OK) return st;
   } else {
     local = build();
@@ -907,6 +978,7 @@ span_la_status run_softmax(const std::vector<int32_t>& key, const int32_t* view_
       if (e != cudaSuccess) st = cuda_fail(e, "softmax attention launch");
     }
   }
+  st = finish_read(entry, stream, st);
   if (ws != nullptr) {
     cudaError_t ef = cudaFreeAsync(ws, stream);
     if (st == SPAN_LA_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync");

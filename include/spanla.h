@@ -40,7 +40,11 @@
  *   work completes on the stream.
  * Asynchrony.  A call only enqueues work on `stream` (a cudaStream_t on the
  *   current device; 0 = legacy default stream).  Outputs are valid once the
- *   stream has reached the call; inputs must stay unchanged until then.
+ *   stream has reached the call; inputs must stay unchanged until then.  The
+ *   pass, branch and softmax calls do not synchronise the device: the
+ *   per-device cache of launch plans (16 per device, keyed on the metadata,
+ *   least recently used evicted) frees an evicted plan in stream order
+ *   behind the calls that read it.
  * Graphs.  The pass, branch and softmax calls may be recorded while `stream`
  *   is being captured into a CUDA graph: the recorded work replays on the
  *   buffers of the recorded call (their current contents), with its own

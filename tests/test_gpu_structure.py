@@ -173,6 +173,55 @@ def test_plan_reused_across_calls_and_streams(cuda_device):
         assert rel_err(f64(state), ref_state) <= TOL["bf16"]
 
 
+def test_plan_cache_eviction_is_stream_ordered(cuda_device):
+    """More distinct layouts than the plan cache keeps per device (16): each
+    further one evicts the least recently used descriptor block, freed in
+    stream order behind its last reads.  The evicting call returns while its
+    stream is still busy (no host synchronisation); results on the current
+    and a second stream, and of a layout evicted earlier and planned again,
+    match the oracle."""
+    import time
+    from helpers import TOL, f64, rel_err, segment_rows
+    from oracle import oracle_pass
+
+    ws = [workloads.make_pass([300 + 7 * i, 129], [30, 60], [0, 1], H=2, dtype="bf16", seed=100 + i)
+          for i in range(24)]
+    ins = [to_device(w, cuda_device) for w in ws]
+
+    def call(i):
+        w, (q, k, v) = ws[i], ins[i]
+        return span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
+                            out=torch.full_like(q, float("nan")))
+
+    def check(i, res):
+        w = ws[i]
+        ref, ref_state = oracle_pass(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu, w.branch_parent)
+        seg = segment_rows(w)
+        assert rel_err(f64(res[0])[seg], ref[seg]) <= TOL["bf16"]
+        assert rel_err(f64(res[1]), ref_state) <= TOL["bf16"]
+
+    results = {i: call(i) for i in range(17)}     # the 17th layout at the latest evicts
+    torch.cuda.synchronize()
+    span_la_check()
+    torch.cuda._sleep(400_000_000)                # ~200 ms of device work ahead of the call
+    t0 = time.perf_counter()
+    results[17] = call(17)                        # a miss that evicts
+    host_ms = (time.perf_counter() - t0) * 1e3
+    torch.cuda.synchronize()
+    span_la_check()
+    assert host_ms < 50.0, "an evicting call waited for the device (%.1f ms)" % host_ms
+    side = torch.cuda.Stream(device=cuda_device)
+    for i in range(18, 24):
+        with torch.cuda.stream(side if i % 2 else torch.cuda.current_stream(cuda_device)):
+            torch.cuda._sleep(2_000_000)
+            results[i] = call(i)
+    results[0] = call(0)                          # evicted above, planned again
+    torch.cuda.synchronize()
+    span_la_check()
+    for i, res in results.items():
+        check(i, res)
+
+
 def _graph_replay_equals_eager(dev, record, w_a, w_b):
     """Record `record(q, k, v, outs)` into a CUDA graph on inputs A, replay it
     after copying inputs B into the same buffers, and compare with an eager
