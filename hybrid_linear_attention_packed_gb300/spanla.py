@@ -204,8 +204,8 @@ def span_la_pass(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
         raise ValueError("out must be a contiguous CUDA tensor like q")
     if (view_state_out.dtype != torch.float32 or not view_state_out.is_contiguous()
-            or view_state_out.numel() < V * H * 4096):
-        raise ValueError("view_state_out must be contiguous fp32 [V, H, 64, 64]")
+            or not view_state_out.is_cuda or view_state_out.numel() < V * H * 4096):
+        raise ValueError("view_state_out must be a contiguous fp32 CUDA tensor [V, H, 64, 64]")
     st = getattr(lib, _entry)(q.data_ptr(), k.data_ptr(), v.data_ptr(), dims,
                               _iptr(vcu), V, _iptr(bcu), B, _iptr(par),
                               out.data_ptr(), view_state_out.data_ptr(), _stream_handle(stream))
