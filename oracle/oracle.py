@@ -49,25 +49,30 @@ def build_oracle(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def bind_library(path: str):
+    """Load a build of ``spanla_oracle.c`` from ``path`` and declare its entry
+    points (the tests also bind copies built with planted mistakes)."""
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    ip = ctypes.POINTER(ctypes.c_int32)
+    lib.oracle_pass.argtypes = [dp, dp, dp, ctypes.c_int64, ctypes.c_int64,
+                                ctypes.c_int64, ip, ctypes.c_int32, ip,
+                                ctypes.c_int32, ip, dp, dp, ctypes.c_int]
+    lib.oracle_pass.restype = ctypes.c_int
+    lib.oracle_branches_from_state.argtypes = [
+        dp, ctypes.c_int32, dp, dp, dp, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int64, ip, ctypes.c_int32, ip, dp, ctypes.c_int]
+    lib.oracle_branches_from_state.restype = ctypes.c_int
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            path = build_oracle()
-            lib = ctypes.CDLL(path)
-            dp = ctypes.POINTER(ctypes.c_double)
-            ip = ctypes.POINTER(ctypes.c_int32)
-            lib.oracle_pass.argtypes = [dp, dp, dp, ctypes.c_int64, ctypes.c_int64,
-                                        ctypes.c_int64, ip, ctypes.c_int32, ip,
-                                        ctypes.c_int32, ip, dp, dp, ctypes.c_int]
-            lib.oracle_pass.restype = ctypes.c_int
-            lib.oracle_branches_from_state.argtypes = [
-                dp, ctypes.c_int32, dp, dp, dp, ctypes.c_int64, ctypes.c_int64,
-                ctypes.c_int64, ip, ctypes.c_int32, ip, dp, ctypes.c_int]
-            lib.oracle_branches_from_state.restype = ctypes.c_int
-            lib.oracle_max_threads.argtypes = []
-            lib.oracle_max_threads.restype = ctypes.c_int
-            _lib = lib
+            _lib = bind_library(build_oracle())
     return _lib
 
 
