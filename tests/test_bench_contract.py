@@ -33,3 +33,19 @@ def test_reference_arm_prints_one_contract_line(layer):
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["workload"].startswith("tiny")
+
+
+def test_error_measure_of_the_cpu_baseline_leg():
+    """The leg that compares the benchmarked output with the oracle uses the
+    parity tests' measure over the rows of segments only."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    from hybrid_linear_attention_packed_gb300 import workloads
+    w = workloads.make_pass([5, 3], [2], [1], H=1, dtype="f32", seed=0, lead_rows=1, mid_rows=2,
+                            tail_rows=1)
+    m = bench.segment_mask(w)
+    assert m.tolist() == [False] + [True] * 8 + [False, False] + [True] * 2 + [False]
+    ref = np.array([[1.0, -4.0], [2.0, 0.5]])
+    assert bench.max_rel_err(ref + np.array([[0.0, 0.4], [0.0, 0.0]]), ref) == pytest.approx(0.1)
+    assert bench.max_rel_err(np.zeros((0, 2)), np.zeros((0, 2))) == 0.0
