@@ -8,8 +8,10 @@ RTXs and Mac Minis", section "The Workload"), so the reassembled outputs and
 view states equal the whole pass's bit for bit.  The step time reduction of a
 weak-scaling job (``sharding.max_over_ranks``) is checked on the same group.
 """
+import datetime
 import os
 import socket
+import time
 
 import numpy as np
 import pytest
@@ -90,3 +92,32 @@ def test_two_ranks_reassemble_the_whole_pass(tmp_path):
     assert sorted(seen) == list(range(w.V))
     assert np.array_equal(got, ref)
     assert np.array_equal(got_state, ref_state)
+
+
+def _leaver_main(rank, port, result_path):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=WORLD, timeout=datetime.timedelta(seconds=5))
+    if rank == 1:
+        return      # leaves between steps: never joins the next collective
+    t0 = time.monotonic()
+    try:
+        sharding.max_over_ranks(1.0, dist)
+        outcome = "completed"
+    except RuntimeError as exc:     # the peer's connection closed, or the timeout ran out
+        outcome = "error: %s" % str(exc).splitlines()[0]
+    with open(result_path, "w") as f:
+        f.write("%s\n%.3f\n" % (outcome, time.monotonic() - t0))
+    dist.destroy_process_group()
+
+
+def test_a_rank_that_leaves_ends_the_others_step_with_an_error(tmp_path):
+    """Failure detection on the host: a rank that leaves between steps makes
+    the next step-time reduction of the others fail within the process
+    group's short timeout instead of waiting for ever."""
+    path = str(tmp_path / "leaver.txt")
+    mp.start_processes(_leaver_main, args=(_free_port(), path), nprocs=WORLD, start_method="spawn")
+    outcome, elapsed = open(path).read().splitlines()[:2]
+    print(outcome, elapsed)
+    assert outcome.startswith("error"), outcome
+    assert float(elapsed) < 30.0
