@@ -155,13 +155,14 @@ def gpu_id_for_smi(torch, dev_index: int) -> str:
 # ---------------------------------------------------------------- algorithmic bytes
 def algorithmic_bytes(plan: dict, H: int, esize: int, T: int) -> dict:
     """Bytes each kernel must move at least once per launch, from the library's
-    own plan: operand rows read, states written/read, outputs written."""
+    own plan (counts summed over heads): operand rows read, states
+    written/read, outputs written."""
     row = 64 * esize
-    state_k = plan["state_rows"] * H * 2 * row + plan["state_slots"] * H * STATE_BYTES
-    out_k = plan["tile_rows"] * H * 4 * row + plan["start_state_reads"] * H * STATE_BYTES
+    state_k = plan["state_rows"] * 2 * row + plan["state_slots"] * STATE_BYTES
+    out_k = plan["tile_rows"] * 4 * row + plan["start_state_reads"] * STATE_BYTES
     return {
         "chunk_state": state_k, "span_state": state_k,
-        "segmented_scan": (2 * plan["state_slots"] + plan["final_states"]) * H * STATE_BYTES,
+        "segmented_scan": (2 * plan["state_slots"] + plan["final_states"]) * STATE_BYTES,
         "tile_output": out_k, "span_output": out_k,
         "split_f32": T * H * 64 * (3 * 4 + 6 * 2),
     }
@@ -686,18 +687,20 @@ def main():
     spanla.span_la_check()
 
     # Roofline of the dominant kernel, from live event timings.
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     if shards_mode:
         plan = None
         for cu, par in zip(shard_cu, shard_par):
-            st_ = spanla.plan_stats([], cu, par, w.H, w.dtype, num_parents=1, from_state=True)
+            st_ = spanla.plan_stats([], cu, par, w.H, w.dtype, num_parents=1, from_state=True,
+                                    num_sms=nsm)
             plan = st_ if plan is None else {key: plan[key] + st_[key] for key in plan}
     elif args.per_request:
         plan = None
         for vcu_r, bcu_r, par_r, _ in req_calls:
-            st_ = spanla.plan_stats(vcu_r, bcu_r, par_r, w.H, w.dtype)
+            st_ = spanla.plan_stats(vcu_r, bcu_r, par_r, w.H, w.dtype, num_sms=nsm)
             plan = st_ if plan is None else {key: plan[key] + st_[key] for key in plan}
     else:
-        plan = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H, w.dtype)
+        plan = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H, w.dtype, num_sms=nsm)
     alg = algorithmic_bytes(plan, w.H, esize, w.T)
     peaks = {}
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")

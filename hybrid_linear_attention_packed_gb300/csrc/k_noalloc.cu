@@ -17,8 +17,10 @@ namespace spanla {
 namespace {
 
 // Largest workspace a no-allocation pass may use: descriptors plus one fp32
-// 64x64 state per span and head (16 KiB each), i.e. about a thousand
-// span-heads -- a 7,400-token or four-request 16-head pass fits.
+// 64x64 state per piece (16 KiB each), i.e. about a thousand pieces.  A
+// piece is the part of one view-head (or long-branch-head) inside one CTA's
+// run of the output kernel, so a pass needs at most about (views + SMs) x
+// heads of them: a 7,400-token 16-head pass needs about 170.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 // Error word of the no-allocation path's kernels (bounded waits that ran out).
 static __device__ unsigned g_noalloc_err;
@@ -36,7 +38,9 @@ Slot g_slots[64];
 
 // Device addresses of the scratch array and error word on the current device.
 // The first call on a device looks them up with cudaGetSymbolAddress (with
-// that device current) and caches them; later calls only read the cache.
+// that device current) and caches them; later calls only read the cache, so
+// the addresses stay valid only while the device's primary context lives (a
+// cudaDeviceReset invalidates them).
 cudaError_t noalloc_scratch(uint8_t** scratch, unsigned** err) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -57,6 +61,17 @@ cudaError_t noalloc_scratch(uint8_t** scratch, unsigned** err) {
   }
   *scratch = s.scratch;
   *err = s.err;
+  return cudaSuccess;
+}
+
+cudaError_t noalloc_error_word(unsigned** err) {
+  *err = nullptr;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_slots[dev].ready) *err = g_slots[dev].err;
   return cudaSuccess;
 }
 

@@ -1,15 +1,14 @@
 // Span-state kernel (bf16 inputs): the local state sum_t k_t v_t^T of every
-// span, i.e. of a run of consecutive 64-row chunks of one segment.
+// piece, i.e. of a run of consecutive rows of one segment-head.
 //
 // "Serving 0.88M TPS from Two RTXs and Mac Minis", section "Kernels": the
 // per-chunk 64x64 products K_c^T V_c of the chunked form, here summed over the
-// chunks of a span inside the tensor cores' fp32 accumulator, so that the scan
-// that follows (one scan for every view of the pass) moves one state per span
-// instead of one per chunk.
+// chunks of a piece inside the tensor cores' fp32 accumulator, so that the
+// scan that follows (one scan for every view of the pass) moves one state per
+// piece instead of one per chunk.
 //
-// Persistent CTAs (one per SM) walk the (span, head) units u = blockIdx.x,
-// blockIdx.x + gridDim.x, ... (heads fastest, so CTAs reading the same rows
-// run together).  4 warps:
+// Persistent CTAs (one per SM) walk their own list of pieces (the host deals
+// the pieces to CTAs longest first onto the least-loaded CTA).  4 warps:
 //   warp 2     producer: K and V of one head, 256 rows (four chunks) at a
 //              time ([256 rows][64 d] bf16, 128-byte swizzle; 32 KB boxes
 //              stream faster than 16 KB ones), into a three-stage ring,
@@ -33,7 +32,7 @@ constexpr int kRows = 4 * kChunk;                        // rows per stage
 constexpr uint32_t kTileBytes = kRows * 128;             // 128 rows x 128 B (one head)
 constexpr uint32_t kStageBytes = 2 * kTileBytes;         // K, V
 constexpr uint32_t kTmemCols = 128;                      // two 64-column accumulators
-constexpr int kDescSlots = 128;                          // span records staged in shared memory
+constexpr int kDescSlots = 128;                          // piece records staged in shared memory
 
 struct SpanSmem {
   static constexpr uint32_t kStage0 = 0;
@@ -55,7 +54,8 @@ __device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity, unsi
 
 __global__ void __launch_bounds__(kThreads, 1)
 span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const SpanDesc* __restrict__ spans, int n_spans, int H, float* __restrict__ ws,
+                  const SpanDesc* __restrict__ spans, const int32_t* __restrict__ span_begin,
+                  float* __restrict__ ws, const uint8_t* __restrict__ prefetch, uint32_t prefetch_bytes,
                   unsigned* __restrict__ err) {
   using L = SpanSmem;
   extern __shared__ uint8_t smem_raw[];
@@ -89,15 +89,21 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   griddep_wait();   // descriptors come from a copy earlier in the stream
   // The scan may be scheduled now: it waits for this grid's completion itself.
   griddep_launch_dependents();
-  const int64_t n_units = static_cast<int64_t>(n_spans) * H;
-  // Stage the span records of this CTA's first units in shared memory, all
-  // loads in flight at once, so the producer does not wait on one per unit.
-  SpanDesc* sdesc = reinterpret_cast<SpanDesc*>(smem + L::kDesc);
-  for (int j = tid; j < kDescSlots; j += kThreads) {
-    const int64_t u = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
-    if (u < n_units) sdesc[j] = spans[u / H];
+  // The pass's descriptor block (the later kernels' schedules) into L2, a
+  // slice per CTA, so that their first reads do not wait on DRAM.
+  if (tid == 0 && prefetch_bytes > 0) {
+    const uint32_t chunk = ((prefetch_bytes + gridDim.x - 1) / gridDim.x + 15u) & ~15u;
+    const uint32_t lo = blockIdx.x * chunk;
+    if (lo < prefetch_bytes) bulk_prefetch_l2(prefetch + lo, min(chunk, prefetch_bytes - lo));
   }
-  auto span_of = [&](int64_t u, int j) { return j < kDescSlots ? sdesc[j] : spans[u / H]; };
+  const int u_begin = span_begin[blockIdx.x];
+  const int n_units = span_begin[blockIdx.x + 1] - u_begin;
+  const SpanDesc* list = spans + u_begin;
+  // Stage this CTA's first piece records in shared memory, all loads in
+  // flight at once, so the producer does not wait on one per piece.
+  SpanDesc* sdesc = reinterpret_cast<SpanDesc*>(smem + L::kDesc);
+  for (int j = tid; j < kDescSlots && j < n_units; j += kThreads) sdesc[j] = list[j];
+  auto span_of = [&](int j) { return j < kDescSlots ? sdesc[j] : list[j]; };
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -108,10 +114,9 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (lane == 0) {
       int c = 0;   // running chunk count (ring position)
       bool ok = true;
-      int j = 0;   // unit count of this CTA
-      for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++j) {
-        const SpanDesc sd = span_of(u, j);
-        const int h = static_cast<int>(u % H);
+      for (int j = 0; j < n_units && ok; ++j) {
+        const SpanDesc sd = span_of(j);
+        const int h = sd.head;
         const int n_chunks = (sd.len + kRows - 1) / kRows;
         for (int q = 0; q < n_chunks; ++q, ++c) {
           const int s = c % kStages;
@@ -132,10 +137,10 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   } else if (warp == 3) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(128, 64, /*a MN*/ 1, /*b MN*/ 1);
-    int c = 0, k = 0;   // running chunk count, running unit count (of this CTA)
+    int c = 0;   // running chunk count
     bool ok = true;
-    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++k) {
-      const SpanDesc sd = span_of(u, k);
+    for (int k = 0; k < n_units && ok; ++k) {
+      const SpanDesc sd = span_of(k);
       const int n_chunks = (sd.len + kRows - 1) / kRows;
       const int b = k & 1;
       if (k >= 2) ok = wait_or_flag(bar(L::kAccFree + b), ((k - 2) >> 1) & 1, err, kErrTimeoutMma);
@@ -172,9 +177,9 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   } else {
     // ------------------------------------------------------------ epilogue (warps 0, 1)
     const int d = warp * 32 + lane;   // state row = TMEM lane (0..63)
-    int k = 0;
-    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
+    for (int k = 0; k < n_units; ++k) {
       const int b = k & 1;
+      const int slot = span_of(k).slot;
       if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kAccReady + b), (k >> 1) & 1, err, kErrTimeoutMma)))
         break;
       tc_fence_after_sync();
@@ -185,7 +190,7 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(L::kAccFree + b));
-      float4* dst = reinterpret_cast<float4*>(ws + (u * kHeadDim + d) * kHeadDim);
+      float4* dst = reinterpret_cast<float4*>(ws + (static_cast<int64_t>(slot) * kHeadDim + d) * kHeadDim);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
@@ -206,14 +211,17 @@ span_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 }  // namespace
 
 cudaError_t launch_span_state(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                              const SpanDesc* spans, int n_spans, int H, float* ws,
-                              int grid, unsigned* err, cudaStream_t stream) {
-  if (n_spans <= 0 || grid <= 0) return cudaSuccess;
+                              const SpanDesc* spans, const int32_t* span_begin, int grid,
+                              float* ws, const void* prefetch, size_t prefetch_bytes, unsigned* err,
+                              cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
   const uint32_t bytes = SpanSmem::kRequest;
   static std::atomic<uint64_t> done{0};
   cudaError_t e = set_smem_limit_once(span_state_kernel, bytes, done);
   if (e != cudaSuccess) return e;
-  span_state_kernel<<<grid, kThreads, bytes, stream>>>(tm_k[0], tm_v[0], spans, n_spans, H, ws, err);
+  span_state_kernel<<<grid, kThreads, bytes, stream>>>(
+      tm_k[0], tm_v[0], spans, span_begin, ws, static_cast<const uint8_t*>(prefetch),
+      static_cast<uint32_t>(prefetch_bytes & ~static_cast<size_t>(15)), err);
   return cudaGetLastError();
 }
 

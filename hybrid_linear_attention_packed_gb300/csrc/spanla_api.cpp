@@ -253,28 +253,41 @@ span_la_status check_parents(const int32_t* parent, int32_t B, int32_t n_parents
 }
 
 // ------------------------------------------------------------------ descriptor build
-// Two plans share one builder.
-//  * span mode (bf16 inputs): every view and every branch longer than one
-//    tile is cut into spans of up to G 128-row tiles.  span_state sums K^T V
-//    per span, the scan turns span states into exclusive prefixes, and
-//    span_output walks each span's tiles carrying the state.  Short branches
-//    are packed (adjacent, contiguous, same parent) into single-tile items.
+// Two plans.
+//  * span mode (bf16 inputs): every tile of every segment-head is laid out
+//    request by request -- a view's tiles, then the tiles of the branches
+//    whose parent it is, head by head -- and the sequence is cut into one
+//    contiguous run per CTA of the output kernel, every run of the same
+//    length (+-1 tile).  A piece (the part of one view-head or long-branch-head
+//    inside one run) owns a state slot: span_state sums K^T V per piece, the
+//    scan turns the slots of each segment-head into exclusive prefixes, and
+//    span_output walks each run carrying the state across its pieces' tiles.
+//    Short branches are packed (adjacent, contiguous, same parent) into
+//    single tiles whose start state is the parent's final state.
 //  * chunk mode (fp32 inputs, split in bf16 parts): one state per 64-row
 //    chunk (chunk_state), the scan over chunks, and one CTA per 128-row tile
 //    (tile_output) starting from its first chunk's prefix.
 struct Plan {
   bool span_mode = true;
-  int G = 1;   // tiles per span (span mode)
-  std::vector<ChunkDesc> chunks;     // chunk mode: 64-row chunks
-  std::vector<SpanDesc> spans;       // span mode
-  std::vector<ScanDesc> scan;        // over chunk or span state slots
-  std::vector<TileDesc> tiles;       // chunk mode: self-contained tiles
-  std::vector<ItemDesc> items;       // span mode
-  std::vector<OutTileDesc> otiles;   // span mode
+  std::vector<ScanDesc> scan;
   std::vector<uint8_t> bounds;
+  // chunk mode
+  std::vector<ChunkDesc> chunks;
+  std::vector<TileDesc> tiles;
+  // span mode
+  std::vector<SpanDesc> spans;       // pieces, in span_state's per-CTA order
+  std::vector<int32_t> span_begin;   // span_state CTA c runs spans[span_begin[c] .. span_begin[c+1])
+  std::vector<WorkTile> work;        // span_output's runs, one after the other
+  std::vector<int32_t> cta_begin;    // span_output CTA c runs work[cta_begin[c] .. cta_begin[c+1])
+  int run_tiles = 0;                 // longest run (tiles)
+  int64_t n_pieces = 0;              // output pieces (packed tiles included), all heads
 
-  int state_slots() const { return static_cast<int>(span_mode ? spans.size() : chunks.size()); }
-  size_t n_out_tiles() const { return span_mode ? otiles.size() : tiles.size(); }
+  int state_slots(int H) const {
+    return span_mode ? static_cast<int>(spans.size()) : static_cast<int>(chunks.size()) * H;
+  }
+  int state_grid() const { return span_begin.empty() ? 0 : static_cast<int>(span_begin.size()) - 1; }
+  int out_grid() const { return cta_begin.empty() ? 0 : static_cast<int>(cta_begin.size()) - 1; }
+  size_t n_out_tiles() const { return span_mode ? work.size() : tiles.size(); }
 
   void push_bound(int32_t& bound0, int32_t& nbound) {
     bound0 = static_cast<int32_t>(bounds.size());
@@ -282,176 +295,300 @@ struct Plan {
     bounds.push_back(0);
   }
 
-  // A segment (view: final_idx >= 0; long branch: stateA = parent).
-  void add_segment(int64_t start, int64_t len, int final_idx, int stateA) {
-    if (span_mode) {
-      const int64_t span_rows = static_cast<int64_t>(G) * kTileRows;
-      const int span0 = static_cast<int>(spans.size());
-      const int n_sp = static_cast<int>((len + span_rows - 1) / span_rows);
-      for (int sp = 0; sp < n_sp; ++sp) {
-        const int64_t r0 = start + sp * span_rows;
-        const int64_t r1 = std::min<int64_t>(start + len, r0 + span_rows);
-        spans.push_back({static_cast<int32_t>(r0), static_cast<int32_t>(r1 - r0)});
-        ItemDesc it{};
-        it.tile0 = static_cast<int32_t>(otiles.size());
-        it.ntiles = static_cast<int32_t>((r1 - r0 + kTileRows - 1) / kTileRows);
-        it.stateA = stateA;
-        it.stateB = sp == 0 ? -1 : span0 + sp;
-        items.push_back(it);
-        for (int64_t r = r0; r < r1; r += kTileRows) {
-          OutTileDesc t{};
-          t.row0 = static_cast<int32_t>(r);
-          t.nrows = static_cast<int32_t>(std::min<int64_t>(kTileRows, r1 - r));
-          push_bound(t.bound0, t.nbound);
-          otiles.push_back(t);
-        }
-      }
-      scan.push_back({span0, n_sp, final_idx, 0});
-    } else {
-      const int chunk0 = static_cast<int>(chunks.size());
-      const int n = static_cast<int>((len + kChunk - 1) / kChunk);
-      for (int c = 0; c < n; ++c) {
-        const int64_t r = start + static_cast<int64_t>(c) * kChunk;
-        chunks.push_back({static_cast<int32_t>(r), static_cast<int32_t>(std::min<int64_t>(kChunk, start + len - r))});
-      }
-      scan.push_back({chunk0, n, final_idx, 0});
-      for (int64_t r = 0; r < len; r += kTileRows) {
-        const int j = static_cast<int>(r / kTileRows);
-        TileDesc t{};
-        t.row0 = static_cast<int32_t>(start + r);
-        t.nrows = static_cast<int32_t>(std::min<int64_t>(kTileRows, len - r));
-        t.stateA = stateA;
-        t.stateB = j == 0 ? -1 : chunk0 + 2 * j;
-        push_bound(t.bound0, t.nbound);
-        tiles.push_back(t);
-      }
+  // chunk mode: a segment (view: final_idx >= 0; long branch: stateA = parent).
+  void add_chunk_segment(int64_t start, int64_t len, int final_idx, int stateA) {
+    const int chunk0 = static_cast<int>(chunks.size());
+    const int n = static_cast<int>((len + kChunk - 1) / kChunk);
+    for (int c = 0; c < n; ++c) {
+      const int64_t r = start + static_cast<int64_t>(c) * kChunk;
+      chunks.push_back({static_cast<int32_t>(r), static_cast<int32_t>(std::min<int64_t>(kChunk, start + len - r))});
     }
-  }
-
-  // Branches: short ones (<= 128 rows) are packed greedily with adjacent,
-  // contiguous branches of the same parent into one tile; longer ones are
-  // handled like views, starting from the parent's state.
-  void add_branches(const int32_t* cu, int32_t B, const int32_t* parent) {
-    int open = -1;   // short-branch tile being filled
-    for (int32_t b = 0; b < B; ++b) {
-      const int64_t start = cu[b], len = cu[b + 1] - cu[b];
-      if (len == 0) continue;
-      if (len > kTileRows) {
-        open = -1;
-        add_segment(start, len, -1, parent[b]);
-        continue;
-      }
-      if (open >= 0) {
-        int32_t& row0 = span_mode ? otiles[open].row0 : tiles[open].row0;
-        int32_t& nrows = span_mode ? otiles[open].nrows : tiles[open].nrows;
-        int32_t& nbound = span_mode ? otiles[open].nbound : tiles[open].nbound;
-        const int32_t par = span_mode ? items.back().stateA : tiles[open].stateA;
-        if (par == parent[b] && row0 + nrows == start && nrows + len <= kTileRows) {
-          bounds.push_back(static_cast<uint8_t>(nrows));
-          nbound += 1;
-          nrows += static_cast<int32_t>(len);
-          continue;
-        }
-      }
-      if (span_mode) {
-        ItemDesc it{static_cast<int32_t>(otiles.size()), 1, parent[b], -1};
-        items.push_back(it);
-        OutTileDesc t{};
-        t.row0 = static_cast<int32_t>(start);
-        t.nrows = static_cast<int32_t>(len);
-        push_bound(t.bound0, t.nbound);
-        open = static_cast<int>(otiles.size());
-        otiles.push_back(t);
-      } else {
-        TileDesc t{};
-        t.row0 = static_cast<int32_t>(start);
-        t.nrows = static_cast<int32_t>(len);
-        t.stateA = parent[b];
-        t.stateB = -1;
-        push_bound(t.bound0, t.nbound);
-        open = static_cast<int>(tiles.size());
-        tiles.push_back(t);
-      }
+    scan.push_back({chunk0, n, final_idx, -1});
+    for (int64_t r = 0; r < len; r += kTileRows) {
+      const int j = static_cast<int>(r / kTileRows);
+      TileDesc t{};
+      t.row0 = static_cast<int32_t>(start + r);
+      t.nrows = static_cast<int32_t>(std::min<int64_t>(kTileRows, len - r));
+      t.stateA = stateA;
+      t.stateB = j == 0 ? -1 : chunk0 + 2 * j;
+      push_bound(t.bound0, t.nbound);
+      tiles.push_back(t);
     }
   }
 };
 
-// Span length G: enough (item, head) work for the GPU, long spans otherwise
-// (fewer states through the scan).  Depends on the metadata and H only.
-int choose_span_tiles(const int32_t* view_cu, int32_t V, const int32_t* branch_cu, int32_t B, int H) {
-  int64_t tiles = 0;
-  for (int32_t s = 0; s < V; ++s) tiles += (view_cu[s + 1] - view_cu[s] + kTileRows - 1) / kTileRows;
+// Branches in list order as output groups: short ones (<= 128 rows) packed
+// greedily with adjacent, contiguous branches of the same parent into one
+// tile (their segment starts go to the bounds table), longer ones alone.
+struct BranchGroup {
+  int parent;
+  int64_t row0, len;
+  bool is_long;
+  int32_t bound0, nbound;
+};
+
+std::vector<BranchGroup> group_branches(const int32_t* cu, int32_t B, const int32_t* parent,
+                                        std::vector<uint8_t>* bounds) {
+  std::vector<BranchGroup> groups;
+  int open = -1;   // short-branch group being filled
   for (int32_t b = 0; b < B; ++b) {
-    const int64_t len = branch_cu[b + 1] - branch_cu[b];
-    if (len > kTileRows) tiles += (len + kTileRows - 1) / kTileRows;
+    const int64_t start = cu[b], len = cu[b + 1] - cu[b];
+    if (len == 0) continue;
+    if (len > kTileRows) {
+      open = -1;
+      groups.push_back({parent[b], start, len, true, 0, 1});
+      continue;
+    }
+    if (open >= 0) {
+      BranchGroup& g = groups[open];
+      if (g.parent == parent[b] && g.row0 + g.len == start && g.len + len <= kTileRows) {
+        bounds->push_back(static_cast<uint8_t>(g.len));
+        g.nbound += 1;
+        g.len += len;
+        continue;
+      }
+    }
+    BranchGroup g{parent[b], start, len, false, static_cast<int32_t>(bounds->size()), 1};
+    bounds->push_back(0);
+    open = static_cast<int>(groups.size());
+    groups.push_back(g);
   }
-  const int64_t g = (tiles * H + kTargetItems - 1) / kTargetItems;
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxSpanTiles, g)));
+  return groups;
+}
+
+Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu, int32_t B,
+                    const int32_t* parent, int H, int num_sms) {
+  Plan plan;
+  plan.span_mode = true;
+  const std::vector<BranchGroup> groups = group_branches(branch_cu, B, parent, &plan.bounds);
+
+  // Requests in order: view p (when p < V) followed by the branch groups
+  // whose parent is p.  Without views (branches from cached states) the
+  // parents that occur, in increasing order.
+  std::vector<int> gparents;
+  for (const BranchGroup& g : groups) gparents.push_back(g.parent);
+  std::sort(gparents.begin(), gparents.end());
+  gparents.erase(std::unique(gparents.begin(), gparents.end()), gparents.end());
+  std::vector<int> requests;
+  for (int32_t v = 0; v < V; ++v) requests.push_back(v);
+  for (int p : gparents)
+    if (p >= V) requests.push_back(p);
+  std::vector<std::vector<int>> by_parent_idx(requests.size());
+  {
+    std::vector<int> pos(requests.size());
+    for (size_t r = 0; r < requests.size(); ++r) pos[r] = static_cast<int>(r);
+    // requests are sorted (views 0..V-1, then parents >= V ascending)
+    for (size_t g = 0; g < groups.size(); ++g) {
+      const auto it = std::lower_bound(requests.begin(), requests.end(), groups[g].parent);
+      by_parent_idx[it - requests.begin()].push_back(static_cast<int>(g));
+    }
+  }
+
+  // Segment-head blocks, head-major: every head has the same sequence
+  // (request by request: the view's tiles, then its branches' tiles).
+  struct Block {
+    int kind;      // 0 view, 1 long branch group, 2 packed short branches
+    int id;        // view index or group index
+    int head;
+    int64_t row0, len;
+    int ntiles;
+  };
+  std::vector<Block> blocks;
+  int64_t W = 0;
+  for (int h = 0; h < H; ++h) {
+    for (size_t r = 0; r < requests.size(); ++r) {
+      const int p = requests[r];
+      if (p < V) {
+        const int64_t len = view_cu[p + 1] - view_cu[p];
+        const int nt = static_cast<int>((len + kTileRows - 1) / kTileRows);
+        blocks.push_back({0, p, h, view_cu[p], len, nt});
+        W += nt;
+      }
+      for (int g : by_parent_idx[r]) {
+        const BranchGroup& bg = groups[g];
+        const int nt = bg.is_long ? static_cast<int>((bg.len + kTileRows - 1) / kTileRows) : 1;
+        blocks.push_back({bg.is_long ? 1 : 2, g, h, bg.row0, bg.len, nt});
+        W += nt;
+      }
+    }
+  }
+
+  // Runs.  Every head has the same sequence of tiles, so when the SMs can
+  // be split evenly over the heads, each head's sequence is cut into R equal
+  // runs and run (p, h) goes to CTA p H + h: CTAs that start together read
+  // the same rows of every head (the same DRAM pages).  Otherwise the whole
+  // head-major sequence is cut into one run per SM.  Either way CTA c takes
+  // the global tiles [cut(c), cut(c+1)) of a list ordered by CTA.
+  const int64_t per_head = H > 0 ? W / H : 0;
+  const int sms = std::max(1, num_sms);
+  const int R = H > 0 ? sms / H : 0;
+  const bool aligned = R >= 1 && per_head > 0 && static_cast<int64_t>(R) * H * 100 >= static_cast<int64_t>(sms) * 85;
+  const int Rh = aligned ? static_cast<int>(std::min<int64_t>(R, per_head)) : 0;
+  const int grid = aligned ? Rh * H : static_cast<int>(std::min<int64_t>(W, sms));
+  // start of CTA c's run in the head-major sequence, and its length
+  auto run_start = [&](int c) -> int64_t {
+    if (!aligned) return grid > 0 ? static_cast<int64_t>(c) * W / grid : 0;
+    const int p = c / H, h = c % H;
+    return static_cast<int64_t>(h) * per_head + static_cast<int64_t>(p) * per_head / Rh;
+  };
+  auto run_len = [&](int c) -> int64_t {
+    if (!aligned) return run_start(c + 1) - run_start(c);
+    const int p = c / H;
+    return static_cast<int64_t>(p + 1) * per_head / Rh - static_cast<int64_t>(p) * per_head / Rh;
+  };
+  // CTA owning head-major tile g, and the end of that CTA's run
+  auto cta_of = [&](int64_t g) -> int {
+    if (!aligned) {
+      int c = static_cast<int>(g * grid / W);
+      while (c + 1 < grid && run_start(c + 1) <= g) ++c;
+      while (c > 0 && run_start(c) > g) --c;
+      return c;
+    }
+    const int h = static_cast<int>(g / per_head);
+    const int64_t j = g - static_cast<int64_t>(h) * per_head;
+    int p = static_cast<int>(j * Rh / per_head);
+    while (p + 1 < Rh && static_cast<int64_t>(p + 1) * per_head / Rh <= j) ++p;
+    while (p > 0 && static_cast<int64_t>(p) * per_head / Rh > j) --p;
+    return p * H + h;
+  };
+  plan.cta_begin.assign(grid + 1, 0);
+  for (int c = 0; c < grid; ++c) {
+    plan.cta_begin[c + 1] = plan.cta_begin[c] + static_cast<int32_t>(run_len(c));
+    plan.run_tiles = std::max<int>(plan.run_tiles, static_cast<int>(run_len(c)));
+  }
+  plan.work.assign(W, WorkTile{});
+
+  std::vector<SpanDesc> pieces;   // in creation order
+  std::vector<int> piece_cta;      // output CTA of each piece
+  int64_t g0 = 0;
+  for (const Block& bk : blocks) {
+    if (bk.kind == 0 && bk.ntiles == 0) {   // empty view: zero final state
+      plan.scan.push_back({0, 0, bk.id, bk.head});
+      continue;
+    }
+    // The block's pieces: [g0, g0 + ntiles) split at the run boundaries.
+    std::vector<std::pair<int, int>> pr;   // local tile ranges [j0, j1)
+    std::vector<int> pcta;
+    {
+      int64_t a = g0;
+      const int64_t end = g0 + bk.ntiles;
+      while (a < end) {
+        const int c = cta_of(a);
+        const int64_t b = std::min<int64_t>(end, run_start(c) + run_len(c));
+        pr.push_back({static_cast<int>(a - g0), static_cast<int>(b - g0)});
+        pcta.push_back(c);
+        a = b;
+      }
+    }
+    const bool slots = bk.kind == 0 || (bk.kind == 1 && pr.size() >= 2);
+    const int slot0 = static_cast<int>(pieces.size());
+    if (slots) plan.scan.push_back({slot0, static_cast<int32_t>(pr.size()), bk.kind == 0 ? bk.id : -1, bk.head});
+    for (size_t k = 0; k < pr.size(); ++k) {
+      const int j0 = pr[k].first, j1 = pr[k].second;
+      const int c = pcta[k];
+      const int64_t r0 = bk.row0 + static_cast<int64_t>(j0) * kTileRows;
+      const int64_t r1 = std::min<int64_t>(bk.row0 + bk.len, bk.row0 + static_cast<int64_t>(j1) * kTileRows);
+      if (slots) {
+        pieces.push_back({static_cast<int32_t>(r0), static_cast<int32_t>(r1 - r0), bk.head,
+                          static_cast<int32_t>(pieces.size())});
+        piece_cta.push_back(c);
+      }
+      const int32_t sA = bk.kind == 0 ? -1 : groups[bk.id].parent;
+      const int32_t sB = (slots && k > 0) ? slot0 + static_cast<int32_t>(k) : -1;
+      ++plan.n_pieces;
+      for (int j = j0; j < j1; ++j) {
+        WorkTile w{};
+        w.row0 = static_cast<int32_t>(bk.row0 + static_cast<int64_t>(j) * kTileRows);
+        w.nrows = static_cast<int32_t>(std::min<int64_t>(kTileRows, bk.len - static_cast<int64_t>(j) * kTileRows));
+        w.head = bk.head;
+        w.flags = (j == j0 ? kTileFirst : 0) | (j + 1 == j1 ? kTileLast : 0) |
+                  ((sA >= 0 || sB >= 0) ? kTileHasInit : 0);
+        w.stateA = sA;
+        w.stateB = sB;
+        if (bk.kind == 2) {
+          const BranchGroup& bg = groups[bk.id];
+          w.bound0 = bg.bound0;
+          w.nbound = bg.nbound;
+          for (int q = 0; q < kInlineBounds && q < bg.nbound; ++q) w.inl[q] = plan.bounds[bg.bound0 + q];
+        } else {
+          w.bound0 = 0;
+          w.nbound = 1;
+        }
+        // position in CTA c's list: its run is contiguous in the head-major order
+        plan.work[plan.cta_begin[c] + (g0 + j - run_start(c))] = w;
+      }
+    }
+    g0 += bk.ntiles;
+  }
+
+  // span_state: with no more pieces than SMs, piece k goes to the CTA that
+  // runs its output (rows read together stay together); otherwise the
+  // pieces are dealt longest first onto the least-loaded CTA.
+  const int64_t n_sp = static_cast<int64_t>(pieces.size());
+  if (n_sp > 0) {
+    std::vector<std::vector<int64_t>> per_cta;
+    if (n_sp <= sms && grid <= sms) {
+      per_cta.resize(grid);
+      for (int64_t u = 0; u < n_sp; ++u) per_cta[piece_cta[u]].push_back(u);
+      // drop CTAs without pieces
+      per_cta.erase(std::remove_if(per_cta.begin(), per_cta.end(),
+                                   [](const std::vector<int64_t>& v) { return v.empty(); }),
+                    per_cta.end());
+    } else {
+      const int sgrid = static_cast<int>(std::min<int64_t>(n_sp, sms));
+      std::vector<int64_t> order(n_sp);
+      for (int64_t u = 0; u < n_sp; ++u) order[u] = u;
+      std::stable_sort(order.begin(), order.end(),
+                       [&](int64_t a, int64_t b) { return pieces[a].len > pieces[b].len; });
+      using Slot = std::pair<int64_t, int>;   // (rows assigned, cta)
+      std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+      for (int c = 0; c < sgrid; ++c) heap.push({0, c});
+      per_cta.resize(sgrid);
+      for (int64_t u : order) {
+        Slot sl = heap.top();
+        heap.pop();
+        per_cta[sl.second].push_back(u);
+        sl.first += pieces[u].len;
+        heap.push(sl);
+      }
+    }
+    const int sgrid = static_cast<int>(per_cta.size());
+    plan.span_begin.assign(sgrid + 1, 0);
+    for (int c = 0; c < sgrid; ++c) {
+      plan.span_begin[c] = static_cast<int32_t>(plan.spans.size());
+      for (int64_t u : per_cta[c]) plan.spans.push_back(pieces[u]);
+    }
+    plan.span_begin[sgrid] = static_cast<int32_t>(plan.spans.size());
+  }
+  return plan;
 }
 
 Plan make_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu, int32_t B,
-               const int32_t* parent, int H, bool span_mode) {
+               const int32_t* parent, int H, bool span_mode, int num_sms) {
+  if (span_mode) return make_span_plan(view_cu, V, branch_cu, B, parent, H, num_sms);
   Plan plan;
-  plan.span_mode = span_mode;
-  plan.G = span_mode ? choose_span_tiles(view_cu, V, branch_cu, B, H) : 1;
+  plan.span_mode = false;
   for (int32_t s = 0; s < V; ++s)
-    plan.add_segment(view_cu[s], view_cu[s + 1] - view_cu[s], s, -1);
-  if (B > 0) plan.add_branches(branch_cu, B, parent);
+    plan.add_chunk_segment(view_cu[s], view_cu[s + 1] - view_cu[s], s, -1);
+  const std::vector<BranchGroup> groups = group_branches(branch_cu, B, parent, &plan.bounds);
+  for (const BranchGroup& g : groups) {
+    if (g.is_long) {
+      plan.add_chunk_segment(g.row0, g.len, -1, g.parent);
+    } else {
+      TileDesc t{};
+      t.row0 = static_cast<int32_t>(g.row0);
+      t.nrows = static_cast<int32_t>(g.len);
+      t.stateA = g.parent;
+      t.stateB = -1;
+      t.bound0 = g.bound0;
+      t.nbound = g.nbound;
+      plan.tiles.push_back(t);
+    }
+  }
   return plan;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
-// Span mode: deal the (item, head) work units to `grid` persistent CTAs,
-// longest first onto the least-loaded CTA, and list each CTA's tiles in
-// order.  Returns the grid size actually used.
-int build_schedule(const Plan& plan, int H, int max_ctas, std::vector<WorkTile>* work,
-                   std::vector<int32_t>* cta_begin) {
-  const int64_t n_units = static_cast<int64_t>(plan.items.size()) * H;
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(n_units, max_ctas)));
-  std::vector<int64_t> order(n_units);
-  for (int64_t u = 0; u < n_units; ++u) order[u] = u;
-  std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
-    return plan.items[a / H].ntiles > plan.items[b / H].ntiles;
-  });
-  using Slot = std::pair<int64_t, int>;   // (tiles assigned, cta)
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int c = 0; c < grid; ++c) heap.push({0, c});
-  std::vector<std::vector<int64_t>> per_cta(grid);
-  for (int64_t u : order) {
-    Slot sl = heap.top();
-    heap.pop();
-    per_cta[sl.second].push_back(u);
-    sl.first += plan.items[u / H].ntiles;
-    heap.push(sl);
-  }
-  work->clear();
-  cta_begin->assign(grid + 1, 0);
-  for (int c = 0; c < grid; ++c) {
-    (*cta_begin)[c] = static_cast<int32_t>(work->size());
-    for (int64_t u : per_cta[c]) {
-      const ItemDesc& it = plan.items[u / H];
-      const int head = static_cast<int>(u % H);
-      for (int j = 0; j < it.ntiles; ++j) {
-        const OutTileDesc& t = plan.otiles[it.tile0 + j];
-        WorkTile w{};
-        w.row0 = t.row0;
-        w.nrows = t.nrows;
-        w.head = head;
-        w.flags = (j == 0 ? kTileFirst : 0) | (j + 1 == it.ntiles ? kTileLast : 0) |
-                  ((it.stateA >= 0 || it.stateB >= 0) ? kTileHasInit : 0);
-        w.stateA = it.stateA;
-        w.stateB = it.stateB;
-        w.bound0 = t.bound0;
-        w.nbound = t.nbound;
-        for (int q = 0; q < kInlineBounds && q < t.nbound; ++q) w.inl[q] = plan.bounds[t.bound0 + q];
-        work->push_back(w);
-      }
-    }
-  }
-  (*cta_begin)[grid] = static_cast<int32_t>(work->size());
-  return grid;
-}
 
 template <typename T>
 size_t put(std::vector<uint8_t>& host, const std::vector<T>& v) {
@@ -482,35 +619,38 @@ span_la_status encode_map(CUtensorMap* map, const void* base, int64_t T, int H, 
 // need to know about it.
 struct DescBlock {
   std::vector<uint8_t> host;
-  size_t off_scan = 0, off_bounds = 0, off_a = 0, off_b = 0, off_c = 0;
+  size_t off_scan = 0, off_bounds = 0, off_a = 0, off_b = 0, off_c = 0, off_d = 0;
   int grid = 0;            // span_output CTAs (span mode)
-  int n_scan = 0, n_spans = 0, n_chunks = 0, n_tiles = 0, state_slots = 0;
+  int state_grid = 0;      // span_state CTAs (span mode)
+  int n_scan = 0, n_chunks = 0, n_tiles = 0;
+  int64_t state_slots = 0; // 16 KiB fp32 states of the workspace (all heads)
   size_t n_out_tiles = 0;
+  size_t block_bytes = 0;  // size of the descriptor block on the device
   bool span_mode = true;
 };
 
-DescBlock make_desc(const Plan& plan, int H, int num_sms) {
+DescBlock make_desc(const Plan& plan, int H) {
   DescBlock d;
   d.span_mode = plan.span_mode;
   d.off_scan = put(d.host, plan.scan);
   d.off_bounds = put(d.host, plan.bounds);
   if (plan.span_mode) {
-    std::vector<WorkTile> work;
-    std::vector<int32_t> cta_begin;
-    if (!plan.items.empty()) d.grid = build_schedule(plan, H, num_sms, &work, &cta_begin);
     d.off_a = put(d.host, plan.spans);
-    d.off_b = put(d.host, work);
-    d.off_c = put(d.host, cta_begin);
+    d.off_d = put(d.host, plan.span_begin);
+    d.off_b = put(d.host, plan.work);
+    d.off_c = put(d.host, plan.cta_begin);
+    d.grid = plan.out_grid();
+    d.state_grid = plan.state_grid();
   } else {
     d.off_a = put(d.host, plan.chunks);
     d.off_b = put(d.host, plan.tiles);
   }
   d.n_scan = static_cast<int>(plan.scan.size());
-  d.n_spans = static_cast<int>(plan.spans.size());
   d.n_chunks = static_cast<int>(plan.chunks.size());
   d.n_tiles = static_cast<int>(plan.tiles.size());
-  d.state_slots = plan.state_slots();
+  d.state_slots = plan.state_slots(H);
   d.n_out_tiles = plan.n_out_tiles();
+  d.block_bytes = d.host.size();
   return d;
 }
 
@@ -704,6 +844,116 @@ span_la_status finish_read(CacheEntry* entry, cudaStream_t stream, span_la_statu
   return st == SPAN_LA_OK ? cuda_fail(e, "cudaEventRecord(descriptor read)") : st;
 }
 
+// The launches of one pass over descriptors already on the device (`block`):
+// for fp32 inputs the split into bf16 parts (into `parts`, six [T][H][64]
+// arrays), then state kernel -> scan -> output kernel, chained with
+// programmatic dependent launch.  `states` holds desc.state_slots fp32
+// states.  With `mc` (the caller holds g_cache_mu) the TMA descriptors of
+// bf16 operands are reused from the last call on the same arrays.
+span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t* parts, float* states,
+                            const void* q, const void* k, const void* v, const span_la_dims& dims,
+                            const float* stateA, float* final_out, void* out, unsigned* err,
+                            cudaStream_t stream, MapCache* mc, int device) {
+  const int H = dims.num_heads;
+  const int64_t T = dims.total_rows;
+  const bool split = dims.dtype == SPAN_LA_F32;
+  cudaError_t e = cudaSuccess;
+  span_la_status st = SPAN_LA_OK;
+
+  // bf16 operand arrays the kernels read through TMA: the inputs themselves,
+  // or, for fp32 inputs, their bf16 high / low parts made by the split kernel.
+  const size_t part_bytes = static_cast<size_t>(T) * H * kHeadDim * 2;
+  const void* ops[3][2] = {{q, nullptr}, {k, nullptr}, {v, nullptr}};
+  if (split) {
+    for (int t = 0; t < 3; ++t)
+      for (int p = 0; p < 2; ++p) ops[t][p] = parts + (2 * t + p) * part_bytes;
+    e = counted_launch(kKernelSplit, stream, [&] {
+      return launch_split_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                              static_cast<const float*>(v), T * H * kHeadDim, parts, stream);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
+  }
+  DeviceOperands tile_ops{}, chunk_ops{};
+  const bool need_maps = desc.n_out_tiles > 0 || desc.state_slots > 0;   // implies T > 0
+  const bool map_hit = mc != nullptr && !split && mc->valid && mc->device == device && mc->q == q &&
+                       mc->k == k && mc->v == v && mc->T == T && mc->H == H && mc->span_mode == desc.span_mode;
+  if (map_hit) {
+    tile_ops = mc->tile_ops;
+    chunk_ops = mc->chunk_ops;
+  }
+  for (int t = 0; t < 3 && st == SPAN_LA_OK && need_maps && !map_hit; ++t) {
+    for (int p = 0; p < (split ? 2 : 1) && st == SPAN_LA_OK; ++p) {
+      CUtensorMap* tm = t == 0 ? &tile_ops.q[p] : t == 1 ? &tile_ops.k[p] : &tile_ops.v[p];
+      CUtensorMap* cm = t == 0 ? &chunk_ops.q[p] : t == 1 ? &chunk_ops.k[p] : &chunk_ops.v[p];
+      st = encode_map(tm, ops[t][p], T, H, kTileBoxRows, 1);
+      // K and V boxes of the state kernel: 64 rows of two heads (chunk
+      // mode) or 256 rows of one head (span mode).
+      if (st == SPAN_LA_OK && t > 0)
+        st = desc.span_mode ? encode_map(cm, ops[t][p], T, H, kSpanBoxRows, 1)
+                            : encode_map(cm, ops[t][p], T, H, kChunkBoxRows, kChunkBoxHeads);
+    }
+  }
+  if (st != SPAN_LA_OK) return st;
+  if (mc != nullptr && !split && need_maps && !map_hit) {
+    mc->valid = true;
+    mc->device = device;
+    mc->q = q;
+    mc->k = k;
+    mc->v = v;
+    mc->T = T;
+    mc->H = H;
+    mc->span_mode = desc.span_mode;
+    mc->tile_ops = tile_ops;
+    mc->chunk_ops = chunk_ops;
+  }
+
+  bool kernel_before = split;   // a kernel precedes the next launch in the stream
+  if (desc.state_slots > 0) {
+    e = desc.span_mode
+            ? counted_launch(kKernelSpanState, stream, [&] {
+                return launch_span_state(chunk_ops.k, chunk_ops.v,
+                                         reinterpret_cast<const SpanDesc*>(block + desc.off_a),
+                                         reinterpret_cast<const int32_t*>(block + desc.off_d),
+                                         desc.state_grid, states, block, desc.block_bytes, err, stream);
+              })
+            : counted_launch(kKernelChunk, stream, [&] {
+                return launch_chunk_state(split, chunk_ops.k, chunk_ops.v,
+                                          reinterpret_cast<const ChunkDesc*>(block + desc.off_a),
+                                          desc.n_chunks, H, states, err, stream, kernel_before);
+              });
+    if (e != cudaSuccess) return cuda_fail(e, "chunk/span-state launch");
+    kernel_before = true;
+  }
+  if (desc.n_scan > 0) {
+    const bool pdl = kernel_before;
+    e = counted_launch(kKernelScan, stream, [&] {
+      return launch_scan(reinterpret_cast<const ScanDesc*>(block + desc.off_scan), desc.n_scan, H,
+                         desc.span_mode, states, final_out, stream, pdl);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "scan launch");
+    kernel_before = true;
+  }
+  if (desc.n_out_tiles > 0) {
+    const bool pdl = kernel_before;
+    if (desc.span_mode) {
+      e = counted_launch(kKernelSpanOutput, stream, [&] {
+        return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v,
+                                  reinterpret_cast<const WorkTile*>(block + desc.off_b),
+                                  reinterpret_cast<const int32_t*>(block + desc.off_c), desc.grid,
+                                  block + desc.off_bounds, stateA, states, out, H, err, stream, pdl);
+      });
+    } else {
+      e = counted_launch(kKernelTile, stream, [&] {
+        return launch_tile_output(split, tile_ops.q, tile_ops.k, tile_ops.v,
+                                  reinterpret_cast<const TileDesc*>(block + desc.off_b), desc.n_tiles,
+                                  block + desc.off_bounds, stateA, states, out, H, err, stream, pdl);
+      });
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "output launch");
+  }
+  return SPAN_LA_OK;
+}
+
 // Common tail of both entry points: descriptors (cached, or uploaded into the
 // call's workspace while the stream is being captured), workspace, launches.
 template <typename BuildPlan>
@@ -726,11 +976,11 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
   span_la_status st = SPAN_LA_OK;
   if (use_cache) {
     cache_lock.lock();
-    st = cached_block(key, device, stream, [&] { return make_desc(build_plan(), H, dev->num_sms); }, &desc,
+    st = cached_block(key, device, stream, [&] { return make_desc(build_plan(), H); }, &desc,
                       &block, &entry);
     if (st != SPAN_LA_OK) return st;
   } else {
-    local = make_desc(build_plan(), H, dev->num_sms);
+    local = make_desc(build_plan(), H);
     desc = &local;
   }
   if (desc->n_out_tiles == 0 && desc->n_scan == 0) return SPAN_LA_OK;
@@ -739,7 +989,7 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
   // and, for fp32 inputs, the six bf16 part arrays.
   const size_t desc_bytes = use_cache ? 0 : align256(desc->host.size());
   const size_t off_states = desc_bytes;
-  const size_t state_bytes = static_cast<size_t>(desc->state_slots) * H * kStateFloats * sizeof(float);
+  const size_t state_bytes = static_cast<size_t>(desc->state_slots) * kStateFloats * sizeof(float);
   const size_t off_parts = align256(off_states + state_bytes);
   const size_t part_bytes = static_cast<size_t>(T) * H * kHeadDim * 2;
   const size_t total = std::max<size_t>(off_parts + (split ? 6 * part_bytes : 0), 256);
@@ -748,110 +998,15 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
   if (injected_alloc_failure()) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): injected failure", total);
   e = cudaMallocAsync(reinterpret_cast<void**>(&ws), total, stream);
   if (e != cudaSuccess) return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(%zu): %s", total, cudaGetErrorString(e));
-  do {
-    if (!use_cache) {
-      e = upload_descriptors(ws, std::move(local.host), true, stream);
-      if (e != cudaSuccess) { st = cuda_fail(e, "cudaMemcpyAsync(descriptors)"); break; }
-      block = ws;
-    }
-
-    // bf16 operand arrays the kernels read through TMA: the inputs themselves,
-    // or, for fp32 inputs, their bf16 high / low parts made by the split kernel.
-    const void* parts[3][2] = {{q, nullptr}, {k, nullptr}, {v, nullptr}};
-    if (split) {
-      for (int t = 0; t < 3; ++t)
-        for (int p = 0; p < 2; ++p) parts[t][p] = ws + off_parts + (2 * t + p) * part_bytes;
-      e = counted_launch(kKernelSplit, stream, [&] {
-        return launch_split_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                                static_cast<const float*>(v), T * H * kHeadDim, ws + off_parts, stream);
-      });
-      if (e != cudaSuccess) { st = cuda_fail(e, "split kernel launch"); break; }
-    }
-    DeviceOperands tile_ops{}, chunk_ops{};
-    const bool need_maps = desc->n_out_tiles > 0 || desc->state_slots > 0;   // implies T > 0
-    // bf16 inputs under the cache lock: reuse the last call's TMA descriptors
-    // when the operand arrays and their shape are the same.
-    MapCache& mc = g_maps[device & (kMaxDevices - 1)];
-    const bool map_hit = use_cache && !split && mc.valid && mc.device == device && mc.q == q && mc.k == k &&
-                         mc.v == v && mc.T == T && mc.H == H && mc.span_mode == desc->span_mode;
-    if (map_hit) {
-      tile_ops = mc.tile_ops;
-      chunk_ops = mc.chunk_ops;
-    }
-    for (int t = 0; t < 3 && st == SPAN_LA_OK && need_maps && !map_hit; ++t) {
-      for (int p = 0; p < (split ? 2 : 1) && st == SPAN_LA_OK; ++p) {
-        CUtensorMap* tm = t == 0 ? &tile_ops.q[p] : t == 1 ? &tile_ops.k[p] : &tile_ops.v[p];
-        CUtensorMap* cm = t == 0 ? &chunk_ops.q[p] : t == 1 ? &chunk_ops.k[p] : &chunk_ops.v[p];
-        st = encode_map(tm, parts[t][p], T, H, kTileBoxRows, 1);
-        // K and V boxes of the state kernel: 64 rows of two heads (chunk
-        // mode) or of one head (span mode).
-        if (st == SPAN_LA_OK && t > 0)
-          st = desc->span_mode ? encode_map(cm, parts[t][p], T, H, kSpanBoxRows, 1)
-                               : encode_map(cm, parts[t][p], T, H, kChunkBoxRows, kChunkBoxHeads);
-      }
-    }
-    if (st != SPAN_LA_OK) break;
-    if (use_cache && !split && need_maps && !map_hit) {
-      mc.valid = true;
-      mc.device = device;
-      mc.q = q;
-      mc.k = k;
-      mc.v = v;
-      mc.T = T;
-      mc.H = H;
-      mc.span_mode = desc->span_mode;
-      mc.tile_ops = tile_ops;
-      mc.chunk_ops = chunk_ops;
-    }
-
-    float* states = reinterpret_cast<float*>(ws + off_states);
-    bool kernel_before = split;   // a kernel precedes the next launch in the stream
-    if (desc->state_slots > 0) {
-      e = desc->span_mode
-              ? counted_launch(kKernelSpanState, stream, [&] {
-                  const int sgrid = static_cast<int>(std::min<int64_t>(
-                      static_cast<int64_t>(desc->n_spans) * H, dev->num_sms));
-                  return launch_span_state(chunk_ops.k, chunk_ops.v,
-                                           reinterpret_cast<const SpanDesc*>(block + desc->off_a),
-                                           desc->n_spans, H, states, sgrid, dev->err, stream);
-                })
-              : counted_launch(kKernelChunk, stream, [&] {
-                  return launch_chunk_state(split, chunk_ops.k, chunk_ops.v,
-                                            reinterpret_cast<const ChunkDesc*>(block + desc->off_a),
-                                            desc->n_chunks, H, states, dev->err, stream, kernel_before);
-                });
-      if (e != cudaSuccess) { st = cuda_fail(e, "chunk/span-state launch"); break; }
-      kernel_before = true;
-    }
-    if (desc->n_scan > 0) {
-      const bool pdl = kernel_before;
-      e = counted_launch(kKernelScan, stream, [&] {
-        return launch_scan(reinterpret_cast<const ScanDesc*>(block + desc->off_scan), desc->n_scan, H,
-                           states, final_out, stream, pdl);
-      });
-      if (e != cudaSuccess) { st = cuda_fail(e, "scan launch"); break; }
-      kernel_before = true;
-    }
-    if (desc->n_out_tiles > 0) {
-      if (desc->span_mode) {
-        const bool pdl = kernel_before;
-        e = counted_launch(kKernelSpanOutput, stream, [&] {
-          return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v,
-                                    reinterpret_cast<const WorkTile*>(block + desc->off_b),
-                                    reinterpret_cast<const int32_t*>(block + desc->off_c), desc->grid,
-                                    block + desc->off_bounds, stateA, states, out, H, dev->err, stream, pdl);
-        });
-      } else {
-        const bool pdl = kernel_before;
-        e = counted_launch(kKernelTile, stream, [&] {
-          return launch_tile_output(split, tile_ops.q, tile_ops.k, tile_ops.v,
-                                    reinterpret_cast<const TileDesc*>(block + desc->off_b), desc->n_tiles,
-                                    block + desc->off_bounds, stateA, states, out, H, dev->err, stream, pdl);
-        });
-      }
-      if (e != cudaSuccess) { st = cuda_fail(e, "output launch"); break; }
-    }
-  } while (false);
+  if (!use_cache) {
+    e = upload_descriptors(ws, std::move(local.host), true, stream);
+    if (e != cudaSuccess) st = cuda_fail(e, "cudaMemcpyAsync(descriptors)");
+    block = ws;
+  }
+  if (st == SPAN_LA_OK)
+    st = enqueue_pass(*desc, block, ws + off_parts, reinterpret_cast<float*>(ws + off_states), q, k, v, dims,
+                      stateA, final_out, out, dev->err, stream,
+                      use_cache ? &g_maps[device & (kMaxDevices - 1)] : nullptr, device);
   st = finish_read(entry, stream, st);
   cudaError_t ef = cudaFreeAsync(ws, stream);
   if (st == SPAN_LA_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync");
@@ -1030,7 +1185,7 @@ span_la_status span_la_pass(const void* q, const void* k, const void* v, span_la
                                             num_views, branch_cu_seqlens, num_branches, branch_parent);
   auto build = [&] {
     return make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches, branch_parent,
-                     dims.num_heads, dims.dtype == SPAN_LA_BF16);
+                     dims.num_heads, dims.dtype == SPAN_LA_BF16, dev->num_sms);
   };
   return run_plan(key, build, q, k, v, dims, view_state_out, view_state_out, out, stream, dev, device);
 }
@@ -1133,7 +1288,7 @@ span_la_status span_la_branches_from_state(const float* cached_state, int32_t nu
                                             branch_cu_seqlens, num_branches, branch_parent);
   auto build = [&] {
     return make_plan(nullptr, 0, branch_cu_seqlens, num_branches, branch_parent, dims.num_heads,
-                     dims.dtype == SPAN_LA_BF16);
+                     dims.dtype == SPAN_LA_BF16, dev->num_sms);
   };
   return run_plan(key, build, q, k, v, dims, cached_state, nullptr, out, stream, dev, device);
 }
@@ -1148,10 +1303,25 @@ span_la_status span_la_check(cudaStream_t stream) {
   unsigned word = 0;
   e = cudaMemcpy(&word, dev->err, sizeof(unsigned), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
-  if (word != 0) {
-    cudaMemset(dev->err, 0, sizeof(unsigned));
-    return fail(SPAN_LA_ERR_TIMEOUT, "a bounded device wait ran out (error word 0x%x)", word);
+  if (word != 0) cudaMemset(dev->err, 0, sizeof(unsigned));
+  // The no-allocation path's own error word, on a device where that path
+  // (or its self-test) has run: read and cleared without allocating.
+  unsigned na_word = 0;
+  unsigned* na_err = nullptr;
+  e = noalloc_error_word(&na_err);
+  if (e != cudaSuccess) return cuda_fail(e, "no-allocation error word");
+  if (na_err != nullptr) {
+    e = cudaMemcpy(&na_word, na_err, sizeof(unsigned), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(no-allocation error word)");
+    if (na_word != 0) {
+      const unsigned zero = 0;
+      e = cudaMemcpy(na_err, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(clear no-allocation error word)");
+    }
   }
+  if (word != 0 || na_word != 0)
+    return fail(SPAN_LA_ERR_TIMEOUT, "a bounded device wait ran out (error word 0x%x, no-allocation path 0x%x)",
+                word, na_word);
   return SPAN_LA_OK;
 }
 
@@ -1169,7 +1339,7 @@ const char* span_la_status_string(span_la_status s) {
 
 const char* span_la_last_error_detail(void) { return g_detail.c_str(); }
 
-int32_t span_la_version(void) { return 100; }
+int32_t span_la_version(void) { return 20000; }
 
 span_la_status span_la_softmax_plan_stats(const int32_t* view_cu_seqlens, int32_t num_views,
                                           const int32_t* branch_cu_seqlens, int32_t num_branches,
@@ -1200,10 +1370,11 @@ span_la_status span_la_plan_stats(const int32_t* view_cu_seqlens, int32_t num_vi
                                   const int32_t* branch_cu_seqlens, int32_t num_branches,
                                   const int32_t* branch_parent, int32_t num_parents,
                                   int32_t from_state, int32_t num_heads, int32_t dtype,
-                                  int64_t* stats) {
+                                  int32_t num_sms, int64_t* stats) {
   g_detail.clear();
   if (stats == nullptr) return fail(SPAN_LA_ERR_INVALID, "stats is NULL");
   if (num_heads < 1) return fail(SPAN_LA_ERR_INVALID, "num_heads %d < 1", num_heads);
+  if (num_sms < 1) return fail(SPAN_LA_ERR_INVALID, "num_sms %d < 1", num_sms);
   if (dtype != SPAN_LA_BF16 && dtype != SPAN_LA_F32) return fail(SPAN_LA_ERR_UNSUPPORTED, "dtype %d", dtype);
   const int64_t T = INT32_MAX;
   std::vector<Segment> segs;
@@ -1213,27 +1384,31 @@ span_la_status span_la_plan_stats(const int32_t* view_cu_seqlens, int32_t num_vi
   if ((st = check_cu(branch_cu_seqlens, num_branches, T, "branch_cu_seqlens", &segs, false)) != SPAN_LA_OK) return st;
   if ((st = check_overlap(segs)) != SPAN_LA_OK) return st;
   if ((st = check_parents(branch_parent, num_branches, from_state ? num_parents : num_views)) != SPAN_LA_OK) return st;
+  const int H = num_heads;
   const Plan plan = make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
-                              branch_parent, num_heads, dtype == SPAN_LA_BF16);
+                              branch_parent, H, dtype == SPAN_LA_BF16, num_sms);
+  // Every count is summed over heads.
   int64_t state_rows = 0, finals = 0, tile_rows = 0, state_reads = 0;
-  for (const ChunkDesc& c : plan.chunks) state_rows += c.len;
+  for (const ChunkDesc& c : plan.chunks) state_rows += static_cast<int64_t>(c.len) * H;
   for (const SpanDesc& c : plan.spans) state_rows += c.len;
-  for (const ScanDesc& s : plan.scan) finals += s.final_idx >= 0;
+  for (const ScanDesc& s : plan.scan) finals += (s.final_idx >= 0) * (plan.span_mode ? 1 : H);
   for (const TileDesc& t : plan.tiles) {
-    tile_rows += t.nrows;
-    state_reads += (t.stateA >= 0) + (t.stateB >= 0);
+    tile_rows += static_cast<int64_t>(t.nrows) * H;
+    state_reads += static_cast<int64_t>((t.stateA >= 0) + (t.stateB >= 0)) * H;
   }
-  for (const OutTileDesc& t : plan.otiles) tile_rows += t.nrows;
-  for (const ItemDesc& it : plan.items) state_reads += (it.stateA >= 0) + (it.stateB >= 0);
-  stats[0] = plan.state_slots();
+  for (const WorkTile& w : plan.work) {
+    tile_rows += w.nrows;
+    if (w.flags & kTileFirst) state_reads += (w.stateA >= 0) + (w.stateB >= 0);
+  }
+  stats[0] = plan.state_slots(H);
   stats[1] = state_rows;
-  stats[2] = static_cast<int64_t>(plan.scan.size());
+  stats[2] = static_cast<int64_t>(plan.scan.size()) * (plan.span_mode ? 1 : H);
   stats[3] = finals;
-  stats[4] = static_cast<int64_t>(plan.n_out_tiles());
+  stats[4] = static_cast<int64_t>(plan.n_out_tiles()) * (plan.span_mode ? 1 : H);
   stats[5] = tile_rows;
   stats[6] = state_reads;
-  stats[7] = static_cast<int64_t>(plan.span_mode ? plan.items.size() : plan.tiles.size());
-  stats[8] = plan.G;
+  stats[7] = plan.span_mode ? plan.n_pieces : static_cast<int64_t>(plan.tiles.size()) * H;
+  stats[8] = plan.span_mode ? plan.run_tiles : 1;
   return SPAN_LA_OK;
 }
 
@@ -1321,72 +1496,29 @@ span_la_status span_la_pass_noalloc(const void* q, const void* k, const void* v,
   e = noalloc_scratch(&ws, &err);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed scratch)");
 
+  // The same plan, descriptors and launches as span_la_pass (so the results
+  // are the same bit for bit); the descriptors and the state slots live in
+  // the fixed scratch.
   const int H = dims.num_heads;
-  const int64_t T = dims.total_rows;
-  const Plan plan = make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
-                              branch_parent, H, true);
-  std::vector<uint8_t> host;
-  const size_t off_scan = put(host, plan.scan);
-  const size_t off_bounds = put(host, plan.bounds);
-  std::vector<WorkTile> work;
-  std::vector<int32_t> cta_begin;
-  int grid = 0;
-  if (!plan.items.empty()) grid = build_schedule(plan, H, num_sms, &work, &cta_begin);
-  const size_t off_spans = put(host, plan.spans);
-  const size_t off_work = put(host, work);
-  const size_t off_begin = put(host, cta_begin);
-  const size_t off_states = host.size();
-  const size_t need = off_states + static_cast<size_t>(plan.state_slots()) * H * kStateFloats * sizeof(float);
+  DescBlock desc = make_desc(make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
+                                       branch_parent, H, true, num_sms), H);
+  const size_t off_states = align256(desc.host.size());
+  const size_t need = off_states + static_cast<size_t>(desc.state_slots) * kStateFloats * sizeof(float);
   if (need > kNoAllocScratchBytes)
     return fail(SPAN_LA_ERR_INVALID,
                 "this pass needs %zu bytes of scratch; the fixed scratch of span_la_pass_noalloc holds "
                 "%zu bytes (use span_la_pass)", need, kNoAllocScratchBytes);
+  if (desc.n_out_tiles == 0 && desc.n_scan == 0) return SPAN_LA_OK;
 
-  // The error word starts each call at zero; everything else in the scratch
-  // is written before it is read.
+  // Everything the kernels read from the scratch is written by this call
+  // first.  The error word is not cleared here: a wait that ran out stays
+  // recorded until span_la_check reads it.
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   e = cudaStreamIsCapturing(stream, &cap);
-  if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(unsigned), stream);
-  if (e == cudaSuccess) e = upload_descriptors(ws, std::move(host), cap != cudaStreamCaptureStatusNone, stream);
+  if (e == cudaSuccess) e = upload_descriptors(ws, std::move(desc.host), cap != cudaStreamCaptureStatusNone, stream);
   if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
-  DeviceOperands tile_ops{}, chunk_ops{};
-  const void* ops[3] = {q, k, v};
-  for (int t = 0; t < 3; ++t) {
-    CUtensorMap* tm = t == 0 ? &tile_ops.q[0] : t == 1 ? &tile_ops.k[0] : &tile_ops.v[0];
-    CUtensorMap* cm = t == 0 ? &chunk_ops.q[0] : t == 1 ? &chunk_ops.k[0] : &chunk_ops.v[0];
-    if ((st = encode_map(tm, ops[t], T, H, kTileBoxRows, 1)) != SPAN_LA_OK) return st;
-    if (t > 0 && (st = encode_map(cm, ops[t], T, H, kSpanBoxRows, 1)) != SPAN_LA_OK) return st;
-  }
-  float* states = reinterpret_cast<float*>(ws + off_states);
-  bool kernel_before = false;
-  if (plan.state_slots() > 0) {
-    e = counted_launch(kKernelSpanState, stream, [&] {
-      const int sgrid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(plan.spans.size()) * H, num_sms));
-      return launch_span_state(chunk_ops.k, chunk_ops.v, reinterpret_cast<const SpanDesc*>(ws + off_spans),
-                               static_cast<int>(plan.spans.size()), H, states, sgrid, err, stream);
-    });
-    if (e != cudaSuccess) return cuda_fail(e, "span-state launch");
-    kernel_before = true;
-  }
-  if (!plan.scan.empty()) {
-    const bool pdl = kernel_before;
-    e = counted_launch(kKernelScan, stream, [&] {
-      return launch_scan(reinterpret_cast<const ScanDesc*>(ws + off_scan), static_cast<int>(plan.scan.size()),
-                         H, states, view_state_out, stream, pdl);
-    });
-    if (e != cudaSuccess) return cuda_fail(e, "scan launch");
-    kernel_before = true;
-  }
-  if (grid > 0) {
-    const bool pdl = kernel_before;
-    e = counted_launch(kKernelSpanOutput, stream, [&] {
-      return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v, reinterpret_cast<const WorkTile*>(ws + off_work),
-                                reinterpret_cast<const int32_t*>(ws + off_begin), grid, ws + off_bounds,
-                                view_state_out, states, out, H, err, stream, pdl);
-    });
-    if (e != cudaSuccess) return cuda_fail(e, "span-output launch");
-  }
-  return SPAN_LA_OK;
+  return enqueue_pass(desc, ws, nullptr, reinterpret_cast<float*>(ws + off_states), q, k, v, dims,
+                      view_state_out, view_state_out, out, err, stream, nullptr, dev);
 }
 
 span_la_status span_la_fault_inject(int32_t kind, int32_t count) {
@@ -1394,6 +1526,19 @@ span_la_status span_la_fault_inject(int32_t kind, int32_t count) {
   if (kind != SPAN_LA_FAULT_ALLOC) return fail(SPAN_LA_ERR_INVALID, "unknown fault kind %d", kind);
   if (count < 0) return fail(SPAN_LA_ERR_INVALID, "count %d < 0", count);
   g_fail_allocs.store(count, std::memory_order_relaxed);
+  return SPAN_LA_OK;
+}
+
+span_la_status span_la_selftest_wait_timeout_noalloc(int32_t limit_us, cudaStream_t stream) {
+  g_detail.clear();
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(SPAN_LA_ERR_INVALID, "limit_us %d not in [1, 1000000]", limit_us);
+  uint8_t* ws = nullptr;
+  unsigned* err = nullptr;
+  cudaError_t e = noalloc_scratch(&ws, &err);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation error word)");
+  e = launch_wait_timeout_probe(static_cast<unsigned>(limit_us), err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "probe launch");
   return SPAN_LA_OK;
 }
 

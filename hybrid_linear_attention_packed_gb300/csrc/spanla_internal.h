@@ -22,12 +22,17 @@ struct ChunkDesc {
   int32_t len;    // valid rows, 1..64
 };
 
-// One segment's run of chunk-state slots for the segmented scan.
+// One run of state slots for the segmented scan: the slots of one segment
+// (chunk mode: one slot per 64-row chunk and head, the grid's y index is the
+// head) or of one segment-head (span mode: head >= 0, one slot per piece).
+// The scan turns the run into exclusive prefixes in place and writes the
+// run's total (the view's final state) to final_out[final_idx] when
+// final_idx >= 0; a run of no slots gives the zero state.
 struct ScanDesc {
-  int32_t chunk0;     // first state slot
-  int32_t nchunks;    // slots in the run (0 for an empty view)
+  int32_t slot0;      // first state slot
+  int32_t nslots;     // slots in the run (0 for an empty view)
   int32_t final_idx;  // index into the final-state output, or -1
-  int32_t pad;
+  int32_t head;       // span mode: the head; chunk mode: -1 (all heads)
 };
 
 // One output tile of up to 128 rows, for one head (the grid's y index).
@@ -47,47 +52,41 @@ struct TileDesc {
   int32_t pad1;
 };
 
-// bf16 path.  A span is a run of up to G consecutive 128-row tiles of one
-// segment (a view or a branch longer than one tile).  The span-state kernel
-// computes the span's local state sum K^T V (span i owns state slot i); the
-// scan turns the slots of each segment into exclusive prefixes; the
-// span-output kernel walks the span's tiles carrying the state.
+// bf16 path (span mode).  The output work -- every tile of every
+// segment-head -- is laid out request by request (a view's tiles, then the
+// tiles of the branches whose parent it is, head by head) and cut into one
+// contiguous run per CTA of the output kernel, so that every CTA gets the
+// same number of tiles.  A *piece* is the part of one segment-head (a view
+// or a branch longer than one tile) inside one run.  Every piece of a view,
+// and every piece of a long branch cut into two or more pieces, owns one
+// state slot: the span-state kernel writes the piece's local sum K^T V
+// there, and the scan turns the slots of each segment-head into exclusive
+// prefixes, i.e. the state entering each piece.
 struct SpanDesc {
-  int32_t row0;   // first row of the span
-  int32_t len;    // rows in the span, 1 .. G*128
+  int32_t row0;   // first row of the piece
+  int32_t len;    // rows in the piece (>= 1)
+  int32_t head;
+  int32_t slot;   // state slot (fp32 [64][64] at ws + slot * 4096)
 };
+static_assert(sizeof(SpanDesc) == 16, "SpanDesc layout");
 
-// One work item of the span-output kernel (for every head): a span, or one
-// tile of packed short branches.  Its start state is stateA[a] + stateB[b]
-// (a missing term is -1), as for TileDesc.
-struct ItemDesc {
-  int32_t tile0;    // first entry of the item's tiles in the tile table
-  int32_t ntiles;   // 1 .. G
-  int32_t stateA;
-  int32_t stateB;
-};
-
-struct OutTileDesc {
-  int32_t row0;
-  int32_t nrows;    // 1 .. 128
-  int32_t bound0;   // segment starts inside the tile, as for TileDesc
-  int32_t nbound;
-};
-
-// One tile of the span-output kernel's per-CTA schedule (48 bytes).  The
-// host deals the (item, head) work units to CTAs and lists each CTA's tiles
-// in processing order; CTA c runs records [cta_begin[c], cta_begin[c+1]).
+// One tile of the span-output kernel's per-CTA schedule (48 bytes).  CTA c
+// runs records [cta_begin[c], cta_begin[c+1]) in order: the tiles of its run.
+// A piece's first tile loads the piece's start state stateA + stateB (the
+// parent view's final state, index into the [n][H][64][64] final-state
+// array, and/or the piece's prefix slot; -1 where absent); every later tile
+// of the piece continues from the state the previous one left.
 constexpr int kInlineBounds = 16;
-constexpr int32_t kTileFirst = 1;      // first tile of its item: load the start state
-constexpr int32_t kTileLast = 2;       // last tile of its item: no state update
-constexpr int32_t kTileHasInit = 4;    // the item has a start state (stateA and/or stateB)
+constexpr int32_t kTileFirst = 1;      // first tile of its piece: load the start state
+constexpr int32_t kTileLast = 2;       // last tile of its piece: no state update
+constexpr int32_t kTileHasInit = 4;    // the piece has a start state (stateA and/or stateB)
 struct WorkTile {
   int32_t row0;
   int32_t nrows;
   int32_t head;
   int32_t flags;
-  int32_t stateA;    // start state terms (first tile of an item), -1 if absent
-  int32_t stateB;
+  int32_t stateA;    // parent view (first tile of a piece), -1 if absent
+  int32_t stateB;    // prefix slot (first tile of a piece), -1 if absent
   int32_t bound0;    // segment starts in the global bounds table
   int32_t nbound;    // the first kInlineBounds are also inline below
   uint8_t inl[kInlineBounds];
@@ -169,22 +168,24 @@ cudaError_t launch_chunk_state(bool split, const CUtensorMap* tm_k, const CUtens
                                const ChunkDesc* chunks, int n_chunks, int H, float* ws,
                                unsigned* err, cudaStream_t stream, bool pdl);
 
-cudaError_t launch_scan(const ScanDesc* scan, int n_scan, int H, float* ws, float* final_out,
-                        cudaStream_t stream, bool pdl);
+// span_mode: one head per entry (ScanDesc::head); otherwise every entry
+// covers all H heads (grid y).
+cudaError_t launch_scan(const ScanDesc* scan, int n_scan, int H, bool span_mode, float* ws,
+                        float* final_out, cudaStream_t stream, bool pdl);
 
+// spans: the pieces in per-CTA order, CTA c running [span_begin[c], span_begin[c+1]).
+// [prefetch, prefetch + prefetch_bytes) is brought into L2 on the way (the
+// pass's descriptors; 16-byte aligned).
 cudaError_t launch_span_state(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                              const SpanDesc* spans, int n_spans, int H, float* ws,
-                              int grid, unsigned* err, cudaStream_t stream);
+                              const SpanDesc* spans, const int32_t* span_begin, int grid,
+                              float* ws, const void* prefetch, size_t prefetch_bytes, unsigned* err,
+                              cudaStream_t stream);
 
 cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                const CUtensorMap* tm_v, const WorkTile* work,
                                const int32_t* cta_begin, int grid, const uint8_t* bounds,
                                const float* stateA, const float* stateB, void* out, int H,
                                unsigned* err, cudaStream_t stream, bool pdl);
-
-// Work items the planner aims for when it picks the span length G.
-constexpr int kTargetItems = 2 * 152;
-constexpr int kMaxSpanTiles = 8;
 
 cudaError_t launch_tile_output(bool split, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                const CUtensorMap* tm_v, const TileDesc* tiles, int n_tiles,
@@ -196,6 +197,9 @@ cudaError_t launch_wait_timeout_probe(unsigned limit_us, unsigned* err, cudaStre
 // Fixed workspace of span_la_pass_noalloc (a file-scope device array).
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 cudaError_t noalloc_scratch(uint8_t** scratch, unsigned** err);
+// The error word of that path on the current device, or NULL when the path
+// has not been set up on it (no lookup is made then).
+cudaError_t noalloc_error_word(unsigned** err);
 
 // Box sizes of the TMA descriptors each kernel expects.
 constexpr int kChunkBoxRows = kChunk;     // chunk-state kernel: 64 rows x 2 heads

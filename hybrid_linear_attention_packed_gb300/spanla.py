@@ -33,7 +33,8 @@ EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
             "span_la_pass_noalloc", "span_la_cache_create", "span_la_cache_destroy",
             "span_la_cache_put", "span_la_cache_contains", "span_la_cache_branches",
             "span_la_cache_stats", "span_la_softmax_pass", "span_la_softmax_branches_from_kv",
-            "span_la_fault_inject", "span_la_softmax_plan_stats")
+            "span_la_fault_inject", "span_la_softmax_plan_stats",
+            "span_la_selftest_wait_timeout_noalloc")
 NUM_KERNELS = 7
 
 
@@ -85,6 +86,8 @@ def load_library(path: Optional[str] = None):
         lib.span_la_version.restype = ctypes.c_int32
         lib.span_la_selftest_wait_timeout.argtypes = [ctypes.c_int32, vp]
         lib.span_la_selftest_wait_timeout.restype = ctypes.c_int
+        lib.span_la_selftest_wait_timeout_noalloc.argtypes = [ctypes.c_int32, vp]
+        lib.span_la_selftest_wait_timeout_noalloc.restype = ctypes.c_int
         lib.span_la_profile_enable.argtypes = [ctypes.c_int32]
         lib.span_la_profile_enable.restype = ctypes.c_int
         lib.span_la_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double),
@@ -97,7 +100,8 @@ def load_library(path: Optional[str] = None):
         lib.span_la_kernel_name.restype = ctypes.c_char_p
         lib.span_la_plan_stats.argtypes = [i32p, ctypes.c_int32, i32p, ctypes.c_int32, i32p,
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                           ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)]
+                                           ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.POINTER(ctypes.c_int64)]
         lib.span_la_plan_stats.restype = ctypes.c_int
         lib.span_la_softmax_pass.argtypes = [vp, vp, vp, Dims, i32p, ctypes.c_int32, i32p,
                                              ctypes.c_int32, i32p, ctypes.c_float, vp, vp, vp]
@@ -425,13 +429,21 @@ def span_la_selftest_wait_timeout(limit_us: int, stream=None) -> None:
            "span_la_selftest_wait_timeout")
 
 
+def span_la_selftest_wait_timeout_noalloc(limit_us: int, stream=None) -> None:
+    lib = load_library()
+    _raise(lib, lib.span_la_selftest_wait_timeout_noalloc(int(limit_us), _stream_handle(stream)),
+           "span_la_selftest_wait_timeout_noalloc")
+
+
 PLAN_FIELDS = ("state_slots", "state_rows", "scan_segments", "final_states", "tiles",
-               "tile_rows", "start_state_reads", "out_items", "span_tiles")
+               "tile_rows", "start_state_reads", "out_items", "run_tiles")
 
 
 def plan_stats(view_cu_seqlens, branch_cu_seqlens, branch_parent, num_heads: int,
-               dtype: str = "bf16", num_parents: int = 0, from_state: bool = False) -> dict:
-    """Work units the library would launch for this metadata (host only)."""
+               dtype: str = "bf16", num_parents: int = 0, from_state: bool = False,
+               num_sms: int = 152) -> dict:
+    """Work units the library would launch for this metadata on a GPU with
+    ``num_sms`` SMs (host only; every count summed over heads)."""
     lib = load_library()
     vcu, bcu, par = _i32(view_cu_seqlens), _i32(branch_cu_seqlens), _i32(branch_parent)
     V = max(len(vcu) - 1, 0)
@@ -439,7 +451,8 @@ def plan_stats(view_cu_seqlens, branch_cu_seqlens, branch_parent, num_heads: int
     stats = (ctypes.c_int64 * len(PLAN_FIELDS))()
     dt = SPAN_LA_BF16 if dtype == "bf16" else SPAN_LA_F32
     _raise(lib, lib.span_la_plan_stats(_iptr(vcu), V, _iptr(bcu), B, _iptr(par), int(num_parents),
-                                       1 if from_state else 0, int(num_heads), dt, stats),
+                                       1 if from_state else 0, int(num_heads), dt, int(num_sms),
+                                       stats),
            "span_la_plan_stats")
     return dict(zip(PLAN_FIELDS, (int(x) for x in stats)))
 

@@ -13,11 +13,15 @@
  * starts from the final state of its parent view (the state after the view's
  * last row) and runs over its own rows only; branches never see one another
  * (section "The Workload": branches attend to the view but not to each other).
- * The work is done in 64-token chunks as the "Kernels" section describes
- * (each chunk a few 64x64 matrix products; one scan of chunk states covers
- * every view of the pass, in three launches): per-chunk local state K^T V,
- * one segmented prefix scan over every view of the pass, and the chunk/branch
- * output (masked Q K^T V inside a tile plus Q S_prev).
+ * The work follows the chunked form the "Kernels" section describes (each
+ * chunk a few 64x64 matrix products; one scan of states covers every view of
+ * the pass, in three launches): a local state K^T V per piece of rows, one
+ * segmented prefix scan over every view of the pass, and the output of every
+ * 128-row tile (masked Q K^T V inside the tile plus Q S_prev).  For bf16
+ * inputs the output work is cut into one run of tiles per SM; a piece is the
+ * part of one view (per head) inside one run, and the output kernel carries
+ * the state from tile to tile on chip.  For fp32 inputs the pieces are
+ * 64-row chunks and every 128-row tile starts from its chunk's prefix.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -156,22 +160,36 @@ span_la_status span_la_branches_from_state(const float *cached_state, int32_t nu
  *
  *   arguments        as for span_la_pass; dims.dtype must be SPAN_LA_BF16
  *                    (fp32 inputs need per-call scratch: SPAN_LA_ERR_UNSUPPORTED)
- *   size limit       descriptors plus one 16 KiB fp32 state per span and head
- *                    must fit in 16 MiB (a 7,400-token or four-request 16-head
- *                    pass does); a larger pass returns SPAN_LA_ERR_INVALID with
- *                    the bytes it needs, before anything is enqueued
+ *   size limit       descriptors plus one 16 KiB fp32 state per piece-head
+ *                    must fit in 16 MiB, i.e. about 1,000 piece-heads.  A
+ *                    piece is the part of one view inside one SM's run of
+ *                    output tiles, so a pass needs at most about
+ *                    (views + SMs) x heads of them: a 16-head pass of up to
+ *                    ~60 views fits on a 152-SM GPU (the 7,400-token pass
+ *                    needs about 170).  A larger pass returns
+ *                    SPAN_LA_ERR_INVALID with the bytes it needs, before
+ *                    anything is enqueued
  *   first call       the first call on a device looks up the array's device
  *                    address (cudaGetSymbolAddress with that device current)
  *                    and caches it; make that first call before any stream
- *                    capture
+ *                    capture, and do not use this entry point across a
+ *                    cudaDeviceReset of that device (the cached address dies
+ *                    with the context)
+ *   memory           the array is reserved on every device whose context
+ *                    loads the library's module that holds it: where it was
+ *                    used, or on every device under eager module loading
+ *                    (CUDA_MODULE_LOADING=EAGER); it stays until the process
+ *                    exits
  *   sharing          every call uses the same array and leaves its contents
  *                    behind; calls whose work overlaps on the GPU (other
  *                    streams, other threads) race on it -- order them on one
  *                    stream
- *   errors           as for span_la_pass, except that device-side wait
- *                    timeouts of this path land in an error word inside the
- *                    library's fixed scratch (cleared at each call) and are
- *                    not reported by span_la_check
+ *   errors           as for span_la_pass.  Device-side wait timeouts of this
+ *                    path land in an error word of its own, which
+ *                    span_la_check (on the same device) reads and clears
+ *                    together with the library's main error word; the word
+ *                    is not cleared by a call, so a timeout stays recorded
+ *                    until span_la_check reports it
  */
 span_la_status span_la_pass_noalloc(const void *q, const void *k, const void *v,
                                     span_la_dims dims,
@@ -183,9 +201,10 @@ span_la_status span_la_pass_noalloc(const void *q, const void *k, const void *v,
 
 /*
  * span_la_check -- synchronise `stream`, then report (and clear) the device
- * error word of the current device.  Returns SPAN_LA_ERR_CUDA if the stream
- * reports a CUDA error, SPAN_LA_ERR_TIMEOUT if a kernel's bounded wait ran
- * out, SPAN_LA_OK otherwise.
+ * error words of the current device: the library's main word and, where
+ * span_la_pass_noalloc has run on the device, that path's own word.  Returns
+ * SPAN_LA_ERR_CUDA if the stream reports a CUDA error, SPAN_LA_ERR_TIMEOUT if
+ * a kernel's bounded wait ran out, SPAN_LA_OK otherwise.  Allocates nothing.
  */
 span_la_status span_la_check(cudaStream_t stream);
 
@@ -207,6 +226,15 @@ int32_t span_la_version(void);
  * runs out neither traps nor hangs.
  */
 span_la_status span_la_selftest_wait_timeout(int32_t limit_us, cudaStream_t stream);
+
+/*
+ * span_la_selftest_wait_timeout_noalloc -- the same failure-detection hook
+ * for the error word of span_la_pass_noalloc: the probe kernel's wait runs
+ * out after `limit_us` and sets that word; span_la_check() then reports
+ * SPAN_LA_ERR_TIMEOUT.  Allocates nothing (the first use on a device looks
+ * the word up, as span_la_pass_noalloc does).
+ */
+span_la_status span_la_selftest_wait_timeout_noalloc(int32_t limit_us, cudaStream_t stream);
 
 /*
  * span_la_fault_inject -- failure-detection hook on the host: with kind
@@ -237,17 +265,18 @@ span_la_status span_la_softmax_plan_stats(const int32_t *view_cu_seqlens, int32_
 
 /*
  * span_la_plan_stats -- host only, no CUDA call: the work units a call with
- * this metadata, head count and dtype would launch (used to count the
- * algorithmic bytes of each kernel).
- *   stats[0] state slots: 64-row chunks (fp32) or spans of up to G tiles (bf16)
- *   stats[1] rows those slots cover (rows whose K and V the state kernel reads)
- *   stats[2] segments of the segmented scan
- *   stats[3] scan segments that write a final view state
- *   stats[4] output tiles (<= 128 rows each)
- *   stats[5] rows those tiles cover
- *   stats[6] fp32 64x64 start-state reads of the output kernel (per head)
- *   stats[7] output work items per head (tiles for fp32, items for bf16)
- *   stats[8] G, the tiles per span (1 for fp32)
+ * this metadata, head count and dtype would launch on a GPU with `num_sms`
+ * SMs (used to count the algorithmic bytes of each kernel).  Every count is
+ * summed over the heads.
+ *   stats[0] state slots: 64-row chunk-heads (fp32) or piece-heads (bf16)
+ *   stats[1] row-heads those slots cover (rows whose K and V the state kernel reads)
+ *   stats[2] runs of the segmented scan
+ *   stats[3] final view states the scan writes (view-heads)
+ *   stats[4] output tile-heads (<= 128 rows each)
+ *   stats[5] row-heads those tiles cover
+ *   stats[6] fp32 64x64 start-state reads of the output kernel
+ *   stats[7] output pieces (fp32: tile-heads)
+ *   stats[8] longest run of tiles of one output CTA (bf16; 1 for fp32)
  * from_state != 0 plans span_la_branches_from_state (views ignored).
  * Returns SPAN_LA_ERR_INVALID on bad metadata, like the entry points.
  */
@@ -255,7 +284,7 @@ span_la_status span_la_plan_stats(const int32_t *view_cu_seqlens, int32_t num_vi
                                   const int32_t *branch_cu_seqlens, int32_t num_branches,
                                   const int32_t *branch_parent, int32_t num_parents,
                                   int32_t from_state, int32_t num_heads, int32_t dtype,
-                                  int64_t *stats);
+                                  int32_t num_sms, int64_t *stats);
 
 /*
  * Kernel profiling (tracing hook).  Kernels are numbered

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.span_la_version() == 100
+    assert lib.span_la_version() == 20000
     for code in range(6):
         assert lib.span_la_status_string(code)
 
@@ -111,25 +111,48 @@ def test_missing_library_fails_loudly(tmp_path):
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("name", ["tiny", "single", "packed4", "cached_long", "sweep4"])
 def test_plan_covers_every_row_once(lib, dtype, name):
-    """The planner's output tiles cover every segment row, and its state slots
-    cover exactly the rows of views and of branches longer than one tile."""
+    """The planner's output tiles cover every segment row of every head, its
+    state slots cover exactly the rows of views (and, where a long branch is
+    cut into pieces, of those branches), and it writes one final state per
+    view-head.  Counts are summed over heads."""
     from hybrid_linear_attention_packed_gb300 import workloads
     w = workloads.by_name(name)
-    st = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H, dtype)
-    assert st["tile_rows"] == w.rows
+    H = w.H
+    st = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, H, dtype, num_sms=152)
+    assert st["tile_rows"] == w.rows * H
+    view_rows = int(w.view_lens.sum())
     long_rows = int(sum(L for L in w.branch_lens if L > 128))
-    assert st["state_rows"] == int(w.view_lens.sum()) + long_rows
-    assert st["scan_segments"] == w.V + sum(1 for L in w.branch_lens if L > 128)
-    assert st["final_states"] == w.V
+    assert st["final_states"] == w.V * H
     if dtype == "f32":
-        assert st["span_tiles"] == 1
-        assert st["state_slots"] == sum(-(-int(L) // 64) for L in list(w.view_lens)
-                                        + [L for L in w.branch_lens if L > 128])
+        assert st["run_tiles"] == 1
+        assert st["state_rows"] == (view_rows + long_rows) * H
+        assert st["scan_segments"] == (w.V + sum(1 for L in w.branch_lens if L > 128)) * H
+        assert st["state_slots"] == H * sum(-(-int(L) // 64) for L in list(w.view_lens)
+                                            + [L for L in w.branch_lens if L > 128])
     else:
-        G = st["span_tiles"]
-        assert 1 <= G <= 8
-        assert st["state_slots"] == sum(-(-int(L) // (128 * G)) for L in list(w.view_lens)
-                                        + [L for L in w.branch_lens if L > 128])
+        assert view_rows * H <= st["state_rows"] <= (view_rows + long_rows) * H
+        # runs of equal length over at least 85 % of the SMs
+        assert st["run_tiles"] <= -(-st["tiles"] // int(0.85 * min(152, st["tiles"])))
+        # every view-head has one scan run; pieces never outnumber
+        # segment-heads plus run boundaries
+        assert st["scan_segments"] >= w.V * H
+        n_seg = w.V + sum(1 for L in w.branch_lens if L > 128)
+        assert st["state_slots"] <= n_seg * H + 152
+
+
+@pytest.mark.parametrize("name", ["single", "packed4", "sweep4"])
+def test_span_plan_runs_are_balanced(lib, name):
+    """The bf16 planner cuts the output work into runs of equal length (+-1
+    tile) over at least 85 % of the SMs, whatever the SM count; on the
+    7,400-token pass with 16 heads and 148 or 152 SMs every run is 7 tiles."""
+    from hybrid_linear_attention_packed_gb300 import workloads
+    w = workloads.by_name(name)
+    for nsm in (1, 7, 64, 148, 152, 1000):
+        st = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H, "bf16", num_sms=nsm)
+        assert st["run_tiles"] <= -(-st["tiles"] // max(1, int(0.85 * min(nsm, st["tiles"]))))
+        assert st["tile_rows"] == w.rows * w.H
+        if name == "single" and nsm in (148, 152):
+            assert st["run_tiles"] == 7
 
 
 def test_view_cache_validation_without_a_device(lib):
@@ -261,8 +284,9 @@ def test_random_metadata_plans_cover_every_row(lib, seed):
     H = int(rng.integers(1, 17))
     rows = int(vl.sum() + bl.sum())
     for dtype in ("bf16", "f32"):
-        st = spanla.plan_stats(vcu, bcu, par, H, dtype)
-        assert st["tile_rows"] == rows
+        st = spanla.plan_stats(vcu, bcu, par, H, dtype, num_sms=152)
+        assert st["tile_rows"] == rows * H
+        assert st["final_states"] == V * H
     sa = spanla.softmax_plan_stats(vcu, bcu, par, H, num_sms=152)
     assert sa["rows"] == rows * H
     assert sa["key_blocks"] >= sa["items"]

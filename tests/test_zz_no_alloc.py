@@ -4,9 +4,11 @@
 while a pass runs (a process that gave the GPU's memory to its own pool, or
 code where an allocation could block or fail at the wrong moment): it runs the
 same pass in a fixed workspace that the library owns.  These tests call it
-through the C ABI and compare two calls in a row with ``span_la_pass`` on the
-same inputs, within the tolerance of the other parity tests.  This file is
-named so that pytest collects it last.
+through the C ABI.  It plans and launches exactly what ``span_la_pass`` does,
+so two calls in a row must give the same bits as ``span_la_pass`` on the same
+inputs; the 7,400-token pass is also checked against the float64 oracle
+within the bf16 bound of the other parity tests.  This file is named so that
+pytest collects it last.
 """
 import ctypes
 
@@ -14,11 +16,14 @@ import numpy as np
 import pytest
 import torch
 
+from helpers import f64, rel_err, segment_rows
 from hybrid_linear_attention_packed_gb300 import spanla, workloads
+from oracle import oracle_pass
 
 pytestmark = pytest.mark.gpu
 
 TOL_BF16 = 1e-2
+SCRATCH_BYTES = 16 << 20
 
 
 def _i32p(a):
@@ -37,9 +42,27 @@ def _noalloc(lib, w, q, k, v, out, state):
     return st, lib.span_la_last_error_detail().decode()
 
 
-def _rel(a, b):
-    a, b = a.double(), b.double()
-    return float((a - b).abs().max() / b.abs().max())
+def _seg(w, dev):
+    return torch.from_numpy(segment_rows(w)).to(dev)
+
+
+def _equal_to_span_la_pass(lib, w, dev):
+    q, k, v = (t.to(dev).contiguous() for t in (w.q, w.k, w.v))
+    out = torch.full_like(q, float("nan"))
+    state = torch.full((w.V, w.H, 64, 64), float("nan"), dtype=torch.float32, device=dev)
+    st, detail = _noalloc(lib, w, q, k, v, out, state)
+    assert st == 0, detail
+    spanla.span_la_check()
+    ref_out, ref_state = spanla.span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
+                                             out=torch.full_like(q, float("nan")))
+    spanla.span_la_check()
+    seg = _seg(w, dev)
+    assert not torch.isnan(out[seg]).any()
+    assert torch.isnan(out[~seg]).all()
+    # same plan, same kernels: the same bits
+    assert torch.equal(out[seg], ref_out[seg])
+    assert torch.equal(state, ref_state)
+    return out, state
 
 
 def test_noalloc_matches_span_la_pass_on_two_calls_in_a_row(cuda_device):
@@ -48,36 +71,61 @@ def test_noalloc_matches_span_la_pass_on_two_calls_in_a_row(cuda_device):
              workloads.make_pass([300, 129, 64], [20, 50, 200, 7], [0, 0, 1, 2], H=4,
                                  dtype="bf16", seed=31)]
     for w in cases:   # two calls in a row, on different passes
-        q, k, v = (t.to(cuda_device).contiguous() for t in (w.q, w.k, w.v))
-        out = torch.full_like(q, float("nan"))
-        state = torch.full((w.V, w.H, 64, 64), float("nan"), dtype=torch.float32, device=cuda_device)
-        st, detail = _noalloc(lib, w, q, k, v, out, state)
-        assert st == 0, detail
-        torch.cuda.synchronize()
-        ref_out, ref_state = spanla.span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
-                                                 out=torch.full_like(q, float("nan")))
-        spanla.span_la_check()
-        seg = torch.zeros(w.T, dtype=torch.bool)
-        for cu in (w.view_cu, w.branch_cu):
-            for s in range(len(cu) - 1):
-                seg[cu[s]:cu[s + 1]] = True
-        seg = seg.to(cuda_device)
-        assert not torch.isnan(out[seg]).any()
-        assert torch.isnan(out[~seg]).all()
-        assert _rel(out[seg], ref_out[seg]) <= TOL_BF16
-        assert _rel(state, ref_state) <= TOL_BF16
+        _equal_to_span_la_pass(lib, w, cuda_device)
 
 
-def test_noalloc_rejects_a_pass_beyond_its_fixed_scratch(cuda_device):
+def test_noalloc_single_request_against_the_oracle(cuda_device):
+    """The 7,400-token pass through the fixed scratch, element by element
+    against the float64 oracle (max|o - o_ref| / max|o_ref| <= 1e-2)."""
     lib = spanla.load_library()
-    w = workloads.sweep(32, 0)   # needs far more than 16 MiB of span states
-    # metadata only is needed before the size check; small dummy tensors would
-    # fail the row-range checks, so use real-size (uninitialised) buffers
-    q = torch.empty((w.T, w.H, 64), dtype=torch.bfloat16, device=cuda_device)
-    out = torch.empty_like(q)
-    state = torch.empty((w.V, w.H, 64, 64), dtype=torch.float32, device=cuda_device)
+    w = workloads.single_request(0)
+    out, state = _equal_to_span_la_pass(lib, w, cuda_device)
+    ref, ref_state = oracle_pass(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu,
+                                 w.branch_parent)
+    seg = segment_rows(w)
+    assert rel_err(f64(out)[seg], ref[seg]) <= TOL_BF16
+    assert rel_err(f64(state), ref_state) <= TOL_BF16
+
+
+def test_noalloc_timeout_is_reported_by_span_la_check(cuda_device):
+    """A bounded wait that runs out on the no-allocation path's error word is
+    reported by span_la_check as SPAN_LA_ERR_TIMEOUT, and cleared by it."""
+    spanla.span_la_check()
+    spanla.span_la_selftest_wait_timeout_noalloc(1000)
+    with pytest.raises(spanla.SpanLAError) as exc:
+        spanla.span_la_check()
+    assert exc.value.status == 5 and "no-allocation path 0x4" in str(exc.value)
+    spanla.span_la_check()   # cleared
+    # the path still works afterwards
+    _equal_to_span_la_pass(spanla.load_library(), workloads.make_pass(
+        [200, 70], [9, 30], [0, 1], H=2, dtype="bf16", seed=5), cuda_device)
+
+
+def _many_views(n_views, H=16, rows=64, seed=7):
+    return workloads.make_pass([rows] * n_views, [], [], H=H, dtype="bf16", seed=seed)
+
+
+def test_noalloc_size_limit(cuda_device):
+    """The scratch holds descriptors plus one 16 KiB state per piece-head.  60
+    one-tile views of 16 heads need 960 states (15.7 MB with the descriptors):
+    they fit and match span_la_pass; 66 views need 1,056 states (17.3 MB):
+    rejected before anything is enqueued, with the bytes the pass needs."""
+    lib = spanla.load_library()
+    st_fit = spanla.plan_stats(_many_views(60).view_cu, [], [], 16, "bf16",
+                               num_sms=torch.cuda.get_device_properties(cuda_device).multi_processor_count)
+    assert st_fit["state_slots"] * 16384 < SCRATCH_BYTES
+    _equal_to_span_la_pass(lib, _many_views(60), cuda_device)
+
+    w = _many_views(66)
+    q = w.q.to(cuda_device)
+    out = torch.full_like(q, float("nan"))
+    state = torch.full((w.V, w.H, 64, 64), float("nan"), dtype=torch.float32, device=cuda_device)
     st, detail = _noalloc(lib, w, q, q, q, out, state)
     assert st == 1 and "fixed scratch" in detail
+    need = int(detail.split("needs ")[1].split(" bytes")[0])
+    assert need > SCRATCH_BYTES
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all() and torch.isnan(state).all()   # nothing written
 
 
 def test_noalloc_rejects_fp32_inputs(cuda_device):
