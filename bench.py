@@ -213,6 +213,44 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
+def event_floor_us(torch, stream, flush, reps: int = 60) -> float:
+    """Median elapsed time of an empty CUDA-event pair on `stream` right after an
+    L2 flush: the floor every event-timed kernel duration includes."""
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(ts[5:])
+
+
+def branch_variants(w, n: int, seed: int = 12345):
+    """n variants of a workload's branch metadata over the same rows: within each
+    parent's run of branches the lengths are permuted, so every variant packs
+    the same rows and views but cuts its branches differently (a fresh plan for
+    the library's plan cache).  Returns (branch_cu, branch_parent) pairs."""
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(w.branch_lens, dtype=np.int64)
+    par = np.asarray(w.branch_parent, dtype=np.int32)
+    out = []
+    for _ in range(n):
+        perm = np.arange(len(lens))
+        b = 0
+        while b < len(lens):
+            e = b
+            while e < len(lens) and par[e] == par[b]:
+                e += 1
+            perm[b:e] = b + rng.permutation(e - b)
+            b = e
+        cu = np.concatenate([[int(w.branch_cu[0])], int(w.branch_cu[0]) + np.cumsum(lens[perm])])
+        out.append((np.ascontiguousarray(cu, dtype=np.int32), par.copy()))
+    return out
+
+
 # ---------------------------------------------------------------- CPU oracle
 def cpu_model() -> str:
     try:
@@ -282,7 +320,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w, args.workload),
+            "config": dict(workload_config(w, args.workload), parallelism="dp1"),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -361,7 +399,8 @@ def run_softmax_reference(args):
     line = {"impl": "reference", "metric": SOFTMAX_METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": reps, "warmup": 0, "ms_per_step": med * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": dict(workload_config(w, args.workload), layer="softmax"),
+            "data": "synthetic", "config": dict(workload_config(w, args.workload), layer="softmax",
+                                                parallelism="dp1"),
             "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -701,7 +740,10 @@ def main():
             plan = st_ if plan is None else {key: plan[key] + st_[key] for key in plan}
     else:
         plan = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H, w.dtype, num_sms=nsm)
-    alg = algorithmic_bytes(plan, w.H, esize, w.T)
+    # the plan above covers every call of a step; bytes per launch divide it by
+    # the calls a step makes (each call launches each kernel once)
+    calls_per_step = len(shard_cu) if shards_mode else (len(req_calls) if args.per_request else 1)
+    alg = {name: b / calls_per_step for name, b in algorithmic_bytes(plan, w.H, esize, w.T).items()}
     peaks = {}
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk):
@@ -728,7 +770,7 @@ def main():
                 "unit": "GB/s", "frac": dk["gbs"] / hbm_peak, "traffic": traffic,
                 "peak_source": peak_src,
                 "alg_bytes_per_launch": dk["alg_bytes"]}
-    step_bytes = sum(alg[n] for n in kernels)
+    step_bytes = sum(alg[n] for n in kernels) * calls_per_step
     chunked = chunked_method_bytes(w, esize) if not shards_mode else rows_per_step * w.H * 4 * 64 * esize
     iob = io_bytes(w, esize) if not shards_mode else rows_per_step * w.H * 4 * 64 * esize
     pass_roofline = {"method_bytes": step_bytes,
@@ -736,7 +778,104 @@ def main():
                      "io_bytes": iob,
                      "io_frac": iob / (ms / 1e3) / 1e9 / hbm_peak,
                      "chunked_method_bytes": chunked,
-                     "chunked_method_frac": chunked / (ms / 1e3) / 1e9 / hbm_peak}
+                     "chunked_method_frac": chunked / (ms / 1e3) / 1e9 / hbm_peak,
+                     "chunked_method_note": "bytes of the pages' layout (one fp32 state per 64-token "
+                                            "chunk through the scan), which this design does not move: "
+                                            "context only; method_frac and io_frac are this design's"}
+
+    # The floor of an event-timed duration on this stream (an empty event pair
+    # after an L2 flush): reported beside the roofline, whose kernel time
+    # includes it.
+    floor_us = event_floor_us(torch, stream, flush)
+    roofline["event_floor_us"] = floor_us
+    if dk["avg_us"] > floor_us:
+        roofline["frac_above_event_floor"] = dk["alg_bytes"] / ((dk["avg_us"] - floor_us) / 1e6) / 1e9 / hbm_peak
+
+    # Fresh metadata every step: 24 variants of the branch layout over the same
+    # rows, cycled, so that every call misses the library's 16-entry plan cache
+    # and builds, uploads and launches a new plan (the host plan build and the
+    # descriptor upload fall inside each step).
+    cold = None
+    if w.B > 1 and not args.per_request:
+        NV = 24
+        variants = branch_variants(w, NV)
+        if shards_mode:
+            def cold_call(j):
+                bcu_j, par_j = variants[j]
+                per = (w.B + 3) // 4
+                for s_ in range(4):
+                    b0, b1 = s_ * per, min(w.B, (s_ + 1) * per)
+                    spanla.span_la_branches_from_state(cached, q, k, v, bcu_j[b0:b1 + 1],
+                                                       np.zeros(b1 - b0, np.int32), out=out)
+        else:
+            def cold_call(j):
+                bcu_j, par_j = variants[j]
+                spanla.span_la_pass(q, k, v, w.view_cu, bcu_j, par_j, out=out, view_state_out=state)
+        for j in range(NV):
+            cold_call(j)
+        torch.cuda.synchronize()
+        KC = min(K, 240)
+        cs = [torch.cuda.Event(enable_timing=True) for _ in range(KC)]
+        ce = [torch.cuda.Event(enable_timing=True) for _ in range(KC)]
+        chost = []
+        for i in range(KC):
+            flush.zero_()
+            cs[i].record(stream)
+            t_h = time.perf_counter()
+            cold_call(i % NV)
+            chost.append((time.perf_counter() - t_h) * 1e6)
+            ce[i].record(stream)
+        torch.cuda.synchronize()
+        spanla.span_la_check()
+        cms = statistics.mean(a.elapsed_time(b) for a, b in zip(cs, ce))
+        cold = {"cold_plan_ms_per_step": cms, "cold_plan_host_us": statistics.median(chost),
+                "cold_plan_value": rows_per_step / (cms / 1e3), "variants": NV, "steps": KC,
+                "mode": "branch lengths permuted within each parent's run of branches: a new "
+                        "plan (host build + descriptor upload) in every step"}
+
+    # Long request: the view pass alone, and the 4 shards run concurrently on
+    # 4 streams, or as one call over all branches, beside the serial shards.
+    long_req = None
+    if shards_mode:
+        def timed(fn, reps):
+            a_ = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+            b_ = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+            for i in range(reps):
+                flush.zero_()
+                a_[i].record(stream)
+                fn()
+                b_[i].record(stream)
+            torch.cuda.synchronize()
+            spanla.span_la_check()
+            return statistics.mean(x.elapsed_time(y) for x, y in zip(a_, b_)) * 1e3
+        vstate = torch.empty((1, w.H, 64, 64), dtype=torch.float32, device=dev)
+        side = [torch.cuda.Stream(device=dev) for _ in range(4)]
+
+        def shards_4_streams():
+            go = torch.cuda.Event()
+            go.record(stream)
+            done = []
+            for strm, cu, par in zip(side, shard_cu, shard_par):
+                strm.wait_event(go)
+                spanla.span_la_branches_from_state(cached, q, k, v, cu, par, out=out, stream=strm)
+                ev = torch.cuda.Event()
+                ev.record(strm)
+                done.append(ev)
+            for ev in done:
+                stream.wait_event(ev)
+
+        all_par = np.zeros(w.B, np.int32)
+        reps = min(K, 200)
+        for fn in (shards_4_streams,):
+            fn()
+        long_req = {
+            "view_pass_us": timed(lambda: spanla.span_la_pass(q, k, v, w.view_cu, [], [], out=out,
+                                                              view_state_out=vstate), reps),
+            "shards_serial_us": ms * 1e3,
+            "shards_4_streams_us": timed(shards_4_streams, reps),
+            "one_call_256_branches_us": timed(lambda: spanla.span_la_branches_from_state(
+                cached, q, k, v, w.branch_cu, all_par, out=out), reps),
+            "view_rows": int(w.view_lens.sum()), "branch_rows": rows_per_step}
 
     # End to end through the public API with host buffers: every step copies
     # its q, k, v from pinned host memory, runs the call and reads out and the
@@ -924,7 +1063,9 @@ def main():
                 "step_ms_min": min(step_ms),
                 "host_enqueue_us": statistics.median(host_us),
                 "graph_us_per_step": graph_us,
-                "warm_l2_us_per_step": warm_us}
+                "warm_l2_us_per_step": warm_us,
+                "cold_plan": cold,
+                "long_request": long_req}
         print(json.dumps(line))
     if pg:
         pg.barrier()

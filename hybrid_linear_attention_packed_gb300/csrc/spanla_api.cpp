@@ -394,6 +394,7 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
     int ntiles;
   };
   std::vector<Block> blocks;
+  blocks.reserve(static_cast<size_t>(H) * (V + groups.size()));
   int64_t W = 0;
   for (int h = 0; h < H; ++h) {
     for (size_t r = 0; r < requests.size(); ++r) {
@@ -456,19 +457,23 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
     plan.cta_begin[c + 1] = plan.cta_begin[c] + static_cast<int32_t>(run_len(c));
     plan.run_tiles = std::max<int>(plan.run_tiles, static_cast<int>(run_len(c)));
   }
-  plan.work.assign(W, WorkTile{});
+  plan.work.resize(W);
 
   std::vector<SpanDesc> pieces;   // in creation order
   std::vector<int> piece_cta;      // output CTA of each piece
+  pieces.reserve(blocks.size() + grid);
+  piece_cta.reserve(blocks.size() + grid);
   int64_t g0 = 0;
+  std::vector<std::pair<int, int>> pr;   // a block's pieces: local tile ranges [j0, j1)
+  std::vector<int> pcta;                 // and their CTAs
   for (const Block& bk : blocks) {
     if (bk.kind == 0 && bk.ntiles == 0) {   // empty view: zero final state
       plan.scan.push_back({0, 0, bk.id, bk.head});
       continue;
     }
     // The block's pieces: [g0, g0 + ntiles) split at the run boundaries.
-    std::vector<std::pair<int, int>> pr;   // local tile ranges [j0, j1)
-    std::vector<int> pcta;
+    pr.clear();
+    pcta.clear();
     {
       int64_t a = g0;
       const int64_t end = g0 + bk.ntiles;
@@ -496,26 +501,28 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
       const int32_t sA = bk.kind == 0 ? -1 : groups[bk.id].parent;
       const int32_t sB = (slots && k > 0) ? slot0 + static_cast<int32_t>(k) : -1;
       ++plan.n_pieces;
+      // CTA c's run is contiguous in the head-major order
+      WorkTile* dst = plan.work.data() + plan.cta_begin[c] + (g0 + j0 - run_start(c));
+      WorkTile w{};
+      w.head = bk.head;
+      w.stateA = sA;
+      w.stateB = sB;
+      if (bk.kind == 2) {
+        const BranchGroup& bg = groups[bk.id];
+        w.bound0 = bg.bound0;
+        w.nbound = bg.nbound;
+        for (int q = 0; q < kInlineBounds && q < bg.nbound; ++q) w.inl[q] = plan.bounds[bg.bound0 + q];
+      } else {
+        w.bound0 = 0;
+        w.nbound = 1;
+      }
+      const int32_t init = (sA >= 0 || sB >= 0) ? kTileHasInit : 0;
       for (int j = j0; j < j1; ++j) {
-        WorkTile w{};
-        w.row0 = static_cast<int32_t>(bk.row0 + static_cast<int64_t>(j) * kTileRows);
-        w.nrows = static_cast<int32_t>(std::min<int64_t>(kTileRows, bk.len - static_cast<int64_t>(j) * kTileRows));
-        w.head = bk.head;
-        w.flags = (j == j0 ? kTileFirst : 0) | (j + 1 == j1 ? kTileLast : 0) |
-                  ((sA >= 0 || sB >= 0) ? kTileHasInit : 0);
-        w.stateA = sA;
-        w.stateB = sB;
-        if (bk.kind == 2) {
-          const BranchGroup& bg = groups[bk.id];
-          w.bound0 = bg.bound0;
-          w.nbound = bg.nbound;
-          for (int q = 0; q < kInlineBounds && q < bg.nbound; ++q) w.inl[q] = plan.bounds[bg.bound0 + q];
-        } else {
-          w.bound0 = 0;
-          w.nbound = 1;
-        }
-        // position in CTA c's list: its run is contiguous in the head-major order
-        plan.work[plan.cta_begin[c] + (g0 + j - run_start(c))] = w;
+        const int64_t r = static_cast<int64_t>(j) * kTileRows;
+        w.row0 = static_cast<int32_t>(bk.row0 + r);
+        w.nrows = static_cast<int32_t>(std::min<int64_t>(kTileRows, bk.len - r));
+        w.flags = (j == j0 ? kTileFirst : 0) | (j + 1 == j1 ? kTileLast : 0) | init;
+        dst[j - j0] = w;
       }
     }
     g0 += bk.ntiles;
@@ -526,39 +533,41 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
   // pieces are dealt longest first onto the least-loaded CTA.
   const int64_t n_sp = static_cast<int64_t>(pieces.size());
   if (n_sp > 0) {
-    std::vector<std::vector<int64_t>> per_cta;
+    std::vector<int32_t> owner(n_sp);   // span_state CTA of each piece
+    int sgrid = 0;
     if (n_sp <= sms && grid <= sms) {
-      per_cta.resize(grid);
-      for (int64_t u = 0; u < n_sp; ++u) per_cta[piece_cta[u]].push_back(u);
-      // drop CTAs without pieces
-      per_cta.erase(std::remove_if(per_cta.begin(), per_cta.end(),
-                                   [](const std::vector<int64_t>& v) { return v.empty(); }),
-                    per_cta.end());
+      // CTAs that have pieces, numbered in output-CTA order
+      std::vector<int32_t> remap(grid, -1);
+      for (int64_t u = 0; u < n_sp; ++u) remap[piece_cta[u]] = 1;
+      for (int c = 0; c < grid; ++c) remap[c] = remap[c] > 0 ? sgrid++ : -1;
+      for (int64_t u = 0; u < n_sp; ++u) owner[u] = remap[piece_cta[u]];
     } else {
-      const int sgrid = static_cast<int>(std::min<int64_t>(n_sp, sms));
+      sgrid = static_cast<int>(std::min<int64_t>(n_sp, sms));
       std::vector<int64_t> order(n_sp);
       for (int64_t u = 0; u < n_sp; ++u) order[u] = u;
       std::stable_sort(order.begin(), order.end(),
                        [&](int64_t a, int64_t b) { return pieces[a].len > pieces[b].len; });
       using Slot = std::pair<int64_t, int>;   // (rows assigned, cta)
-      std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+      std::vector<Slot> heap_store;
+      heap_store.reserve(sgrid);
+      std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap(std::greater<Slot>(),
+                                                                          std::move(heap_store));
       for (int c = 0; c < sgrid; ++c) heap.push({0, c});
-      per_cta.resize(sgrid);
       for (int64_t u : order) {
         Slot sl = heap.top();
         heap.pop();
-        per_cta[sl.second].push_back(u);
+        owner[u] = sl.second;
         sl.first += pieces[u].len;
         heap.push(sl);
       }
     }
-    const int sgrid = static_cast<int>(per_cta.size());
+    // counting sort of the pieces by owner, keeping creation order within a CTA
     plan.span_begin.assign(sgrid + 1, 0);
-    for (int c = 0; c < sgrid; ++c) {
-      plan.span_begin[c] = static_cast<int32_t>(plan.spans.size());
-      for (int64_t u : per_cta[c]) plan.spans.push_back(pieces[u]);
-    }
-    plan.span_begin[sgrid] = static_cast<int32_t>(plan.spans.size());
+    for (int64_t u = 0; u < n_sp; ++u) ++plan.span_begin[owner[u] + 1];
+    for (int c = 0; c < sgrid; ++c) plan.span_begin[c + 1] += plan.span_begin[c];
+    plan.spans.resize(n_sp);
+    std::vector<int32_t> fill(plan.span_begin.begin(), plan.span_begin.end() - 1);
+    for (int64_t u = 0; u < n_sp; ++u) plan.spans[fill[owner[u]]++] = pieces[u];
   }
   return plan;
 }
@@ -598,6 +607,9 @@ size_t put(std::vector<uint8_t>& host, const std::vector<T>& v) {
   return off;
 }
 
+template <typename T>
+size_t bytes_of(const std::vector<T>& v) { return align256(v.size() * sizeof(T)); }
+
 // 3-D view (d, token, head) of a [T][H][64] bf16 array; box = {64, rows, heads}.
 span_la_status encode_map(CUtensorMap* map, const void* base, int64_t T, int H, int box_rows,
                           int box_heads) {
@@ -632,6 +644,8 @@ struct DescBlock {
 DescBlock make_desc(const Plan& plan, int H) {
   DescBlock d;
   d.span_mode = plan.span_mode;
+  d.host.reserve(bytes_of(plan.scan) + bytes_of(plan.bounds) + bytes_of(plan.spans) + bytes_of(plan.span_begin) +
+                 bytes_of(plan.work) + bytes_of(plan.cta_begin) + bytes_of(plan.chunks) + bytes_of(plan.tiles));
   d.off_scan = put(d.host, plan.scan);
   d.off_bounds = put(d.host, plan.bounds);
   if (plan.span_mode) {

@@ -49,3 +49,28 @@ def test_error_measure_of_the_cpu_baseline_leg():
     ref = np.array([[1.0, -4.0], [2.0, 0.5]])
     assert bench.max_rel_err(ref + np.array([[0.0, 0.4], [0.0, 0.0]]), ref) == pytest.approx(0.1)
     assert bench.max_rel_err(np.zeros((0, 2)), np.zeros((0, 2))) == 0.0
+
+
+def test_reference_arm_config_matches_the_gpu_arm_keys():
+    """Both arms name the workload with the same config keys (the GPU arm adds
+    no key the reference arm lacks)."""
+    d = _run("--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "1")
+    assert d["config"]["parallelism"] == "dp1"
+
+
+def test_branch_variants_for_the_cold_plan_leg():
+    """The cold-plan leg's metadata variants cover the same rows with the same
+    parents and views, and cut the branches differently (fresh plans)."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    from hybrid_linear_attention_packed_gb300 import workloads
+    w = workloads.single_request(0)
+    vs = bench.branch_variants(w, 24)
+    seen = set()
+    for cu, par in vs:
+        assert cu[0] == w.branch_cu[0] and cu[-1] == w.branch_cu[-1]
+        assert np.array_equal(par, w.branch_parent)
+        assert sorted(np.diff(cu).tolist()) == sorted(w.branch_lens.tolist())
+        seen.add(tuple(cu.tolist()))
+    assert len(seen) > 16   # more distinct plans than the plan cache holds

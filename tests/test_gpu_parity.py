@@ -213,3 +213,13 @@ def test_packed_pass_equals_one_pass_per_request(cuda_device):
     print("shared %.2e, per request %.2e, between %.2e, states %.2e" % (e_shared, e_alone, e_pair, e_state))
     assert max(e_shared, e_alone, e_pair, e_state) <= TOL["bf16"]
     assert torch.isnan(alone[torch.from_numpy(~seg).to(cuda_device)]).all()
+
+
+def test_fp32_at_single_request_size(cuda_device):
+    """fp32 inputs at the 7,400-token pass's size: 16 heads, one 7,400-row view
+    and the same 8 branches, q, k ~ N(0,1)/8, v ~ N(0,1), so the fp32 path's
+    chunk-state and tile-output kernels run on a full-size grid; within 1e-3."""
+    w0 = workloads.single_request(0)
+    w = workloads.make_pass(w0.view_lens, w0.branch_lens, w0.branch_parent, H=16, dtype="f32",
+                            seed=7, name="single request, fp32 inputs")
+    _check_full(w, cuda_device)
