@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--per-request", action="store_true",
                     help="run each request of the workload (a view and its branches) as its own "
                          "pass instead of one shared pass (the page's shared-branch-pass lever)")
+    ap.add_argument("--pass-variant", choices=["one", "three"], default="one",
+                    help="bf16 pass structure: one cooperative launch (default) or span state -> "
+                         "scan -> output in three launches")
     ap.add_argument("--layer", choices=["linear", "softmax"], default="linear",
                     help="linear: the packed linear-attention pass (default); softmax: the "
                          "hybrid model's softmax-attention layer over the same packed rows")
@@ -341,6 +344,8 @@ def workload_config(w, name: str) -> dict:
 
 
 def add_mode(cfg: dict, args) -> dict:
+    cfg = dict(cfg, **{"pass": "three launches" if getattr(args, "pass_variant", "one") == "three"
+                       else "one launch"})
     if getattr(args, "cache", False) and args.workload == "cached_long":
         cfg = dict(cfg, step="span_la_cache_branches by key over the view-state cache, 4 shards of "
                              "64 branches; tokens/s counts branch rows")
@@ -614,6 +619,8 @@ def main():
     if pg:
         pg.barrier()
     from hybrid_linear_attention_packed_gb300 import sharding, spanla, workloads
+    spanla.set_pass_variant(spanla.PASS_THREE_LAUNCHES if args.pass_variant == "three"
+                            else spanla.PASS_ONE_LAUNCH)
 
     # Weak scaling: every rank runs its own pass (independent requests).
     w = workloads.by_name(args.workload, args.seed + rank)

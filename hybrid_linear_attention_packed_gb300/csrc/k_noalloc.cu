@@ -16,11 +16,14 @@
 namespace spanla {
 namespace {
 
-// Largest workspace a no-allocation pass may use: descriptors plus one fp32
-// 64x64 state per piece (16 KiB each), i.e. about a thousand pieces.  A
-// piece is the part of one view-head (or long-branch-head) inside one CTA's
-// run of the output kernel, so a pass needs at most about (views + SMs) x
-// heads of them: a 7,400-token 16-head pass needs about 170.
+// Largest workspace a no-allocation pass may use: descriptors (64 bytes per
+// output tile) plus the fp32 64x64 workspace states (16 KiB each).  A piece
+// is the part of one view-head (or long-branch-head) inside one CTA's run of
+// the output kernel.  The one-launch structure keeps a state only for a piece
+// whose state another CTA needs (at most one per boundary between runs), so
+// there the descriptors set the limit (about 200,000 tiles); the three-launch
+// structure keeps one per piece, at most about (views + SMs) x heads of them
+// (a 7,400-token 16-head pass needs about 170, the array about a thousand).
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 // Error word of the no-allocation path's kernels (bounded waits that ran out).
 static __device__ unsigned g_noalloc_err;

@@ -1,29 +1,45 @@
 // Span-output kernel (bf16 inputs): the output of every view row and every
-// branch row, carrying the state across the tiles of a piece.
+// branch row, carrying the state across the tiles of a piece -- and, as the
+// one-launch pass, the piece states and the prefix sums as well.
 //
 // "Serving 0.88M TPS from Two RTXs and Mac Minis", section "Kernels" (each
 // 64-token chunk: a masked Q K^T times V inside the chunk plus Q times the
-// state entering it; shared branch passes with the small kernels fused) and
-// section "The Workload" (branches attend to the view, not to each other).
+// state entering it; one scan per pass; shared branch passes with the small
+// kernels fused) and section "The Workload" (branches attend to the view, not
+// to each other).
 //
 // Each CTA runs one contiguous run of (tile, head) work from a host-built
 // list.  A piece is the part of one view-head or long-branch-head inside the
 // run; a tile of packed short branches is a piece of its own.  With S the
-// state entering a tile (the piece's start state stateA[a] + stateB[b] for
-// its first tile: the scan prefix and/or the parent view's final state -- the
-// branch fork), every row i of the tile gets
+// state entering a tile (the piece's start state for its first tile), every
+// row i of the tile gets
 //
 //     o_i = sum_{start(i) <= j <= i} (q_i . k_j) v_j  +  S^T q_i ,
 //
 // and the next tile of the piece starts from S + K^T V of this one.
 //
+// Start states.  With three launches (span_state -> scan -> this kernel) a
+// piece's start state is one scanned prefix slot plus, for branches, the
+// parent view's final state written by the scan.  In the one-launch pass
+// (fused) this kernel first sums K^T V over its own pieces whose state other
+// CTAs need (phase 1, written to workspace slots), counts itself in a global
+// counter, and a CTA whose pieces start from other CTAs' states waits until
+// every phase-1 CTA has counted itself (the grid is launched cooperatively,
+// so every CTA is resident) and sums those slots itself: no scan.  The CTA
+// that holds the last tile of a view-head computes the view's final state
+// on chip (K^T V of that tile added to the running state), writes it out and
+// starts that view's following branch tiles in its run from it directly.
+//
 // Software pipelined over consecutive tiles t.  15 warps:
-//   warp 0     producer: Q, K, V tiles by TMA into a four-stage ring.
+//   warp 0     producer: phase-1 K, V tiles, then Q, K, V tiles by TMA into
+//              a four-stage ring.
 //   warp 1     front issuer (one lane; the warp zeroes partial-tile K/V
-//              rows), as soon as tile t has landed:  P(t) = Q K^T  (M128
-//              N128 K64) into TMEM buffer t & 1, then, unless t ends its
-//              piece, the tile's own state  dS(t) = K^T V  (M128 N64 K128)
-//              into TMEM region t & 1.
+//              rows): phase 1, K^T V summed over each phase-1 piece into a
+//              TMEM region; then per tile, as soon as it has landed,
+//              P(t) = Q K^T  (M128 N128 K64) into TMEM buffer t & 1, then,
+//              unless t ends its piece (or when it ends a view-head), the
+//              tile's own state  dS(t) = K^T V  (M128 N64 K128) into TMEM
+//              region t & 1.
 //   warp 2     O issuer (one lane): once the P conversion has turned P(t)
 //              into bf16 in place,  O(t) = P(t) V  (M128 N64 K128, P read
 //              from tensor memory), then, with S(t) staged,  O(t) += Q S_hi +
@@ -35,16 +51,15 @@
 //              in tensor memory -- 64 fp32 columns become 64 bf16 in the half's
 //              first 32 columns (P V reads keys 0..63 from columns 0..31 and
 //              keys 64..127 from columns 64..95).
-//   warps 11-14 state and output, one warp per lane quarter.  They hold the
-//              running fp32 state in registers (a 32-column half of one state
-//              row per thread); per step t they add dS(t) to it (or load the
-//              next piece's start state, fetched a tile ahead), stage S(t+1)
-//              as bf16 high / low parts for Q S, and then store O(t).
-// No tensor-core work waits on the state warps' arithmetic except Q S, and
-// the state chain runs through registers only, so the tensor pipe sees the
-// MMAs of consecutive tiles back to back.  K^T V runs with M = 128 and the K
-// tile as both 64-wide M atoms, so TMEM lanes 64..127 hold a copy of dS rows
-// 0..63: the lower copy is read for columns 0..31, the upper for 32..63.
+//   warps 11-14 state and output, one warp per lane quarter.  Phase 1: the
+//              piece states out of TMEM into the workspace.  Then they hold
+//              the running fp32 state in registers (a 32-column half of one
+//              state row per thread); per step t they add dS(t) to it (or load
+//              the next piece's start state), stage S(t+1) as bf16 high / low
+//              parts for Q S, and then store O(t).
+// K^T V runs with M = 128 and the K tile as both 64-wide M atoms, so TMEM
+// lanes 64..127 hold a copy of rows 0..63: the lower copy is read for
+// columns 0..31, the upper for 32..63.
 #include "spanla_internal.h"
 #include "tc_ptx.cuh"
 
@@ -56,34 +71,60 @@ constexpr int kGroupWarps = 4;                           // state and output
 constexpr int kGroupThreads = 32 * kGroupWarps;
 constexpr int kConvWarps = 8;                            // P conversion
 constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kStateWarp0 = 3 + kConvWarps;              // first state/output warp
 constexpr int kStages = 4;
 constexpr uint32_t kRowTileBytes = kTileRows * 128;        // 128 rows x 128 B
 constexpr uint32_t kStageBytes = 3 * kRowTileBytes;       // Q K V
 constexpr uint32_t kStateTileBytes = kHeadDim * 128;       // 64 rows x 128 B (bf16)
 constexpr uint32_t kSOpBytes = 2 * kStateTileBytes;         // S as bf16 hi + lo
 constexpr int kCoordSlots = 64;                              // tile coordinates staged for the producer
+constexpr int kP1Slots = 32;                                 // phase-1 piece records staged
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: P buffers (128 each), O buffers (64 each), dS regions (64 each).
 constexpr uint32_t kColP0 = 0, kColP1 = 128, kColO0 = 256, kColO1 = 320, kColD0 = 384, kColD1 = 448;
+constexpr uint32_t kNamedStateBar = 1;                       // bar.sync id of the state warps
 
 struct OutSmem {
   static constexpr uint32_t kStage0 = 0;
   static constexpr uint32_t kQ = 0, kK = kRowTileBytes, kV = 2 * kRowTileBytes;
   static constexpr uint32_t kS = kStages * kStageBytes;          // two S operands (hi, lo)
   static constexpr uint32_t kBar = kS + 2 * kSOpBytes;
-  // barrier slots (8 bytes each); the pairs are used by alternate tiles.
-  // Empty takes two arrivals per tile: the front issuer's MMAs and the O
-  // issuer's MMAs both read the stage.
+  // barrier slots (8 bytes each); the pairs are used by alternate tiles (or
+  // phase-1 pieces).  Empty takes two arrivals per use: the front issuer's
+  // and the O issuer's MMAs both read a tile's stage (the front issuer
+  // arrives twice on a phase-1 stage).
   static constexpr int kFull = 0, kEmpty = kStages, kPReady = 2 * kStages,
                        kPDone = kPReady + 2, kOReady = kPReady + 4, kOFree = kPReady + 6,
                        kSSmem = kPReady + 8, kDReady = kPReady + 10, kDFree = kPReady + 12,
-                       kNumBars = kPReady + 14;
+                       kP1Ready = kPReady + 14, kP1Free = kPReady + 16, kP1Done = kPReady + 18,
+                       kNumBars = kPReady + 19;
   static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
+  static constexpr uint32_t kN1 = kTmemSlot + 4;                  // phase-1 tiles of this CTA
   static constexpr uint32_t kCoord = kTmemSlot + 8;              // (row0, head) of the first tiles
-  static constexpr uint32_t kBytes = kCoord + 8 * kCoordSlots;
+  static constexpr uint32_t kP1 = kCoord + 8 * kCoordSlots;      // phase-1 piece records
+  static constexpr uint32_t kBytes = kP1 + sizeof(SpanDesc) * kP1Slots;
   static constexpr uint32_t kRequest = kBytes + 1024;
 };
 static_assert(OutSmem::kRequest <= 227 * 1024, "shared memory budget");
+
+// Kernel parameters besides the tensor maps (see SpanOutputArgs).
+struct OutParams {
+  const WorkTile* work;
+  const int32_t* cta_begin;
+  const uint8_t* bounds;
+  const float* stateA;
+  float* ws;
+  float* final_out;
+  __nv_bfloat16* out;
+  unsigned* err;
+  const SpanDesc* p1;
+  const int32_t* p1_begin;
+  unsigned* counter;
+  int a_rows;
+  int H;
+  int fused;
+  int n_p1_ctas;
+};
 
 __device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity, unsigned* err,
                                              unsigned code) {
@@ -92,14 +133,39 @@ __device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity, unsi
   return false;
 }
 
-__device__ __forceinline__ WorkTile load_tile(const WorkTile* p) {
-  WorkTile t;
-  const uint4* src = reinterpret_cast<const uint4*>(p);
-  uint4* dst = reinterpret_cast<uint4*>(&t);
-  dst[0] = __ldg(src);
-  dst[1] = __ldg(src + 1);
-  dst[2] = __ldg(src + 2);
-  return t;
+// The parts of a tile record each role reads (fewer registers per role).
+struct TileHead {     // row0, nrows, head, flags
+  int32_t row0, nrows, head, flags;
+};
+struct TileState {    // ... and the start-state recipe
+  int32_t row0, nrows, head, flags, stateA, stateB, a_n, b_n, final_idx;
+};
+struct TileMask {     // rows and segment starts (P conversion)
+  int32_t nrows, bound0, nbound;
+  uint4 inl;
+};
+
+__device__ __forceinline__ TileHead load_head(const WorkTile* p) {
+  const int4 a = __ldg(reinterpret_cast<const int4*>(p));
+  return TileHead{a.x, a.y, a.z, a.w};
+}
+
+__device__ __forceinline__ TileState load_state(const WorkTile* p) {
+  const int4 a = __ldg(reinterpret_cast<const int4*>(p));
+  const int4 b = __ldg(reinterpret_cast<const int4*>(p) + 1);
+  const int32_t f = __ldg(&p->final_idx);
+  return TileState{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, f};
+}
+
+__device__ __forceinline__ TileMask load_mask(const WorkTile* p) {
+  const int4 c = __ldg(reinterpret_cast<const int4*>(p) + 2);
+  const uint4 d = __ldg(reinterpret_cast<const uint4*>(p) + 3);
+  return TileMask{__ldg(&p->nrows), c.y, c.z, d};
+}
+
+__device__ __forceinline__ int inline_bound(const uint4& v, int q) {
+  const uint32_t w = q < 4 ? v.x : q < 8 ? v.y : q < 12 ? v.z : v.w;
+  return static_cast<int>((w >> (8 * (q & 3))) & 0xffu);
 }
 
 // Write 32 state values (columns 32*half ..) of row d as bf16 high / low parts
@@ -122,17 +188,29 @@ __device__ __forceinline__ void stage_state_half_row(uint8_t* s_op, int d, int h
   }
 }
 
+// 32 fp32 values (one half-row of a state) to global memory.
+__device__ __forceinline__ void store_half_row(float* dst, const float* x) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) d4[c] = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const WorkTile* __restrict__ work,
-                   const int32_t* __restrict__ cta_begin, const uint8_t* __restrict__ bounds,
-                   const float* __restrict__ stateA, const float* __restrict__ stateB,
-                   __nv_bfloat16* __restrict__ out, int H, unsigned* __restrict__ err) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ OutParams prm) {
   using L = OutSmem;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
+  const int H = prm.H;
+  unsigned* err = prm.err;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -153,7 +231,10 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_init(bar(L::kSSmem + b), kGroupThreads);
       mbar_init(bar(L::kDReady + b), 1);
       mbar_init(bar(L::kDFree + b), kGroupThreads);
+      mbar_init(bar(L::kP1Ready + b), 1);
+      mbar_init(bar(L::kP1Free + b), kGroupThreads);
     }
+    mbar_init(bar(L::kP1Done), kGroupThreads);
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -163,16 +244,33 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   // The schedule comes from a copy that completed before the first kernel of
   // the pass began, and Q, K, V from before that: every role but the one that
   // reads the start states runs ahead of the previous kernel's completion.
-  const int i_begin = cta_begin[blockIdx.x];
-  const int n = cta_begin[blockIdx.x + 1] - i_begin;
-  const WorkTile* list = work + i_begin;
+  const int i_begin = prm.cta_begin[blockIdx.x];
+  const int n = prm.cta_begin[blockIdx.x + 1] - i_begin;
+  const WorkTile* list = prm.work + i_begin;
+  // Phase-1 pieces of this CTA (one-launch pass only).
+  const int p1_begin = prm.fused ? prm.p1_begin[blockIdx.x] : 0;
+  const int n_p1 = prm.fused ? prm.p1_begin[blockIdx.x + 1] - p1_begin : 0;
+  const SpanDesc* p1 = prm.p1 + p1_begin;
   int2* coord = reinterpret_cast<int2*>(smem + L::kCoord);
-  // The producer's tile coordinates: loads issued before the CTA-wide set-up
-  // completes, so their latency overlaps it.
-  int2 c_lo = make_int2(0, 0), c_hi = make_int2(0, 0);
+  SpanDesc* p1s = reinterpret_cast<SpanDesc*>(smem + L::kP1);
+  // Warp 0 stages the producer's tile coordinates and the phase-1 pieces
+  // (loads issued before the CTA-wide set-up completes, so their latency
+  // overlaps it) and counts the phase-1 tiles.
   if (warp == 0) {
+    int2 c_lo = make_int2(0, 0), c_hi = make_int2(0, 0);
     if (lane < n) c_lo = make_int2(list[lane].row0, list[lane].head);
     if (lane + 32 < n && lane + 32 < kCoordSlots) c_hi = make_int2(list[lane + 32].row0, list[lane + 32].head);
+    int tiles1 = 0;
+    for (int j = lane; j < n_p1; j += 32) {
+      const SpanDesc sd = p1[j];
+      if (j < kP1Slots) p1s[j] = sd;
+      tiles1 += (sd.len + kTileRows - 1) / kTileRows;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tiles1 += __shfl_xor_sync(0xffffffffu, tiles1, o);
+    if (lane < n) coord[lane] = c_lo;
+    if (lane + 32 < n && lane + 32 < kCoordSlots) coord[lane + 32] = c_hi;
+    if (lane == 0) *reinterpret_cast<int*>(smem + L::kN1) = tiles1;
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -182,20 +280,29 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  const int n1 = *reinterpret_cast<const int*>(smem + L::kN1);   // phase-1 tiles
+  auto p1_of = [&](int j) { return j < kP1Slots ? p1s[j] : p1[j]; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane < n) coord[lane] = c_lo;
-    if (lane + 32 < n && lane + 32 < kCoordSlots) coord[lane + 32] = c_hi;
-    __syncwarp();
     if (lane == 0) {
       bool ok = true;
-      int i = 0;
-      for (; i < n; ++i) {
+      int u = 0;   // load index: phase-1 tiles, then the run's tiles
+      for (int j = 0; j < n_p1 && ok; ++j) {
+        const SpanDesc sd = p1_of(j);
+        for (int r = 0; r < sd.len && ok; r += kTileRows, ++u) {
+          const int s = u % kStages;
+          if (!wait_or_flag(bar(L::kEmpty + s), ((u / kStages) & 1) ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
+          const uint32_t st = base + L::kStage0 + s * kStageBytes;
+          mbar_arrive_expect_tx(bar(L::kFull + s), 2 * kRowTileBytes);
+          tma_load_3d(st + L::kK, &tm_k, bar(L::kFull + s), 0, sd.row0 + r, sd.head);
+          tma_load_3d(st + L::kV, &tm_v, bar(L::kFull + s), 0, sd.row0 + r, sd.head);
+        }
+      }
+      for (int i = 0; i < n && ok; ++i, ++u) {
         const int2 rc = i < kCoordSlots ? coord[i] : make_int2(list[i].row0, list[i].head);
-        const int s = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        if (!wait_or_flag(bar(L::kEmpty + s), ph ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
+        const int s = u % kStages;
+        if (!wait_or_flag(bar(L::kEmpty + s), ((u / kStages) & 1) ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
         const uint32_t st = base + L::kStage0 + s * kStageBytes;
         mbar_arrive_expect_tx(bar(L::kFull + s), kStageBytes);
         tma_load_3d(st + L::kQ, &tm_q, bar(L::kFull + s), 0, rc.x, rc.y);
@@ -203,38 +310,73 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tma_load_3d(st + L::kV, &tm_v, bar(L::kFull + s), 0, rc.x, rc.y);
       }
       // Wait (bounded) for the last loads to land before the CTA can exit.
-      for (int u = (i > kStages ? i - kStages : 0); u < i; ++u)
-        mbar_wait_bounded(bar(L::kFull + u % kStages), (u / kStages) & 1, ok ? kWaitLimitNs : 1000000ull);
+      for (int w = (u > kStages ? u - kStages : 0); w < u; ++w)
+        mbar_wait_bounded(bar(L::kFull + w % kStages), (w / kStages) & 1, ok ? kWaitLimitNs : 1000000ull);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ front issuer
     constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, 0, 0);
     constexpr uint32_t id_kv = idesc_bf16_f32(128, 64, 1, 1);
-    WorkTile nxt = n > 0 ? load_tile(list) : WorkTile{};
-    for (int i = 0; i < n; ++i) {
-      const WorkTile r = nxt;
-      if (i + 1 < n) nxt = load_tile(list + i + 1);
-      const int s = i % kStages, b = i & 1;
-      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kFull + s), (i / kStages) & 1, err, kErrTimeoutTma)))
+    bool ok = true;
+    int u = 0;
+    // Zero K and V rows past `rows` in a stage (they may hold anything, even
+    // NaN, or rows of another segment).
+    auto zero_tail = [&](uint32_t st, int rows) {
+      if (rows >= kTileRows) return;
+      uint8_t* vrow = smem + (st + L::kV - base);
+      uint8_t* krow = smem + (st + L::kK - base);
+      for (int q = rows * 8 + lane; q < kTileRows * 8; q += 32) {
+        *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(krow + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+    };
+    // Phase 1: K^T V summed over each piece into TMEM region j & 1.
+    for (int j = 0; j < n_p1 && ok; ++j) {
+      const SpanDesc sd = p1_of(j);
+      const int b = j & 1;
+      if (j >= 2) ok = wait_or_flag(bar(L::kP1Free + b), ((j - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      for (int r = 0; r < sd.len; r += kTileRows, ++u) {
+        const int s = u % kStages;
+        ok = wait_or_flag(bar(L::kFull + s), (u / kStages) & 1, err, kErrTimeoutTma);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const uint32_t st = base + L::kStage0 + s * kStageBytes;
+        zero_tail(st, sd.len - r);
+        __syncwarp();
+        tc_fence_after_sync();
+        if (lane == 0) {
+          const uint32_t colD = b ? kColD1 : kColD0;
+          for (int kk = 0; kk < kTileRows / 16; ++kk)
+            mma_bf16(tmem + colD, smem_desc_sw128(st + L::kK + kk * 2048, 0, 1024),
+                     smem_desc_sw128(st + L::kV + kk * 2048, kRowTileBytes, 1024), id_kv,
+                     (r > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(L::kEmpty + s));
+          mma_commit(bar(L::kEmpty + s));
+          if (r + kTileRows >= sd.len) mma_commit(bar(L::kP1Ready + b));
+        }
+        __syncwarp();
+      }
+    }
+    // The dS regions take the run's tiles once phase 1 has been read out.
+    if (ok && n_p1 > 0) ok = wait_or_flag(bar(L::kP1Done), 0, err, kErrTimeoutMma);
+    ok = __all_sync(0xffffffffu, ok);
+    TileHead nxt = (ok && n > 0) ? load_head(list) : TileHead{};
+    for (int i = 0; i < n && ok; ++i, ++u) {
+      const TileHead r = nxt;
+      if (i + 1 < n) nxt = load_head(list + i + 1);
+      const int s = u % kStages, b = i & 1;
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kFull + s), (u / kStages) & 1, err, kErrTimeoutTma)))
         break;
       const uint32_t st = base + L::kStage0 + s * kStageBytes;
-      if (r.nrows < kTileRows) {
-        // K and V rows past the tile may hold anything, even NaN; zero them so
-        // masked P entries multiply zeros.  (A partial tile is the last of its
-        // piece, so no state update reads them.)
-        uint8_t* vrow = smem + (st + L::kV - base);
-        uint8_t* krow = smem + (st + L::kK - base);
-        for (int q = r.nrows * 8 + lane; q < kTileRows * 8; q += 32) {
-          *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(krow + q * 16) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-      }
+      // (A partial tile is the last of its piece: no state update reads its
+      // tail, and a view-head's last tile sums only its own rows.)
+      zero_tail(st, r.nrows);
       __syncwarp();
       // P buffer b is free once P V of tile i-2 (which read it) has completed.
-      bool ok = true;
-      if (i >= 2) ok = wait_or_flag(bar(L::kOReady + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      bool ok2 = true;
+      if (i >= 2) ok2 = wait_or_flag(bar(L::kOReady + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (!__all_sync(0xffffffffu, ok2)) break;
       tc_fence_after_sync();
       if (lane == 0) {
         const uint32_t colP = b ? kColP1 : kColP0;
@@ -245,11 +387,11 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       }
       __syncwarp();
       // dS region b is free once the state warps have read dS(i-2).
-      if (i >= 2) ok = wait_or_flag(bar(L::kDFree + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (i >= 2) ok2 = wait_or_flag(bar(L::kDFree + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (!__all_sync(0xffffffffu, ok2)) break;
       tc_fence_after_sync();
       if (lane == 0) {
-        if (!(r.flags & kTileLast)) {
+        if (!(r.flags & kTileLast) || (r.flags & kTileFinalOut)) {
           // A = [K | K]^T (both 64-wide M atoms read the K tile: leading byte
           // offset 0), so TMEM lanes 64..127 hold a second copy of rows 0..63.
           const uint32_t colD = b ? kColD1 : kColD0;
@@ -265,11 +407,12 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   } else if (warp == 2) {
     // ------------------------------------------------------------ O issuer
     constexpr uint32_t id_n64_b_mn = idesc_bf16_f32(128, 64, 0, 1);
-    WorkTile nxt = n > 0 ? load_tile(list) : WorkTile{};
+    TileHead nxt = n > 0 ? load_head(list) : TileHead{};
     for (int i = 0; i < n; ++i) {
-      const WorkTile r = nxt;
-      if (i + 1 < n) nxt = load_tile(list + i + 1);
-      const int s = i % kStages, b = i & 1;
+      const TileHead r = nxt;
+      if (i + 1 < n) nxt = load_head(list + i + 1);
+      const int u = n1 + i;
+      const int s = u % kStages, b = i & 1;
       const uint32_t st = base + L::kStage0 + s * kStageBytes;
       const bool has_state = !(r.flags & kTileFirst) || (r.flags & kTileHasInit);
       const uint32_t colO = b ? kColO1 : kColO0;
@@ -311,18 +454,20 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int half = (warp - 3) >> 2;             // 64-column half of P this warp converts
     const int row = quarter * 32 + lane;          // tile row = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    WorkTile nxt = n > 0 ? load_tile(list) : WorkTile{};
+    TileMask nxt = n > 0 ? load_mask(list) : TileMask{};
     for (int i = 0; i < n; ++i) {
-      const WorkTile r = nxt;
-      if (i + 1 < n) nxt = load_tile(list + i + 1);
+      const TileMask r = nxt;
+      if (i + 1 < n) nxt = load_mask(list + i + 1);
       const int b = i & 1;
       int seg_start = 0;
       if (r.nbound > 1) {
         const int nb = r.nbound < kInlineBounds ? r.nbound : kInlineBounds;
-        for (int q = 1; q < nb; ++q)
-          if (r.inl[q] <= row) seg_start = r.inl[q];
+        for (int q = 1; q < nb; ++q) {
+          const int sb = inline_bound(r.inl, q);
+          if (sb <= row) seg_start = sb;
+        }
         for (int q = kInlineBounds; q < r.nbound; ++q) {
-          const int sb = bounds[r.bound0 + q];
+          const int sb = prm.bounds[r.bound0 + q];
           if (sb <= row) seg_start = sb;
         }
       }
@@ -348,12 +493,12 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int c = 0; c < 32; ++c) {
           const int jj = c0 + 2 * c;
           float p0 = __uint_as_float(c < 16 ? r0[2 * c] : r1[2 * c - 32]);
-          float p1 = __uint_as_float(c < 16 ? r0[2 * c + 1] : r1[2 * c - 31]);
+          float p1v = __uint_as_float(c < 16 ? r0[2 * c + 1] : r1[2 * c - 31]);
           if (!all_kept) {
             p0 = (jj >= seg_start && jj <= hi_col) ? p0 : 0.f;
-            p1 = (jj + 1 >= seg_start && jj + 1 <= hi_col) ? p1 : 0.f;
+            p1v = (jj + 1 >= seg_start && jj + 1 <= hi_col) ? p1v : 0.f;
           }
-          pk[c] = pack_bf16x2(p0, p1);
+          pk[c] = pack_bf16x2(p0, p1v);
         }
       }
       // bf16 pairs of this half's 64 columns go to its first 32 columns, all
@@ -371,65 +516,161 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // State work: lanes 0..63 and their copy in lanes 64..127 hold state rows
     // d = row & 63; the lower copy handles columns 0..31, the upper 32..63.
     const int d = row & 63, sh = row >> 6;
-    // The running state (row d, columns 32*sh ..) in fp32, and the first
-    // term of the next piece's start state as loaded a tile ahead (summed
-    // only when it is needed, so the loads stay in flight meanwhile).
-    float s_run[32], s_a[32];
-    // Which start state s_a holds, and which state each S operand holds
-    // (first tile of a piece only; -1 = none / a running state).  A run of
-    // pieces with the same start state (the packed branch tiles of one
-    // parent) fetches and stages it once per operand.
-    int64_t tag_a = -1, tag_op0 = -1, tag_op1 = -1;
-    auto start_tag = [&](const WorkTile& r) -> int64_t {
+    const int64_t half_row = static_cast<int64_t>(d) * kHeadDim + sh * 32;   // offset in a state
+    bool ok = true;
+
+    // Phase 1: each piece's K^T V out of TMEM into its workspace slot; then
+    // this CTA counts itself in the grid-wide counter.
+    for (int j = 0; j < n_p1 && ok; ++j) {
+      const SpanDesc sd = p1_of(j);
+      const int b = j & 1;
+      ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kP1Ready + b), (j >> 1) & 1, err, kErrTimeoutMma));
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t r0[32];
+      tmem_ld_32cols(tmem + lane_base + (b ? kColD1 : kColD0) + 32 * sh, r0);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kP1Free + b));
+      store_half_row(prm.ws + static_cast<int64_t>(sd.slot) * kStateFloats + half_row,
+                     reinterpret_cast<const float*>(r0));
+    }
+    if (n_p1 > 0) {
+      mbar_arrive(bar(L::kP1Done));
+      __threadfence();
+      named_barrier_sync(kNamedStateBar, kGroupThreads);
+      if (tid == kStateWarp0 * 32) atomicAdd(prm.counter, 1u);
+    }
+    // Wait (bounded) until every phase-1 CTA has counted itself, once, before
+    // the first read of another CTA's slots.
+    bool synced = !prm.fused;
+    auto grid_sync = [&]() {
+      if (synced) return;
+      synced = true;
+      if (tid == kStateWarp0 * 32) {
+        const unsigned long long t0 = global_timer_ns();
+        while (ld_acquire_gpu(prm.counter) < static_cast<unsigned>(prm.n_p1_ctas)) {
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeoutMma);
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      named_barrier_sync(kNamedStateBar, kGroupThreads);
+    };
+
+    // The running state (row d, columns 32*sh ..) in fp32.  tag_run names the
+    // start state it holds while it is one (after the first tile of a
+    // one-tile piece, or a view's final state); -1 once tiles have been added
+    // to it.  A run of pieces with the same start state (the packed branch
+    // tiles of one parent) loads it once, and each S operand remembers the
+    // start state it holds, so that it is staged once per operand.
+    float s_run[32];
+    int64_t tag_run = -1, tag_op0 = -1, tag_op1 = -1;
+    auto carry_tag = [&](int view, int head) -> int64_t {
+      return (static_cast<int64_t>(1) << 62) | (static_cast<int64_t>(view) << 16) | head;
+    };
+    auto start_tag = [&](const TileState& r) -> int64_t {
       if (!(r.flags & kTileFirst) || !(r.flags & kTileHasInit)) return -1;
-      return ((static_cast<int64_t>(r.stateA) + 1) << 40) ^ ((static_cast<int64_t>(r.stateB) + 1) << 16) ^
+      if (r.flags & kTileCarry) return carry_tag(r.final_idx, r.head);
+      return ((static_cast<int64_t>(r.stateA) + 1) << 40) ^ ((static_cast<int64_t>(r.a_n)) << 34) ^
+             ((static_cast<int64_t>(r.stateB) + 1) << 16) ^ (static_cast<int64_t>(r.b_n) << 10) ^
              static_cast<int64_t>(r.head);
     };
-
-    // Issue the loads of the start state of the piece starting at tile record
-    // `r`: the parent view's final state, or else the prefix slot.
-    auto fetch_state = [&](const WorkTile& r) {
-      const int64_t tag = start_tag(r);
-      if (tag >= 0 && tag == tag_a) return;   // already in s_a
-      tag_a = tag;
-      const float4* a = nullptr;
-      if (r.stateA >= 0)
-        a = reinterpret_cast<const float4*>(
-                stateA + ((static_cast<int64_t>(r.stateA) * H + r.head) * kHeadDim + d) * kHeadDim) + sh * 8;
-      else if (r.stateB >= 0)
-        a = reinterpret_cast<const float4*>(stateB + (static_cast<int64_t>(r.stateB) * kHeadDim + d) * kHeadDim) +
-            sh * 8;
-      if (a != nullptr) {
+    // Sum, in order, of the states of term A (a_n states a_rows heads apart)
+    // and term B (b_n workspace slots) into s_run.  The group reads each
+    // state coalesced (thread g of the group takes float4 number g + 128 c),
+    // the sum goes through S operand t & 1 (free: its last reader was Q S of
+    // tile t - 2), and each thread takes its half-row back from there.  The
+    // buffer index is XOR-swizzled on the half-row so that both sides are
+    // free of bank conflicts.
+    auto sum_start = [&](int t, const TileState& r) {
+      const int g = tid - kStateWarp0 * 32;
+      const int na = r.a_n, total = r.a_n + r.b_n;
+      const float* pa =
+          na > 0 ? prm.stateA + (static_cast<int64_t>(r.stateA) * prm.a_rows + (prm.a_rows > 1 ? r.head : 0)) *
+                                    kStateFloats
+                 : nullptr;
+      const int64_t sa = static_cast<int64_t>(prm.a_rows) * kStateFloats;
+      const float* pb = r.b_n > 0 ? prm.ws + static_cast<int64_t>(r.stateB) * kStateFloats : nullptr;
+      auto src = [&](int k) -> const float4* {
+        return reinterpret_cast<const float4*>(k < na ? pa + k * sa : pb + static_cast<int64_t>(k - na) * kStateFloats) + g;
+      };
+      float4 acc[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 v4 = __ldcg(a + c);
-          s_a[4 * c] = v4.x; s_a[4 * c + 1] = v4.y; s_a[4 * c + 2] = v4.z; s_a[4 * c + 3] = v4.w;
-        }
+      for (int c = 0; c < 8; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      auto add4 = [](float4& x, const float4 y) { x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w; };
+      int k = 0;
+      for (; k + 2 <= total; k += 2) {
+        const float4* p0 = src(k);
+        const float4* p1 = src(k + 1);
+        float4 x[8], y[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) x[c] = __ldcg(p0 + 128 * c);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) y[c] = __ldcg(p1 + 128 * c);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) add4(acc[c], x[c]);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) add4(acc[c], y[c]);
       }
+      if (k < total) {
+        const float4* p0 = src(k);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) add4(acc[c], __ldcg(p0 + 128 * c));
+      }
+      float4* buf = reinterpret_cast<float4*>(smem + L::kS + (t & 1) * kSOpBytes);
+      if (t & 1) tag_op1 = -1; else tag_op0 = -1;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int f = g + 128 * c, hr = f >> 3;
+        buf[hr * 8 + ((f & 7) ^ ((hr >> 1) & 7))] = acc[c];
+      }
+      named_barrier_sync(kNamedStateBar, kGroupThreads);
+      const int hr = 2 * d + sh;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 v4 = buf[hr * 8 + (c ^ ((hr >> 1) & 7))];
+        s_run[4 * c] = v4.x; s_run[4 * c + 1] = v4.y; s_run[4 * c + 2] = v4.z; s_run[4 * c + 3] = v4.w;
+      }
+      named_barrier_sync(kNamedStateBar, kGroupThreads);
     };
-
     // The running state becomes the start state of the piece starting at `r`
-    // (a piece with both terms -- a later piece of a long branch -- adds its
-    // prefix slot here).
-    auto start_piece = [&](const WorkTile& r) {
-      const bool has = r.stateA >= 0 || r.stateB >= 0;
+    // (its S is staged next into operand t & 1): zero, the final state this
+    // CTA computed (carry), the one it holds already, or the sum of term A
+    // and term B.
+    auto start_piece = [&](int t, const TileState& r) {
+      if (!(r.flags & kTileHasInit)) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) s_run[e] = has ? s_a[e] : 0.f;
-      if (r.stateA >= 0 && r.stateB >= 0) {
-        const float4* bb = reinterpret_cast<const float4*>(
-            stateB + (static_cast<int64_t>(r.stateB) * kHeadDim + d) * kHeadDim) + sh * 8;
+        for (int e = 0; e < 32; ++e) s_run[e] = 0.f;
+        tag_run = -1;
+        return;
+      }
+      const int64_t tag = start_tag(r);
+      if (tag == tag_run) return;
+      tag_run = tag;
+      if (r.flags & kTileCarry) {
+        // The running state has moved on since the view's last tile (a long
+        // branch ran in between): this thread's own half-row of the final
+        // state, as it wrote it.
+        const float4* p4 = reinterpret_cast<const float4*>(
+            prm.final_out + (static_cast<int64_t>(r.final_idx) * H + r.head) * kStateFloats + half_row);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const float4 v4 = __ldcg(bb + c);
-          s_run[4 * c] += v4.x; s_run[4 * c + 1] += v4.y; s_run[4 * c + 2] += v4.z; s_run[4 * c + 3] += v4.w;
+          const float4 v4 = __ldcg(p4 + c);
+          s_run[4 * c] = v4.x; s_run[4 * c + 1] = v4.y; s_run[4 * c + 2] = v4.z; s_run[4 * c + 3] = v4.w;
         }
+        return;
       }
+      if (prm.fused) grid_sync();
+      sum_start(t, r);
     };
 
     // S(t) -> S operand t & 1 (when tile t uses a state and the operand does
     // not hold that start state already).  The operand was last read by Q S
     // of tile t-2, whose completion o_work(t-2) saw.
-    auto stage = [&](int t, const WorkTile& r) {
+    auto stage = [&](int t, const TileState& r) {
       const int64_t tag = start_tag(r);
       const bool uses = !(r.flags & kTileFirst) || (r.flags & kTileHasInit);
       const int64_t held = (t & 1) ? tag_op1 : tag_op0;
@@ -442,14 +683,14 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     };
 
     // O(i) -> global (rows of the tile only).
-    auto o_work = [&](int i, const WorkTile& r) -> bool {
+    auto o_work = [&](int i, const TileState& r) -> bool {
       const int b = i & 1;
       if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
         return false;
       tc_fence_after_sync();
       const uint32_t colO = b ? kColO1 : kColO0;
       uint4* dst = reinterpret_cast<uint4*>(
-          out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim);
+          prm.out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim);
       const bool store = row < r.nrows;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -472,42 +713,52 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       return true;
     };
 
-    griddep_wait();   // start states from the scan
-    if (n > 0) {
-      WorkTile cur = load_tile(list);
-      WorkTile nxt = n > 1 ? load_tile(list + 1) : WorkTile{};
-      fetch_state(cur);
-      start_piece(cur);
+    // Tile i's dS into the running state; at the last tile of a view-head
+    // that is the view's final state: write it out; the branch tiles of this
+    // run that start from it (carry) find it in s_run.
+    auto take_ds = [&](int i, const TileState& r) -> bool {
+      const int b = i & 1;
+      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kDReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
+        return false;
+      tc_fence_after_sync();
+      if (!(r.flags & kTileLast) || (r.flags & kTileFinalOut)) {
+        uint32_t r0[32];
+        tmem_ld_32cols(tmem + lane_base + (b ? kColD1 : kColD0) + 32 * sh, r0);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s_run[e] += __uint_as_float(r0[e]);
+        tag_run = -1;
+      }
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kDFree + b));
+      if (r.flags & kTileFinalOut) {
+        store_half_row(prm.final_out + (static_cast<int64_t>(r.final_idx) * H + r.head) * kStateFloats + half_row,
+                       s_run);
+        tag_run = carry_tag(r.final_idx, r.head);
+      }
+      return true;
+    };
+
+    if (ok) griddep_wait();   // start states from the scan (three launches)
+    if (ok && n > 0) {
+      TileState cur = load_state(list);
+      TileState nxt = n > 1 ? load_state(list + 1) : TileState{};
+      start_piece(0, cur);
       stage(0, cur);
-      if (n > 1 && (nxt.flags & kTileFirst)) fetch_state(nxt);
-      bool ok = true;
       for (int i = 0; i < n && ok; ++i) {
-        WorkTile nxt2 = i + 2 < n ? load_tile(list + i + 2) : WorkTile{};
         // S(i+1) first: the O issuer needs it right after P V of tile i+1.
         if (i + 1 < n) {
-          const int b = i & 1;
-          ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kDReady + b), (i >> 1) & 1, err, kErrTimeoutMma));
+          ok = take_ds(i, cur);
           if (!ok) break;
-          tc_fence_after_sync();
-          if (!(cur.flags & kTileLast)) {
-            uint32_t r0[32];
-            tmem_ld_32cols(tmem + lane_base + (b ? kColD1 : kColD0) + 32 * sh, r0);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s_run[e] += __uint_as_float(r0[e]);
-          } else {
-            start_piece(nxt);
-          }
-          tc_fence_before_sync();
-          mbar_arrive(bar(L::kDFree + b));
+          if (cur.flags & kTileLast) start_piece(i + 1, nxt);
           stage(i + 1, nxt);
-          // s_a is free again: fetch the start state of tile i+2 if it
-          // begins a piece.
-          if (i + 2 < n && (nxt2.flags & kTileFirst)) fetch_state(nxt2);
+        } else if (cur.flags & kTileFinalOut) {
+          ok = take_ds(i, cur);
+          if (!ok) break;
         }
         ok = o_work(i, cur);
         cur = nxt;
-        nxt = nxt2;
+        if (i + 2 < n) nxt = load_state(list + i + 2);
       }
     }
   }
@@ -522,27 +773,45 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 }  // namespace
 
 cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                               const CUtensorMap* tm_v, const WorkTile* work,
-                               const int32_t* cta_begin, int grid, const uint8_t* bounds,
-                               const float* stateA, const float* stateB, void* out, int H,
-                               unsigned* err, cudaStream_t stream, bool pdl) {
-  if (grid <= 0) return cudaSuccess;
+                               const CUtensorMap* tm_v, const SpanOutputArgs& a, cudaStream_t stream) {
+  if (a.grid <= 0) return cudaSuccess;
   const uint32_t bytes = OutSmem::kRequest;
   static std::atomic<uint64_t> done{0};
   cudaError_t e = set_smem_limit_once(span_output_kernel, bytes, done);
   if (e != cudaSuccess) return e;
+  OutParams p{};
+  p.work = a.work;
+  p.cta_begin = a.cta_begin;
+  p.bounds = a.bounds;
+  p.stateA = a.stateA;
+  p.ws = a.ws;
+  p.final_out = a.final_out;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.err = a.err;
+  p.p1 = a.p1;
+  p.p1_begin = a.p1_begin;
+  p.counter = a.counter;
+  p.a_rows = a.a_rows;
+  p.H = a.H;
+  p.fused = a.fused ? 1 : 0;
+  p.n_p1_ctas = a.n_p1_ctas;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (a.fused) {
+    // CTAs wait on one another: all of them must be resident at once.
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, span_output_kernel, tm_q[0], tm_k[0], tm_v[0], work, cta_begin,
-                            bounds, stateA, stateB, static_cast<__nv_bfloat16*>(out), H, err);
+  cfg.numAttrs = (a.fused || a.pdl) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, span_output_kernel, tm_q[0], tm_k[0], tm_v[0], p);
 }
 
 }  // namespace spanla

@@ -49,6 +49,11 @@ span_la_status cuda_fail(cudaError_t e, const char* what) {
   return fail(SPAN_LA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Structure of the bf16 pass (span_la_pass_variant): 0 = one launch, 1 =
+// three launches (span state -> scan -> output).
+std::atomic<int32_t> g_pass_variant{0};
+bool one_launch() { return g_pass_variant.load(std::memory_order_relaxed) == 0; }
+
 // Fault injection (span_la_fault_inject): the next g_fail_allocs device
 // allocations of the library fail as if the device were out of memory.
 std::atomic<int32_t> g_fail_allocs{0};
@@ -281,6 +286,10 @@ struct Plan {
   std::vector<int32_t> cta_begin;    // span_output CTA c runs work[cta_begin[c] .. cta_begin[c+1])
   int run_tiles = 0;                 // longest run (tiles)
   int64_t n_pieces = 0;              // output pieces (packed tiles included), all heads
+  // one-launch pass: spans / span_begin are the phase-1 pieces per output CTA
+  bool fused = false;
+  int n_p1_ctas = 0;                 // CTAs with phase-1 pieces
+  std::vector<int32_t> empty_views;  // views without rows (their final state is zero)
 
   int state_slots(int H) const {
     return span_mode ? static_cast<int>(spans.size()) : static_cast<int>(chunks.size()) * H;
@@ -357,7 +366,7 @@ std::vector<BranchGroup> group_branches(const int32_t* cu, int32_t B, const int3
 }
 
 Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu, int32_t B,
-                    const int32_t* parent, int H, int num_sms) {
+                    const int32_t* parent, int H, int num_sms, bool fused) {
   Plan plan;
   plan.span_mode = true;
   const std::vector<BranchGroup> groups = group_branches(branch_cu, B, parent, &plan.bounds);
@@ -459,54 +468,116 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
   }
   plan.work.resize(W);
 
-  std::vector<SpanDesc> pieces;   // in creation order
-  std::vector<int> piece_cta;      // output CTA of each piece
+  // Pass 1: every block's pieces (split at the run boundaries), and for the
+  // one-launch pass, per view-head, the run that holds its last tile and
+  // whether any tile of its branches lies in another run (then every piece
+  // of the view, the last one too, publishes its state).
+  struct BPiece { int j0, j1, c; };
+  std::vector<BPiece> bps;
+  bps.reserve(blocks.size() + grid);
+  std::vector<int32_t> bp_off(blocks.size() + 1, 0);
+  std::vector<int32_t> vlast(fused ? static_cast<size_t>(V) * H : 0, -1);
+  std::vector<uint8_t> vall(fused ? static_cast<size_t>(V) * H : 0, 0);
+  {
+    int64_t g0 = 0;
+    for (size_t bi = 0; bi < blocks.size(); ++bi) {
+      const Block& bk = blocks[bi];
+      bp_off[bi] = static_cast<int32_t>(bps.size());
+      int64_t a0 = g0;
+      const int64_t end = g0 + bk.ntiles;
+      while (a0 < end) {
+        const int c = cta_of(a0);
+        const int64_t b0 = std::min<int64_t>(end, run_start(c) + run_len(c));
+        bps.push_back({static_cast<int>(a0 - g0), static_cast<int>(b0 - g0), c});
+        a0 = b0;
+      }
+      if (fused) {
+        if (bk.kind == 0 && bk.ntiles > 0) vlast[static_cast<size_t>(bk.id) * H + bk.head] = bps.back().c;
+        if (bk.kind != 0) {
+          const size_t vh = static_cast<size_t>(groups[bk.id].parent) * H + bk.head;
+          for (size_t q = bp_off[bi]; q < bps.size(); ++q)
+            if (bps[q].c != vlast[vh]) vall[vh] = 1;
+        }
+      }
+      g0 += bk.ntiles;
+    }
+    bp_off[blocks.size()] = static_cast<int32_t>(bps.size());
+  }
+
+  // Pass 2: state slots, start-state recipes and the tile records.
+  std::vector<SpanDesc> pieces;   // pieces with a slot, in creation order
+  std::vector<int> piece_cta;      // output CTA of each
   pieces.reserve(blocks.size() + grid);
   piece_cta.reserve(blocks.size() + grid);
+  std::vector<int32_t> vslot0(fused ? static_cast<size_t>(V) * H : 0, 0);
+  std::vector<int32_t> vnslot(fused ? static_cast<size_t>(V) * H : 0, 0);
   int64_t g0 = 0;
-  std::vector<std::pair<int, int>> pr;   // a block's pieces: local tile ranges [j0, j1)
-  std::vector<int> pcta;                 // and their CTAs
-  for (const Block& bk : blocks) {
+  for (size_t bi = 0; bi < blocks.size(); ++bi) {
+    const Block& bk = blocks[bi];
     if (bk.kind == 0 && bk.ntiles == 0) {   // empty view: zero final state
-      plan.scan.push_back({0, 0, bk.id, bk.head});
+      if (fused) {
+        if (bk.head == 0) plan.empty_views.push_back(bk.id);
+      } else {
+        plan.scan.push_back({0, 0, bk.id, bk.head});
+      }
       continue;
     }
-    // The block's pieces: [g0, g0 + ntiles) split at the run boundaries.
-    pr.clear();
-    pcta.clear();
-    {
-      int64_t a = g0;
-      const int64_t end = g0 + bk.ntiles;
-      while (a < end) {
-        const int c = cta_of(a);
-        const int64_t b = std::min<int64_t>(end, run_start(c) + run_len(c));
-        pr.push_back({static_cast<int>(a - g0), static_cast<int>(b - g0)});
-        pcta.push_back(c);
-        a = b;
-      }
-    }
-    const bool slots = bk.kind == 0 || (bk.kind == 1 && pr.size() >= 2);
+    const int m = bp_off[bi + 1] - bp_off[bi];
+    const BPiece* bp = bps.data() + bp_off[bi];
+    const int32_t parent = bk.kind == 0 ? -1 : groups[bk.id].parent;
+    const size_t pvh = parent >= 0 ? static_cast<size_t>(parent) * H + bk.head : 0;
+    // pieces of this block that own a slot: k < nslots
+    int nslots;
+    if (!fused) nslots = (bk.kind == 0 || (bk.kind == 1 && m >= 2)) ? m : 0;
+    else if (bk.kind == 0) nslots = vall[static_cast<size_t>(bk.id) * H + bk.head] ? m : m - 1;
+    else nslots = bk.kind == 1 ? m - 1 : 0;
     const int slot0 = static_cast<int>(pieces.size());
-    if (slots) plan.scan.push_back({slot0, static_cast<int32_t>(pr.size()), bk.kind == 0 ? bk.id : -1, bk.head});
-    for (size_t k = 0; k < pr.size(); ++k) {
-      const int j0 = pr[k].first, j1 = pr[k].second;
-      const int c = pcta[k];
-      const int64_t r0 = bk.row0 + static_cast<int64_t>(j0) * kTileRows;
-      const int64_t r1 = std::min<int64_t>(bk.row0 + bk.len, bk.row0 + static_cast<int64_t>(j1) * kTileRows);
-      if (slots) {
+    if (!fused && nslots > 0) plan.scan.push_back({slot0, nslots, bk.kind == 0 ? bk.id : -1, bk.head});
+    if (fused && bk.kind == 0) {
+      vslot0[static_cast<size_t>(bk.id) * H + bk.head] = slot0;
+      vnslot[static_cast<size_t>(bk.id) * H + bk.head] = nslots;
+    }
+    for (int k = 0; k < m; ++k) {
+      const int j0 = bp[k].j0, j1 = bp[k].j1, c = bp[k].c;
+      if (k < nslots) {
+        const int64_t r0 = bk.row0 + static_cast<int64_t>(j0) * kTileRows;
+        const int64_t r1 = std::min<int64_t>(bk.row0 + bk.len, bk.row0 + static_cast<int64_t>(j1) * kTileRows);
         pieces.push_back({static_cast<int32_t>(r0), static_cast<int32_t>(r1 - r0), bk.head,
                           static_cast<int32_t>(pieces.size())});
         piece_cta.push_back(c);
       }
-      const int32_t sA = bk.kind == 0 ? -1 : groups[bk.id].parent;
-      const int32_t sB = (slots && k > 0) ? slot0 + static_cast<int32_t>(k) : -1;
       ++plan.n_pieces;
-      // CTA c's run is contiguous in the head-major order
-      WorkTile* dst = plan.work.data() + plan.cta_begin[c] + (g0 + j0 - run_start(c));
       WorkTile w{};
       w.head = bk.head;
-      w.stateA = sA;
-      w.stateB = sB;
+      w.final_idx = -1;
+      w.stateA = -1;
+      w.stateB = -1;
+      int32_t init = 0;
+      if (!fused) {
+        // three launches: the parent's final state (scan output) and the
+        // piece's scanned prefix slot
+        if (parent >= 0) { w.stateA = parent; w.a_n = 1; }
+        if (nslots > 0 && k > 0) { w.stateB = slot0 + k; w.b_n = 1; }
+        init = (w.a_n + w.b_n) > 0 ? kTileHasInit : 0;
+      } else {
+        // one launch: the parent's final state from this CTA (carry) or as
+        // the sum of the parent view-head's pieces; the own prefix as the
+        // sum of the earlier pieces
+        if (parent >= 0) {
+          if (k == 0 && c == vlast[pvh]) {
+            init = kTileHasInit | kTileCarry;
+            w.final_idx = parent;
+          } else if (vnslot[pvh] > 0) {
+            w.stateA = vslot0[pvh];
+            w.a_n = vnslot[pvh];
+          }
+        }
+        if (k > 0) {
+          w.stateB = slot0;
+          w.b_n = k;
+        }
+        if (w.a_n + w.b_n > 0) init |= kTileHasInit;
+      }
       if (bk.kind == 2) {
         const BranchGroup& bg = groups[bk.id];
         w.bound0 = bg.bound0;
@@ -516,16 +587,35 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
         w.bound0 = 0;
         w.nbound = 1;
       }
-      const int32_t init = (sA >= 0 || sB >= 0) ? kTileHasInit : 0;
+      // CTA c's run is contiguous in the head-major order
+      WorkTile* dst = plan.work.data() + plan.cta_begin[c] + (g0 + j0 - run_start(c));
       for (int j = j0; j < j1; ++j) {
         const int64_t r = static_cast<int64_t>(j) * kTileRows;
         w.row0 = static_cast<int32_t>(bk.row0 + r);
         w.nrows = static_cast<int32_t>(std::min<int64_t>(kTileRows, bk.len - r));
         w.flags = (j == j0 ? kTileFirst : 0) | (j + 1 == j1 ? kTileLast : 0) | init;
+        if (fused && bk.kind == 0 && k + 1 == m && j + 1 == j1) {
+          w.flags |= kTileFinalOut;
+          w.final_idx = bk.id;
+        }
         dst[j - j0] = w;
       }
     }
     g0 += bk.ntiles;
+  }
+  if (fused) {
+    // phase-1 pieces listed per output CTA (index = the CTA of the run)
+    plan.span_begin.assign(grid + 1, 0);
+    for (int c : piece_cta) ++plan.span_begin[c + 1];
+    for (int c = 0; c < grid; ++c) {
+      plan.n_p1_ctas += plan.span_begin[c + 1] > 0;
+      plan.span_begin[c + 1] += plan.span_begin[c];
+    }
+    plan.spans.resize(pieces.size());
+    std::vector<int32_t> fill(plan.span_begin.begin(), plan.span_begin.end() - 1);
+    for (size_t u = 0; u < pieces.size(); ++u) plan.spans[fill[piece_cta[u]]++] = pieces[u];
+    plan.fused = true;
+    return plan;
   }
 
   // span_state: with no more pieces than SMs, piece k goes to the CTA that
@@ -573,8 +663,8 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
 }
 
 Plan make_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu, int32_t B,
-               const int32_t* parent, int H, bool span_mode, int num_sms) {
-  if (span_mode) return make_span_plan(view_cu, V, branch_cu, B, parent, H, num_sms);
+               const int32_t* parent, int H, bool span_mode, int num_sms, bool fused = false) {
+  if (span_mode) return make_span_plan(view_cu, V, branch_cu, B, parent, H, num_sms, fused && V > 0);
   Plan plan;
   plan.span_mode = false;
   for (int32_t s = 0; s < V; ++s)
@@ -639,6 +729,9 @@ struct DescBlock {
   size_t n_out_tiles = 0;
   size_t block_bytes = 0;  // size of the descriptor block on the device
   bool span_mode = true;
+  bool fused = false;      // one-launch pass (span mode)
+  int n_p1_ctas = 0;
+  std::vector<int32_t> empty_views;
 };
 
 DescBlock make_desc(const Plan& plan, int H) {
@@ -665,6 +758,9 @@ DescBlock make_desc(const Plan& plan, int H) {
   d.state_slots = plan.state_slots(H);
   d.n_out_tiles = plan.n_out_tiles();
   d.block_bytes = d.host.size();
+  d.fused = plan.fused;
+  d.n_p1_ctas = plan.n_p1_ctas;
+  d.empty_views = plan.empty_views;
   return d;
 }
 
@@ -865,9 +961,9 @@ span_la_status finish_read(CacheEntry* entry, cudaStream_t stream, span_la_statu
 // states.  With `mc` (the caller holds g_cache_mu) the TMA descriptors of
 // bf16 operands are reused from the last call on the same arrays.
 span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t* parts, float* states,
-                            const void* q, const void* k, const void* v, const span_la_dims& dims,
-                            const float* stateA, float* final_out, void* out, unsigned* err,
-                            cudaStream_t stream, MapCache* mc, int device) {
+                            unsigned* counter, const void* q, const void* k, const void* v,
+                            const span_la_dims& dims, const float* stateA, float* final_out, void* out,
+                            unsigned* err, cudaStream_t stream, MapCache* mc, int device) {
   const int H = dims.num_heads;
   const int64_t T = dims.total_rows;
   const bool split = dims.dtype == SPAN_LA_F32;
@@ -921,6 +1017,40 @@ span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t
     mc->chunk_ops = chunk_ops;
   }
 
+  if (desc.fused) {
+    // One launch: the counter of the CTAs' phase-1 states starts at zero;
+    // views without rows get the zero final state.
+    e = cudaMemsetAsync(counter, 0, sizeof(unsigned), stream);
+    for (size_t j = 0; j < desc.empty_views.size() && e == cudaSuccess; ++j)
+      e = cudaMemsetAsync(final_out + static_cast<int64_t>(desc.empty_views[j]) * H * kStateFloats, 0,
+                          static_cast<size_t>(H) * kStateFloats * sizeof(float), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(pass counter)");
+    if (desc.n_out_tiles > 0) {
+      SpanOutputArgs a;
+      a.work = reinterpret_cast<const WorkTile*>(block + desc.off_b);
+      a.cta_begin = reinterpret_cast<const int32_t*>(block + desc.off_c);
+      a.grid = desc.grid;
+      a.bounds = block + desc.off_bounds;
+      a.stateA = states;
+      a.a_rows = 1;
+      a.ws = states;
+      a.final_out = final_out;
+      a.out = out;
+      a.H = H;
+      a.err = err;
+      a.fused = true;
+      a.p1 = reinterpret_cast<const SpanDesc*>(block + desc.off_a);
+      a.p1_begin = reinterpret_cast<const int32_t*>(block + desc.off_d);
+      a.counter = counter;
+      a.n_p1_ctas = desc.n_p1_ctas;
+      e = counted_launch(kKernelSpanOutput, stream, [&] {
+        return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v, a, stream);
+      });
+      if (e != cudaSuccess) return cuda_fail(e, "one-launch pass");
+    }
+    return SPAN_LA_OK;
+  }
+
   bool kernel_before = split;   // a kernel precedes the next launch in the stream
   if (desc.state_slots > 0) {
     e = desc.span_mode
@@ -950,11 +1080,21 @@ span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t
   if (desc.n_out_tiles > 0) {
     const bool pdl = kernel_before;
     if (desc.span_mode) {
+      SpanOutputArgs a;
+      a.work = reinterpret_cast<const WorkTile*>(block + desc.off_b);
+      a.cta_begin = reinterpret_cast<const int32_t*>(block + desc.off_c);
+      a.grid = desc.grid;
+      a.bounds = block + desc.off_bounds;
+      a.stateA = stateA;
+      a.a_rows = H;
+      a.ws = states;
+      a.final_out = final_out;
+      a.out = out;
+      a.H = H;
+      a.err = err;
+      a.pdl = pdl;
       e = counted_launch(kKernelSpanOutput, stream, [&] {
-        return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v,
-                                  reinterpret_cast<const WorkTile*>(block + desc.off_b),
-                                  reinterpret_cast<const int32_t*>(block + desc.off_c), desc.grid,
-                                  block + desc.off_bounds, stateA, states, out, H, err, stream, pdl);
+        return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v, a, stream);
       });
     } else {
       e = counted_launch(kKernelTile, stream, [&] {
@@ -997,14 +1137,15 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
     local = make_desc(build_plan(), H);
     desc = &local;
   }
-  if (desc->n_out_tiles == 0 && desc->n_scan == 0) return SPAN_LA_OK;
+  if (desc->n_out_tiles == 0 && desc->n_scan == 0 && desc->empty_views.empty()) return SPAN_LA_OK;
 
   // Workspace: the descriptor block when it is not cached, the state slots
   // and, for fp32 inputs, the six bf16 part arrays.
   const size_t desc_bytes = use_cache ? 0 : align256(desc->host.size());
   const size_t off_states = desc_bytes;
   const size_t state_bytes = static_cast<size_t>(desc->state_slots) * kStateFloats * sizeof(float);
-  const size_t off_parts = align256(off_states + state_bytes);
+  const size_t off_counter = align256(off_states + state_bytes);
+  const size_t off_parts = off_counter + 256;
   const size_t part_bytes = static_cast<size_t>(T) * H * kHeadDim * 2;
   const size_t total = std::max<size_t>(off_parts + (split ? 6 * part_bytes : 0), 256);
 
@@ -1018,7 +1159,8 @@ span_la_status run_plan(const std::vector<int32_t>& key, BuildPlan&& build_plan,
     block = ws;
   }
   if (st == SPAN_LA_OK)
-    st = enqueue_pass(*desc, block, ws + off_parts, reinterpret_cast<float*>(ws + off_states), q, k, v, dims,
+    st = enqueue_pass(*desc, block, ws + off_parts, reinterpret_cast<float*>(ws + off_states),
+                      reinterpret_cast<unsigned*>(ws + off_counter), q, k, v, dims,
                       stateA, final_out, out, dev->err, stream,
                       use_cache ? &g_maps[device & (kMaxDevices - 1)] : nullptr, device);
   st = finish_read(entry, stream, st);
@@ -1195,11 +1337,13 @@ span_la_status span_la_pass(const void* q, const void* k, const void* v, span_la
 
   int device = 0;
   cudaGetDevice(&device);
-  const std::vector<int32_t> key = plan_key(device, dims.dtype, dims.num_heads, 0, dev->num_sms, view_cu_seqlens,
-                                            num_views, branch_cu_seqlens, num_branches, branch_parent);
+  const bool fused = one_launch();
+  const std::vector<int32_t> key = plan_key(device, dims.dtype, dims.num_heads, fused ? 4 : 0, dev->num_sms,
+                                            view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
+                                            branch_parent);
   auto build = [&] {
     return make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches, branch_parent,
-                     dims.num_heads, dims.dtype == SPAN_LA_BF16, dev->num_sms);
+                     dims.num_heads, dims.dtype == SPAN_LA_BF16, dev->num_sms, fused);
   };
   return run_plan(key, build, q, k, v, dims, view_state_out, view_state_out, out, stream, dev, device);
 }
@@ -1400,19 +1544,20 @@ span_la_status span_la_plan_stats(const int32_t* view_cu_seqlens, int32_t num_vi
   if ((st = check_parents(branch_parent, num_branches, from_state ? num_parents : num_views)) != SPAN_LA_OK) return st;
   const int H = num_heads;
   const Plan plan = make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
-                              branch_parent, H, dtype == SPAN_LA_BF16, num_sms);
+                              branch_parent, H, dtype == SPAN_LA_BF16, num_sms, !from_state && one_launch());
   // Every count is summed over heads.
   int64_t state_rows = 0, finals = 0, tile_rows = 0, state_reads = 0;
   for (const ChunkDesc& c : plan.chunks) state_rows += static_cast<int64_t>(c.len) * H;
   for (const SpanDesc& c : plan.spans) state_rows += c.len;
   for (const ScanDesc& s : plan.scan) finals += (s.final_idx >= 0) * (plan.span_mode ? 1 : H);
+  if (plan.fused) finals = static_cast<int64_t>(num_views) * H;
   for (const TileDesc& t : plan.tiles) {
     tile_rows += static_cast<int64_t>(t.nrows) * H;
     state_reads += static_cast<int64_t>((t.stateA >= 0) + (t.stateB >= 0)) * H;
   }
   for (const WorkTile& w : plan.work) {
     tile_rows += w.nrows;
-    if (w.flags & kTileFirst) state_reads += (w.stateA >= 0) + (w.stateB >= 0);
+    if ((w.flags & kTileFirst) && !(w.flags & kTileCarry)) state_reads += w.a_n + w.b_n;
   }
   stats[0] = plan.state_slots(H);
   stats[1] = state_rows;
@@ -1515,14 +1660,15 @@ span_la_status span_la_pass_noalloc(const void* q, const void* k, const void* v,
   // the fixed scratch.
   const int H = dims.num_heads;
   DescBlock desc = make_desc(make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
-                                       branch_parent, H, true, num_sms), H);
+                                       branch_parent, H, true, num_sms, one_launch()), H);
   const size_t off_states = align256(desc.host.size());
-  const size_t need = off_states + static_cast<size_t>(desc.state_slots) * kStateFloats * sizeof(float);
+  const size_t off_counter = align256(off_states + static_cast<size_t>(desc.state_slots) * kStateFloats * sizeof(float));
+  const size_t need = off_counter + sizeof(unsigned);
   if (need > kNoAllocScratchBytes)
     return fail(SPAN_LA_ERR_INVALID,
                 "this pass needs %zu bytes of scratch; the fixed scratch of span_la_pass_noalloc holds "
                 "%zu bytes (use span_la_pass)", need, kNoAllocScratchBytes);
-  if (desc.n_out_tiles == 0 && desc.n_scan == 0) return SPAN_LA_OK;
+  if (desc.n_out_tiles == 0 && desc.n_scan == 0 && desc.empty_views.empty()) return SPAN_LA_OK;
 
   // Everything the kernels read from the scratch is written by this call
   // first.  The error word is not cleared here: a wait that ran out stays
@@ -1531,8 +1677,17 @@ span_la_status span_la_pass_noalloc(const void* q, const void* k, const void* v,
   e = cudaStreamIsCapturing(stream, &cap);
   if (e == cudaSuccess) e = upload_descriptors(ws, std::move(desc.host), cap != cudaStreamCaptureStatusNone, stream);
   if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
-  return enqueue_pass(desc, ws, nullptr, reinterpret_cast<float*>(ws + off_states), q, k, v, dims,
+  return enqueue_pass(desc, ws, nullptr, reinterpret_cast<float*>(ws + off_states),
+                      reinterpret_cast<unsigned*>(ws + off_counter), q, k, v, dims,
                       view_state_out, view_state_out, out, err, stream, nullptr, dev);
+}
+
+span_la_status span_la_pass_variant(int32_t variant) {
+  g_detail.clear();
+  if (variant != SPAN_LA_PASS_ONE_LAUNCH && variant != SPAN_LA_PASS_THREE_LAUNCHES)
+    return fail(SPAN_LA_ERR_INVALID, "unknown pass variant %d", variant);
+  g_pass_variant.store(variant, std::memory_order_relaxed);
+  return SPAN_LA_OK;
 }
 
 span_la_status span_la_fault_inject(int32_t kind, int32_t count) {

@@ -70,28 +70,41 @@ struct SpanDesc {
 };
 static_assert(sizeof(SpanDesc) == 16, "SpanDesc layout");
 
-// One tile of the span-output kernel's per-CTA schedule (48 bytes).  CTA c
+// One tile of the span-output kernel's per-CTA schedule (64 bytes).  CTA c
 // runs records [cta_begin[c], cta_begin[c+1]) in order: the tiles of its run.
-// A piece's first tile loads the piece's start state stateA + stateB (the
-// parent view's final state, index into the [n][H][64][64] final-state
-// array, and/or the piece's prefix slot; -1 where absent); every later tile
-// of the piece continues from the state the previous one left.
+// A piece's first tile loads the piece's start state, the sum of two runs of
+// fp32 states:  term A = states stateA .. stateA + a_n - 1 of the A array
+// (the parent view's final state: with three launches the final-state array,
+// [n][H][64][64], a_n = 1; in the one-launch pass the parent view-head's
+// piece states), and term B = slots stateB .. stateB + b_n - 1 of the
+// workspace (the piece's own prefix: one scanned slot with three launches,
+// the earlier pieces' states in the one-launch pass).  A piece flagged
+// kTileCarry starts instead from the final state the same CTA computed at
+// the last tile of the parent view-head (kTileFinalOut), which also writes it
+// to the final-state output (view final_idx).  Every later tile of a piece
+// continues from the state the previous one left.
 constexpr int kInlineBounds = 16;
 constexpr int32_t kTileFirst = 1;      // first tile of its piece: load the start state
 constexpr int32_t kTileLast = 2;       // last tile of its piece: no state update
-constexpr int32_t kTileHasInit = 4;    // the piece has a start state (stateA and/or stateB)
+constexpr int32_t kTileHasInit = 4;    // the piece has a start state
+constexpr int32_t kTileCarry = 8;      // start state: this CTA's last final state
+constexpr int32_t kTileFinalOut = 16;  // last tile of a view-head: compute and write its final state
 struct WorkTile {
   int32_t row0;
   int32_t nrows;
   int32_t head;
   int32_t flags;
-  int32_t stateA;    // parent view (first tile of a piece), -1 if absent
-  int32_t stateB;    // prefix slot (first tile of a piece), -1 if absent
+  int32_t stateA;    // first state of term A (first tile of a piece)
+  int32_t stateB;    // first slot of term B
+  int32_t a_n;       // states in term A (0: none)
+  int32_t b_n;       // slots in term B (0: none)
+  int32_t final_idx; // view of a kTileFinalOut tile (else -1)
   int32_t bound0;    // segment starts in the global bounds table
   int32_t nbound;    // the first kInlineBounds are also inline below
+  int32_t pad;
   uint8_t inl[kInlineBounds];
 };
-static_assert(sizeof(WorkTile) == 48, "WorkTile layout");
+static_assert(sizeof(WorkTile) == 64, "WorkTile layout");
 
 // Softmax-attention layer over the packed rows: one work item = up to 128
 // query rows [r0, r0 + nrows) of one segment (or of several whole short
@@ -181,11 +194,32 @@ cudaError_t launch_span_state(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                               float* ws, const void* prefetch, size_t prefetch_bytes, unsigned* err,
                               cudaStream_t stream);
 
+// The output kernel's arguments.  For the one-launch pass (fused) each CTA
+// first sums K^T V over its phase-1 pieces (p1[p1_begin[c] .. p1_begin[c+1]),
+// slots of `ws`), then counts itself in *counter; a CTA that needs other
+// CTAs' slots waits until *counter reaches n_p1_ctas (the CTAs with phase-1
+// work).  The grid is then launched cooperatively (every CTA resident).
+struct SpanOutputArgs {
+  const WorkTile* work = nullptr;
+  const int32_t* cta_begin = nullptr;
+  int grid = 0;
+  const uint8_t* bounds = nullptr;
+  const float* stateA = nullptr;   // term A array
+  int a_rows = 1;                  // heads per state index of term A (H, or 1 for slots)
+  float* ws = nullptr;             // slots (term B; phase-1 output)
+  float* final_out = nullptr;      // view final states [V][H][64][64]
+  void* out = nullptr;
+  int H = 0;
+  unsigned* err = nullptr;
+  bool pdl = false;
+  bool fused = false;
+  const SpanDesc* p1 = nullptr;
+  const int32_t* p1_begin = nullptr;
+  unsigned* counter = nullptr;
+  int n_p1_ctas = 0;
+};
 cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                               const CUtensorMap* tm_v, const WorkTile* work,
-                               const int32_t* cta_begin, int grid, const uint8_t* bounds,
-                               const float* stateA, const float* stateB, void* out, int H,
-                               unsigned* err, cudaStream_t stream, bool pdl);
+                               const CUtensorMap* tm_v, const SpanOutputArgs& a, cudaStream_t stream);
 
 cudaError_t launch_tile_output(bool split, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                const CUtensorMap* tm_v, const TileDesc* tiles, int n_tiles,

@@ -34,7 +34,7 @@ EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
             "span_la_cache_put", "span_la_cache_contains", "span_la_cache_branches",
             "span_la_cache_stats", "span_la_softmax_pass", "span_la_softmax_branches_from_kv",
             "span_la_fault_inject", "span_la_softmax_plan_stats",
-            "span_la_selftest_wait_timeout_noalloc")
+            "span_la_selftest_wait_timeout_noalloc", "span_la_pass_variant")
 NUM_KERNELS = 7
 
 
@@ -110,6 +110,8 @@ def load_library(path: Optional[str] = None):
                                                    ctypes.c_int32, ctypes.c_int32,
                                                    ctypes.POINTER(ctypes.c_int64)]
         lib.span_la_softmax_plan_stats.restype = ctypes.c_int
+        lib.span_la_pass_variant.argtypes = [ctypes.c_int32]
+        lib.span_la_pass_variant.restype = ctypes.c_int
         lib.span_la_fault_inject.argtypes = [ctypes.c_int32, ctypes.c_int32]
         lib.span_la_fault_inject.restype = ctypes.c_int
         lib.span_la_softmax_branches_from_kv.argtypes = [vp, vp, ctypes.c_int64, i32p, ctypes.c_int32,
@@ -427,6 +429,17 @@ def span_la_selftest_wait_timeout(limit_us: int, stream=None) -> None:
     lib = load_library()
     _raise(lib, lib.span_la_selftest_wait_timeout(int(limit_us), _stream_handle(stream)),
            "span_la_selftest_wait_timeout")
+
+
+PASS_ONE_LAUNCH = 0
+PASS_THREE_LAUNCHES = 1
+
+
+def set_pass_variant(variant: int) -> None:
+    """Process-wide structure of the bf16 pass (``span_la_pass_variant``):
+    ``PASS_ONE_LAUNCH`` (default) or ``PASS_THREE_LAUNCHES``."""
+    lib = load_library()
+    _raise(lib, lib.span_la_pass_variant(int(variant)), "span_la_pass_variant")
 
 
 def span_la_selftest_wait_timeout_noalloc(limit_us: int, stream=None) -> None:

@@ -160,15 +160,21 @@ span_la_status span_la_branches_from_state(const float *cached_state, int32_t nu
  *
  *   arguments        as for span_la_pass; dims.dtype must be SPAN_LA_BF16
  *                    (fp32 inputs need per-call scratch: SPAN_LA_ERR_UNSUPPORTED)
- *   size limit       descriptors plus one 16 KiB fp32 state per piece-head
- *                    must fit in 16 MiB, i.e. about 1,000 piece-heads.  A
- *                    piece is the part of one view inside one SM's run of
- *                    output tiles, so a pass needs at most about
- *                    (views + SMs) x heads of them: a 16-head pass of up to
- *                    ~60 views fits on a 152-SM GPU (the 7,400-token pass
- *                    needs about 170).  A larger pass returns
- *                    SPAN_LA_ERR_INVALID with the bytes it needs, before
- *                    anything is enqueued
+ *   size limit       the descriptors (64 bytes per 128-row output tile of
+ *                    one head) plus the workspace states (16 KiB fp32 each)
+ *                    must fit in 16 MiB.  A piece is the part of one view-
+ *                    head inside one SM's run of output tiles.  In the
+ *                    one-launch structure (the default, span_la_pass_variant)
+ *                    only a piece whose state another SM needs has a
+ *                    workspace state, at most one per boundary between two
+ *                    runs (fewer than the SM count), so the descriptors set
+ *                    the limit: about 200,000 output tiles, i.e. some 25
+ *                    million token-heads.  In the three-launch structure
+ *                    every piece-head has one, about 1,000 in all: a pass
+ *                    needs at most about (views + SMs) x heads of them (a
+ *                    16-head pass of up to ~60 views fits on a 152-SM GPU).
+ *                    A larger pass returns SPAN_LA_ERR_INVALID with the bytes
+ *                    it needs, before anything is enqueued
  *   first call       the first call on a device looks up the array's device
  *                    address (cudaGetSymbolAddress with that device current)
  *                    and caches it; make that first call before any stream
@@ -237,6 +243,27 @@ span_la_status span_la_selftest_wait_timeout(int32_t limit_us, cudaStream_t stre
 span_la_status span_la_selftest_wait_timeout_noalloc(int32_t limit_us, cudaStream_t stream);
 
 /*
+ * span_la_pass_variant -- how span_la_pass and span_la_pass_noalloc run a
+ * bf16 pass (process-wide; calls made afterwards use it).  Both compute the
+ * same result (up to the order of fp32 additions of states):
+ *   SPAN_LA_PASS_ONE_LAUNCH (default): one cooperative launch.  Each CTA
+ *     sums K^T V over its own pieces whose state another CTA needs, counts
+ *     itself in a grid-wide counter, waits (bounded) for the others only
+ *     where it needs their states and sums those itself; the CTA that holds a
+ *     view's last tile computes the view's final state on chip, writes it to
+ *     view_state_out and starts the view's branches in its run from it.  One
+ *     scan per pass without a scan kernel ("Kernels": one scan per pass; the
+ *     small kernels fused).
+ *   SPAN_LA_PASS_THREE_LAUNCHES: span state -> segmented scan -> output, as
+ *     the "Kernels" section lays the pass out.
+ * fp32 passes and span_la_branches_from_state always take the launches of
+ * their own path.  Unknown variant: SPAN_LA_ERR_INVALID.
+ */
+#define SPAN_LA_PASS_ONE_LAUNCH 0
+#define SPAN_LA_PASS_THREE_LAUNCHES 1
+span_la_status span_la_pass_variant(int32_t variant);
+
+/*
  * span_la_fault_inject -- failure-detection hook on the host: with kind
  * SPAN_LA_FAULT_ALLOC, the library's next `count` device allocations
  * (workspace, descriptor blocks) fail as if the device were out of memory,
@@ -266,15 +293,20 @@ span_la_status span_la_softmax_plan_stats(const int32_t *view_cu_seqlens, int32_
 /*
  * span_la_plan_stats -- host only, no CUDA call: the work units a call with
  * this metadata, head count and dtype would launch on a GPU with `num_sms`
- * SMs (used to count the algorithmic bytes of each kernel).  Every count is
- * summed over the heads.
- *   stats[0] state slots: 64-row chunk-heads (fp32) or piece-heads (bf16)
- *   stats[1] row-heads those slots cover (rows whose K and V the state kernel reads)
- *   stats[2] runs of the segmented scan
- *   stats[3] final view states the scan writes (view-heads)
+ * SMs (used to count the algorithmic bytes of each kernel), for the pass
+ * variant in effect (span_la_pass_variant).  Every count is summed over the
+ * heads.
+ *   stats[0] state slots: 64-row chunk-heads (fp32) or piece-heads (bf16);
+ *            in the one-launch pass, the pieces whose state another CTA reads
+ *   stats[1] row-heads those slots cover (rows whose K and V are read to
+ *            make them: by the state kernel, or in the one-launch pass's first
+ *            phase)
+ *   stats[2] runs of the segmented scan (0 in the one-launch pass)
+ *   stats[3] final view states written (view-heads)
  *   stats[4] output tile-heads (<= 128 rows each)
  *   stats[5] row-heads those tiles cover
- *   stats[6] fp32 64x64 start-state reads of the output kernel
+ *   stats[6] fp32 64x64 start-state reads of the output kernel (each state
+ *            of a sum counted)
  *   stats[7] output pieces (fp32: tile-heads)
  *   stats[8] longest run of tiles of one output CTA (bf16; 1 for fp32)
  * from_state != 0 plans span_la_branches_from_state (views ignored).

@@ -134,19 +134,30 @@ def test_injected_allocation_failure_enqueues_nothing(cuda_device):
     assert not torch.isnan(out[: w.rows]).any() and not torch.isnan(state).any()
 
 
-def test_profiler_counts_and_times_every_launch(cuda_device):
+@pytest.mark.parametrize("variant", ["one_launch", "three_launches"])
+def test_profiler_counts_and_times_every_launch(cuda_device, variant):
+    """Three passes launch three span-output kernels, and, in the three-launch
+    structure, three span-state and three scan kernels too; each is timed."""
     w = workloads.single_request(0)
     q, k, v = to_device(w, cuda_device)
-    spanla.profile_reset()
-    spanla.profile_enable(True)
-    for _ in range(3):
-        span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
-    span_la_check()
-    spanla.profile_enable(False)
-    prof = spanla.profile_read()
+    one = variant == "one_launch"
+    spanla.set_pass_variant(spanla.PASS_ONE_LAUNCH if one else spanla.PASS_THREE_LAUNCHES)
+    try:
+        spanla.profile_reset()
+        spanla.profile_enable(True)
+        for _ in range(3):
+            span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+        span_la_check()
+        spanla.profile_enable(False)
+        prof = spanla.profile_read()
+    finally:
+        spanla.profile_enable(False)
+        spanla.set_pass_variant(spanla.PASS_ONE_LAUNCH)
+    launched = ("span_output",) if one else ("span_state", "segmented_scan", "span_output")
     for name in ("span_state", "segmented_scan", "span_output"):
-        assert prof[name]["launches"] == 3 and prof[name]["timed"] == 3
-        assert prof[name]["ms"] > 0
+        n = 3 if name in launched else 0
+        assert prof[name]["launches"] == n and prof[name]["timed"] == n
+        assert (prof[name]["ms"] > 0) == (n > 0)
     assert prof["chunk_state"]["launches"] == 0
 
 

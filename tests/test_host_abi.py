@@ -108,17 +108,24 @@ def test_missing_library_fails_loudly(tmp_path):
         spanla.load_library(str(tmp_path / "nope.so"))
 
 
+@pytest.mark.parametrize("variant", [spanla.PASS_ONE_LAUNCH, spanla.PASS_THREE_LAUNCHES])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("name", ["tiny", "single", "packed4", "cached_long", "sweep4"])
-def test_plan_covers_every_row_once(lib, dtype, name):
-    """The planner's output tiles cover every segment row of every head, its
-    state slots cover exactly the rows of views (and, where a long branch is
-    cut into pieces, of those branches), and it writes one final state per
-    view-head.  Counts are summed over heads."""
+def test_plan_covers_every_row_once(lib, dtype, name, variant):
+    """The planner's output tiles cover every segment row of every head and it
+    writes one final state per view-head.  With three launches the state
+    slots cover exactly the rows of views (and of long branches cut into
+    pieces) and the scan runs once per view-head; the one-launch pass publishes
+    only the pieces another CTA reads, and has no scan.  Counts are summed
+    over heads."""
     from hybrid_linear_attention_packed_gb300 import workloads
     w = workloads.by_name(name)
     H = w.H
-    st = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, H, dtype, num_sms=152)
+    spanla.set_pass_variant(variant)
+    try:
+        st = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, H, dtype, num_sms=152)
+    finally:
+        spanla.set_pass_variant(spanla.PASS_ONE_LAUNCH)
     assert st["tile_rows"] == w.rows * H
     view_rows = int(w.view_lens.sum())
     long_rows = int(sum(L for L in w.branch_lens if L > 128))
@@ -129,15 +136,31 @@ def test_plan_covers_every_row_once(lib, dtype, name):
         assert st["scan_segments"] == (w.V + sum(1 for L in w.branch_lens if L > 128)) * H
         assert st["state_slots"] == H * sum(-(-int(L) // 64) for L in list(w.view_lens)
                                             + [L for L in w.branch_lens if L > 128])
-    else:
+        return
+    # runs of equal length over at least 85 % of the SMs
+    assert st["run_tiles"] <= -(-st["tiles"] // int(0.85 * min(152, st["tiles"])))
+    n_seg = w.V + sum(1 for L in w.branch_lens if L > 128)
+    assert st["state_slots"] <= n_seg * H + 152
+    if variant == spanla.PASS_THREE_LAUNCHES:
         assert view_rows * H <= st["state_rows"] <= (view_rows + long_rows) * H
-        # runs of equal length over at least 85 % of the SMs
-        assert st["run_tiles"] <= -(-st["tiles"] // int(0.85 * min(152, st["tiles"])))
-        # every view-head has one scan run; pieces never outnumber
-        # segment-heads plus run boundaries
         assert st["scan_segments"] >= w.V * H
-        n_seg = w.V + sum(1 for L in w.branch_lens if L > 128)
-        assert st["state_slots"] <= n_seg * H + 152
+    else:
+        assert 0 <= st["state_rows"] <= (view_rows + long_rows) * H
+        assert st["scan_segments"] == 0
+
+
+def test_one_launch_plan_of_a_pass_that_fits_one_run_per_request(lib):
+    """Requests small next to a run: in the one-launch pass a view whose
+    branches all lie in the run that holds its last tile publishes nothing
+    (its CTA computes the final state and starts the branches from it), so
+    passes of many small requests read K and V once."""
+    from hybrid_linear_attention_packed_gb300 import workloads
+    w = workloads.make_pass([130] * 40, [20] * 80, np.repeat(np.arange(40), 2), H=2, dtype="bf16", seed=1)
+    st = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, w.H, "bf16", num_sms=8)
+    assert st["tile_rows"] == w.rows * w.H and st["final_states"] == w.V * w.H
+    assert st["scan_segments"] == 0
+    # at most the view-heads cut by a run boundary publish their pieces
+    assert st["state_slots"] <= 2 * 8
 
 
 @pytest.mark.parametrize("name", ["single", "packed4", "sweep4"])

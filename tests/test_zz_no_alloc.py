@@ -106,26 +106,34 @@ def _many_views(n_views, H=16, rows=64, seed=7):
 
 
 def test_noalloc_size_limit(cuda_device):
-    """The scratch holds descriptors plus one 16 KiB state per piece-head.  60
-    one-tile views of 16 heads need 960 states (15.7 MB with the descriptors):
-    they fit and match span_la_pass; 66 views need 1,056 states (17.3 MB):
-    rejected before anything is enqueued, with the bytes the pass needs."""
+    """The scratch holds descriptors plus the 16 KiB workspace states.  In the
+    three-launch structure every piece-head has one: 60 one-tile views of 16
+    heads need 960 (15.7 MB with the descriptors) and fit and match
+    span_la_pass; 66 views need 1,056 (17.3 MB): rejected before anything is
+    enqueued, with the bytes the pass needs.  The one-launch structure keeps
+    states only across run boundaries, so the 66-view pass fits there."""
     lib = spanla.load_library()
-    st_fit = spanla.plan_stats(_many_views(60).view_cu, [], [], 16, "bf16",
-                               num_sms=torch.cuda.get_device_properties(cuda_device).multi_processor_count)
-    assert st_fit["state_slots"] * 16384 < SCRATCH_BYTES
-    _equal_to_span_la_pass(lib, _many_views(60), cuda_device)
+    nsm = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    spanla.set_pass_variant(spanla.PASS_THREE_LAUNCHES)
+    try:
+        st_fit = spanla.plan_stats(_many_views(60).view_cu, [], [], 16, "bf16", num_sms=nsm)
+        assert st_fit["state_slots"] * 16384 < SCRATCH_BYTES
+        _equal_to_span_la_pass(lib, _many_views(60), cuda_device)
 
-    w = _many_views(66)
-    q = w.q.to(cuda_device)
-    out = torch.full_like(q, float("nan"))
-    state = torch.full((w.V, w.H, 64, 64), float("nan"), dtype=torch.float32, device=cuda_device)
-    st, detail = _noalloc(lib, w, q, q, q, out, state)
-    assert st == 1 and "fixed scratch" in detail
-    need = int(detail.split("needs ")[1].split(" bytes")[0])
-    assert need > SCRATCH_BYTES
-    torch.cuda.synchronize()
-    assert torch.isnan(out).all() and torch.isnan(state).all()   # nothing written
+        w = _many_views(66)
+        q = w.q.to(cuda_device)
+        out = torch.full_like(q, float("nan"))
+        state = torch.full((w.V, w.H, 64, 64), float("nan"), dtype=torch.float32, device=cuda_device)
+        st, detail = _noalloc(lib, w, q, q, q, out, state)
+        assert st == 1 and "fixed scratch" in detail
+        need = int(detail.split("needs ")[1].split(" bytes")[0])
+        assert need > SCRATCH_BYTES
+        torch.cuda.synchronize()
+        assert torch.isnan(out).all() and torch.isnan(state).all()   # nothing written
+    finally:
+        spanla.set_pass_variant(spanla.PASS_ONE_LAUNCH)
+    assert spanla.plan_stats(w.view_cu, [], [], 16, "bf16", num_sms=nsm)["state_slots"] < nsm
+    _equal_to_span_la_pass(lib, w, cuda_device)
 
 
 def test_noalloc_rejects_fp32_inputs(cuda_device):
