@@ -77,6 +77,9 @@ constexpr uint32_t kRowTileBytes = kTileRows * 128;        // 128 rows x 128 B
 constexpr uint32_t kStageBytes = 3 * kRowTileBytes;       // Q K V
 constexpr uint32_t kStateTileBytes = kHeadDim * 128;       // 64 rows x 128 B (bf16)
 constexpr uint32_t kSOpBytes = 2 * kStateTileBytes;         // S as bf16 hi + lo
+constexpr uint32_t kOQuarterBytes = kOutStoreRows * 128;     // 32 rows of O (bf16) on their way out
+static_assert(kOutStoreRows == 32, "one TMA store per warp's rows");
+static_assert(4 * kOQuarterBytes <= kSOpBytes, "O staging fits in one S operand");
 constexpr int kCoordSlots = 64;                              // tile coordinates staged for the producer
 constexpr int kP1Slots = 32;                                 // phase-1 piece records staged
 constexpr uint32_t kTmemCols = 512;
@@ -203,7 +206,8 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ OutParams prm) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const __grid_constant__ OutParams prm) {
   using L = OutSmem;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -239,6 +243,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
 
   // The schedule comes from a copy that completed before the first kernel of
@@ -683,12 +688,26 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     };
 
     // O(i) -> global (rows of the tile only).
-    auto o_work = [&](int i, const TileState& r) -> bool {
+    // Tiles whose O goes out through S operand i & 1 (TMA stores): not a
+    // one-tile piece with a start state (that piece keeps its start state in
+    // the operand for the next one-tile piece: packed branches of one parent,
+    // stored row by row), and at least one whole 32-row group.
+    auto o_through_smem = [&](const TileState& r) {
+      return (r.flags & (kTileFirst | kTileLast | kTileHasInit)) != (kTileFirst | kTileLast | kTileHasInit) &&
+             r.nrows >= 32;
+    };
+    auto o_work = [&](int i, const TileState& r, bool live) -> bool {
       const int b = i & 1;
-      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
+      if (!live || !__all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
         return false;
       tc_fence_after_sync();
       const uint32_t colO = b ? kColO1 : kColO0;
+      // A warp whose 32 rows all lie in the tile writes them, 128-byte
+      // swizzled, into its quarter of S operand b (free: Q S of tile i has
+      // completed) and stores them with one TMA store; otherwise each thread
+      // stores its own row if it lies in the tile.
+      const bool whole = o_through_smem(r) && (quarter + 1) * 32 <= r.nrows;
+      uint8_t* ob = smem + L::kS + b * kSOpBytes + quarter * kOQuarterBytes;
       uint4* dst = reinterpret_cast<uint4*>(
           prm.out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim);
       const bool store = row < r.nrows;
@@ -701,13 +720,24 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tc_fence_before_sync();
           mbar_arrive(bar(L::kOFree + b));
         }
-        if (store) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[4 * h + c] = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c]), __uint_as_float(r0[8 * c + 1])),
-                                        pack_bf16x2(__uint_as_float(r0[8 * c + 2]), __uint_as_float(r0[8 * c + 3])),
-                                        pack_bf16x2(__uint_as_float(r0[8 * c + 4]), __uint_as_float(r0[8 * c + 5])),
-                                        pack_bf16x2(__uint_as_float(r0[8 * c + 6]), __uint_as_float(r0[8 * c + 7])));
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v4 = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c]), __uint_as_float(r0[8 * c + 1])),
+                                      pack_bf16x2(__uint_as_float(r0[8 * c + 2]), __uint_as_float(r0[8 * c + 3])),
+                                      pack_bf16x2(__uint_as_float(r0[8 * c + 4]), __uint_as_float(r0[8 * c + 5])),
+                                      pack_bf16x2(__uint_as_float(r0[8 * c + 6]), __uint_as_float(r0[8 * c + 7])));
+          if (whole)
+            *reinterpret_cast<uint4*>(ob + lane * 128 + (((4 * h + c) ^ (lane & 7)) << 4)) = v4;
+          else if (store)
+            dst[4 * h + c] = v4;
+        }
+      }
+      if (whole) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_o, smem_addr(ob), 0, r.row0 + quarter * 32, r.head);
+          bulk_commit_group();
         }
       }
       return true;
@@ -716,51 +746,71 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // Tile i's dS into the running state; at the last tile of a view-head
     // that is the view's final state: write it out; the branch tiles of this
     // run that start from it (carry) find it in s_run.
-    auto take_ds = [&](int i, const TileState& r) -> bool {
+    // (Without `live`, or when the wait runs out, nothing is read or
+    // written, but the start-state tags change as they would have: they
+    // decide which named barriers the group reaches.)
+    auto take_ds = [&](int i, const TileState& r, bool live) -> bool {
       const int b = i & 1;
-      if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kDReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
-        return false;
-      tc_fence_after_sync();
+      const bool good =
+          live && __all_sync(0xffffffffu, wait_or_flag(bar(L::kDReady + b), (i >> 1) & 1, err, kErrTimeoutMma));
+      if (good) tc_fence_after_sync();
       if (!(r.flags & kTileLast) || (r.flags & kTileFinalOut)) {
-        uint32_t r0[32];
-        tmem_ld_32cols(tmem + lane_base + (b ? kColD1 : kColD0) + 32 * sh, r0);
-        tmem_ld_wait();
+        if (good) {
+          uint32_t r0[32];
+          tmem_ld_32cols(tmem + lane_base + (b ? kColD1 : kColD0) + 32 * sh, r0);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s_run[e] += __uint_as_float(r0[e]);
+          for (int e = 0; e < 32; ++e) s_run[e] += __uint_as_float(r0[e]);
+        }
         tag_run = -1;
       }
-      tc_fence_before_sync();
-      mbar_arrive(bar(L::kDFree + b));
+      if (good) {
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kDFree + b));
+      }
       if (r.flags & kTileFinalOut) {
-        store_half_row(prm.final_out + (static_cast<int64_t>(r.final_idx) * H + r.head) * kStateFloats + half_row,
-                       s_run);
+        if (good)
+          store_half_row(
+              prm.final_out + (static_cast<int64_t>(r.final_idx) * H + r.head) * kStateFloats + half_row, s_run);
         tag_run = carry_tag(r.final_idx, r.head);
       }
-      return true;
+      return good;
     };
 
     if (ok) griddep_wait();   // start states from the scan (three launches)
-    if (ok && n > 0) {
+    // The group's named barriers (here, in the start-state sum and in the
+    // grid-wide wait) are reached by all four warps alike: where they fall
+    // depends on the tiles and the start-state tags only.  A warp whose
+    // bounded wait ran out goes on through the loop without waiting, reading
+    // or writing results (the error word is set; the pass is void).
+    if (n > 0) {
       TileState cur = load_state(list);
       TileState nxt = n > 1 ? load_state(list + 1) : TileState{};
       start_piece(0, cur);
       stage(0, cur);
-      for (int i = 0; i < n && ok; ++i) {
+      bool prev_smem = false;   // O(i-1) went out through S operand (i+1) & 1
+      for (int i = 0; i < n; ++i) {
         // S(i+1) first: the O issuer needs it right after P V of tile i+1.
+        if (i + 1 < n || (cur.flags & kTileFinalOut)) ok = take_ds(i, cur, ok);
         if (i + 1 < n) {
-          ok = take_ds(i, cur);
-          if (!ok) break;
+          if (prev_smem) {
+            // The TMA stores of O(i-1) have left S operand (i+1) & 1.
+            if (lane == 0) bulk_wait_read_all();
+            ok = named_barrier_and(kNamedStateBar, kGroupThreads, ok);
+          }
           if (cur.flags & kTileLast) start_piece(i + 1, nxt);
           stage(i + 1, nxt);
-        } else if (cur.flags & kTileFinalOut) {
-          ok = take_ds(i, cur);
-          if (!ok) break;
         }
-        ok = o_work(i, cur);
+        ok = o_work(i, cur, ok);
+        prev_smem = o_through_smem(cur);
+        if (prev_smem) {   // S operand i & 1 no longer holds a start state
+          if (i & 1) tag_op1 = -1; else tag_op0 = -1;
+        }
         cur = nxt;
         if (i + 2 < n) nxt = load_state(list + i + 2);
       }
     }
+    if (lane == 0) bulk_wait_all();   // the last O stores have completed
   }
 
   griddep_launch_dependents();
@@ -773,7 +823,8 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 }  // namespace
 
 cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                               const CUtensorMap* tm_v, const SpanOutputArgs& a, cudaStream_t stream) {
+                               const CUtensorMap* tm_v, const CUtensorMap* tm_o, const SpanOutputArgs& a,
+                               cudaStream_t stream) {
   if (a.grid <= 0) return cudaSuccess;
   const uint32_t bytes = OutSmem::kRequest;
   static std::atomic<uint64_t> done{0};
@@ -811,7 +862,7 @@ cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
   }
   cfg.attrs = attr;
   cfg.numAttrs = (a.fused || a.pdl) ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, span_output_kernel, tm_q[0], tm_k[0], tm_v[0], p);
+  return cudaLaunchKernelEx(&cfg, span_output_kernel, tm_q[0], tm_k[0], tm_v[0], *tm_o, p);
 }
 
 }  // namespace spanla

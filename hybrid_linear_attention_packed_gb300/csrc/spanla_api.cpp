@@ -869,6 +869,8 @@ struct MapCache {
   int H = 0;
   bool span_mode = false;
   DeviceOperands tile_ops{}, chunk_ops{};
+  const void* o = nullptr;     // output array of tm_o
+  CUtensorMap tm_o{};
 };
 MapCache g_maps[kMaxDevices];
 
@@ -1004,6 +1006,17 @@ span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t
     }
   }
   if (st != SPAN_LA_OK) return st;
+  // The span-output kernel stores whole 32-row groups of O with TMA.
+  CUtensorMap tm_o{};
+  const bool span_out = desc.span_mode && desc.n_out_tiles > 0;
+  if (span_out) {
+    if (mc != nullptr && mc->valid && map_hit && mc->o == out) {
+      tm_o = mc->tm_o;
+    } else {
+      st = encode_map(&tm_o, out, T, H, kOutStoreRows, 1);
+      if (st != SPAN_LA_OK) return st;
+    }
+  }
   if (mc != nullptr && !split && need_maps && !map_hit) {
     mc->valid = true;
     mc->device = device;
@@ -1015,6 +1028,11 @@ span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t
     mc->span_mode = desc.span_mode;
     mc->tile_ops = tile_ops;
     mc->chunk_ops = chunk_ops;
+    mc->o = nullptr;
+  }
+  if (mc != nullptr && span_out && mc->valid && !split) {
+    mc->o = out;
+    mc->tm_o = tm_o;
   }
 
   if (desc.fused) {
@@ -1044,7 +1062,7 @@ span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t
       a.counter = counter;
       a.n_p1_ctas = desc.n_p1_ctas;
       e = counted_launch(kKernelSpanOutput, stream, [&] {
-        return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v, a, stream);
+        return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v, &tm_o, a, stream);
       });
       if (e != cudaSuccess) return cuda_fail(e, "one-launch pass");
     }
@@ -1094,7 +1112,7 @@ span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t
       a.err = err;
       a.pdl = pdl;
       e = counted_launch(kKernelSpanOutput, stream, [&] {
-        return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v, a, stream);
+        return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v, &tm_o, a, stream);
       });
     } else {
       e = counted_launch(kKernelTile, stream, [&] {

@@ -218,8 +218,12 @@ struct SpanOutputArgs {
   unsigned* counter = nullptr;
   int n_p1_ctas = 0;
 };
+// tm_q/k/v: 128-row boxes of one head; tm_o: the output array, 32-row boxes
+// of one head (a warp's rows, stored with one TMA store when all lie in the
+// tile).
 cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                               const CUtensorMap* tm_v, const SpanOutputArgs& a, cudaStream_t stream);
+                               const CUtensorMap* tm_v, const CUtensorMap* tm_o, const SpanOutputArgs& a,
+                               cudaStream_t stream);
 
 cudaError_t launch_tile_output(bool split, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                const CUtensorMap* tm_v, const TileDesc* tiles, int n_tiles,
@@ -240,5 +244,6 @@ constexpr int kChunkBoxRows = kChunk;     // chunk-state kernel: 64 rows x 2 hea
 constexpr int kChunkBoxHeads = 2;
 constexpr int kSpanBoxRows = 4 * kChunk;  // span-state kernel: 256 rows x 1 head
 constexpr int kTileBoxRows = kTileRows;   // tile-output kernel: 128 rows x 1 head
+constexpr int kOutStoreRows = 32;         // span-output kernel's O stores: 32 rows x 1 head
 
 }  // namespace spanla
