@@ -824,18 +824,54 @@ def main():
         KC = min(K, 240)
         cs = [torch.cuda.Event(enable_timing=True) for _ in range(KC)]
         ce = [torch.cuda.Event(enable_timing=True) for _ in range(KC)]
-        chost = []
         for i in range(KC):
             flush.zero_()
             cs[i].record(stream)
-            t_h = time.perf_counter()
             cold_call(i % NV)
-            chost.append((time.perf_counter() - t_h) * 1e6)
             ce[i].record(stream)
         torch.cuda.synchronize()
         spanla.span_la_check()
         cms = statistics.mean(a.elapsed_time(b) for a, b in zip(cs, ce))
+        # Host time of one call that builds a new plan, with the device busy
+        # on earlier work (as in a serving loop) but no backlog of calls
+        # ahead of it: the loop above runs ahead of the device, so its host
+        # times would measure the device's pace, not the host's cost.
+        cbusy = torch.empty(256 << 20, dtype=torch.float32, device=dev)
+        chost = []
+        for i in range(2 * NV):
+            torch.cuda.synchronize()
+            cbusy.zero_()
+            t_h = time.perf_counter()
+            cold_call((i + 1) % NV)
+            chost.append((time.perf_counter() - t_h) * 1e6)
+        torch.cuda.synchronize()
+        spanla.span_la_check()
+        # The same through the C entry point with prepared arguments (the
+        # library's own cost of a new plan, without the Python binding).
+        chost_c = None
+        if not shards_mode:
+            lib_c = spanla.load_library()
+            dims_c = spanla.Dims(q.shape[0], q.shape[1], 64,
+                                 spanla.SPAN_LA_BF16 if w.dtype == "bf16" else spanla.SPAN_LA_F32)
+            vcu_c = np.ascontiguousarray(w.view_cu, dtype=np.int32)
+            prep = [(np.ascontiguousarray(b_, dtype=np.int32), np.ascontiguousarray(p_, dtype=np.int32))
+                    for b_, p_ in variants]
+            raw_c = [(q.data_ptr(), k.data_ptr(), v.data_ptr(), dims_c, vcu_c.ctypes.data, len(vcu_c) - 1,
+                      b_.ctypes.data, len(b_) - 1, p_.ctypes.data, out.data_ptr(), state.data_ptr(),
+                      stream.cuda_stream) for b_, p_ in prep]
+            chost_c = []
+            for i in range(2 * NV):
+                torch.cuda.synchronize()
+                cbusy.zero_()
+                t_h = time.perf_counter()
+                st_c = lib_c.span_la_pass(*raw_c[(i + 1) % NV])
+                chost_c.append((time.perf_counter() - t_h) * 1e6)
+                assert st_c == 0
+            torch.cuda.synchronize()
+            spanla.span_la_check()
+        del cbusy
         cold = {"cold_plan_ms_per_step": cms, "cold_plan_host_us": statistics.median(chost),
+                "cold_plan_host_us_c_abi": statistics.median(chost_c) if chost_c else None,
                 "cold_plan_value": rows_per_step / (cms / 1e3), "variants": NV, "steps": KC,
                 "mode": "branch lengths permuted within each parent's run of branches: a new "
                         "plan (host build + descriptor upload) in every step"}

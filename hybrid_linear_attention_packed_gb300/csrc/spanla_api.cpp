@@ -783,6 +783,77 @@ cudaError_t upload_descriptors(void* dst, std::vector<uint8_t>&& bytes, bool cap
   return cudaMemcpyAsync(dst, kept.data(), kept.size(), cudaMemcpyHostToDevice, stream);
 }
 
+// ------------------------------------------------------------------ pinned staging
+// Cached descriptor blocks go to the device through pinned host buffers: a
+// copy from pageable memory makes the calling thread wait until the stream's
+// earlier work has finished, which puts the whole queue ahead of the pass on
+// the host's critical path.  A buffer is reused once the copy that read it has
+// completed (one event per buffer), so the pool holds as many buffers as
+// uploads in flight at once, up to kPinnedBufs per device; past that an upload
+// waits for the oldest copy.
+constexpr size_t kPinnedBufs = 16;
+constexpr size_t kPinnedMinBytes = 64 << 10;
+struct PinnedBuf {
+  int device = -1;
+  uint8_t* p = nullptr;
+  size_t cap = 0;
+  cudaEvent_t done = nullptr;   // recorded after the copy that read it
+  uint64_t used = 0;
+};
+std::mutex g_pin_mu;
+std::vector<PinnedBuf> g_pin;
+uint64_t g_pin_clock = 0;
+
+// True when the copy that last read `b` has completed.
+bool pinned_free(const PinnedBuf& b) {
+  const cudaError_t q = cudaEventQuery(b.done);
+  if (q == cudaErrorNotReady) (void)cudaGetLastError();   // not an error: clear it
+  return q == cudaSuccess;
+}
+
+cudaError_t upload_pinned(void* dst, const std::vector<uint8_t>& bytes, int device, cudaStream_t stream) {
+  if (bytes.empty()) return cudaSuccess;
+  const size_t n = bytes.size();
+  std::lock_guard<std::mutex> lock(g_pin_mu);
+  PinnedBuf* pick = nullptr;
+  size_t mine = 0;
+  for (auto& b : g_pin) {
+    if (b.device != device) continue;
+    ++mine;
+    if (b.cap >= n && pinned_free(b) && (pick == nullptr || b.cap < pick->cap)) pick = &b;
+  }
+  cudaError_t e = cudaSuccess;
+  if (pick == nullptr) {
+    if (mine < kPinnedBufs) {
+      PinnedBuf nb;
+      nb.device = device;
+      e = cudaEventCreateWithFlags(&nb.done, cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+      g_pin.push_back(nb);
+      pick = &g_pin.back();
+    } else {   // the least recently used buffer of this device, once its copy is done
+      for (auto& b : g_pin)
+        if (b.device == device && (pick == nullptr || b.used < pick->used)) pick = &b;
+      e = cudaEventSynchronize(pick->done);
+    }
+    if (e == cudaSuccess && pick->cap < n) {
+      if (pick->p != nullptr) cudaFreeHost(pick->p);
+      pick->p = nullptr;
+      pick->cap = 0;
+      size_t cap = kPinnedMinBytes;
+      while (cap < n) cap *= 2;
+      e = cudaHostAlloc(reinterpret_cast<void**>(&pick->p), cap, cudaHostAllocPortable);
+      if (e == cudaSuccess) pick->cap = cap;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  std::memcpy(pick->p, bytes.data(), n);
+  e = cudaMemcpyAsync(dst, pick->p, n, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaEventRecord(pick->done, stream);
+  pick->used = ++g_pin_clock;
+  return e;
+}
+
 // ------------------------------------------------------------------ plan cache
 // Passes with the same metadata (every layer of a model step, for instance)
 // reuse one uploaded descriptor block: the plan depends on the metadata, the
@@ -929,8 +1000,7 @@ span_la_status cached_block(const std::vector<int32_t>& key, int device, cudaStr
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&en.d_block), bytes, stream);
   if (e != cudaSuccess)
     return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(descriptors, %zu): %s", bytes, cudaGetErrorString(e));
-  if (!en.desc.host.empty())
-    e = cudaMemcpyAsync(en.d_block, en.desc.host.data(), en.desc.host.size(), cudaMemcpyHostToDevice, stream);
+  e = upload_pinned(en.d_block, en.desc.host, device, stream);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&en.uploaded, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventRecord(en.uploaded, stream);
   if (e != cudaSuccess) {
