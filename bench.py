@@ -772,7 +772,7 @@ def main():
         kk["share"] = kk["avg_us"] / tot
     dom = max(kernels, key=lambda n: kernels[n]["avg_us"])
     dk = kernels[dom]
-    traffic = recorded_traffic(dom, args.workload)
+    traffic = recorded_traffic(dom, args.workload + ("/three" if args.pass_variant == "three" else ""))
     roofline = {"bound": "hbm", "kernel": dom, "achieved": dk["gbs"], "peak": hbm_peak,
                 "unit": "GB/s", "frac": dk["gbs"] / hbm_peak, "traffic": traffic,
                 "peak_source": peak_src,
