@@ -343,9 +343,13 @@ def workload_config(w, name: str) -> dict:
     return cfg
 
 
+def pass_structure(args) -> str:
+    """The bf16 pass structure this run used (a top-level key of the line, not
+    part of `config`: the workload is the same whichever structure runs it)."""
+    return "three launches" if getattr(args, "pass_variant", "one") == "three" else "one launch"
+
+
 def add_mode(cfg: dict, args) -> dict:
-    cfg = dict(cfg, **{"pass": "three launches" if getattr(args, "pass_variant", "one") == "three"
-                       else "one launch"})
     if getattr(args, "cache", False) and args.workload == "cached_long":
         cfg = dict(cfg, step="span_la_cache_branches by key over the view-state cache, 4 shards of "
                              "64 branches; tokens/s counts branch rows")
@@ -1091,6 +1095,7 @@ def main():
                 "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": vs, "dtype": w.dtype, "data": "synthetic",
                 "config": dict(add_mode(workload_config(w, args.workload), args), parallelism="dp%d" % world),
+                "pass_structure": pass_structure(args),
                 "roofline": roofline, "pass_roofline": pass_roofline,
                 "kernels": kernels, "plan": plan,
                 "cpu_baseline": cpu,

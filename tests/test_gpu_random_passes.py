@@ -2,7 +2,8 @@
 float64 oracles, element by element: view and branch lengths drawn from a
 wide range (empty segments, single rows, multi-tile views and branches), 1 to
 3 heads, both input types for the linear pass, several scales for the softmax
-layer, rows of no segment between the segments.
+layer, rows of no segment between the segments; and 16-head passes of up to
+8 requests in both structures of the bf16 pass (one launch, three launches).
 
 Tolerances as in the other parity tests: max|o_gpu - o_ref| / max|o_ref| <=
 1e-3 (fp32 inputs) or 1e-2 (bf16 inputs); the view states likewise; lse
@@ -14,7 +15,7 @@ import torch
 
 from helpers import TOL, f64, rel_err, segment_rows, to_device
 from hybrid_linear_attention_packed_gb300 import (span_la_check, span_la_pass, span_la_softmax_pass,
-                                                  workloads)
+                                                  spanla, workloads)
 from oracle import oracle_pass, oracle_softmax_pass
 
 pytestmark = pytest.mark.gpu
@@ -40,7 +41,38 @@ def _random_pass(seed, dtype, q_scale=1.0 / 8, k_scale=1.0 / 8):
 @pytest.mark.parametrize("seed", range(8))
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_random_linear_passes(cuda_device, seed, dtype):
-    w = _random_pass(seed, dtype)
+    _check_random_linear(cuda_device, _random_pass(seed, dtype), seed, dtype)
+
+
+def _random_wide_pass(seed):
+    """16 heads and up to 8 requests of up to 3,000-row views with up to 40
+    branches each: the plan cuts every head's tiles into several runs, so
+    pieces, workspace states, carried final states and branch tiles in other
+    runs all occur."""
+    rng = np.random.default_rng([seed, 91])
+    V = int(rng.integers(1, 9))
+    view_lens = [int(rng.integers(0, 3000)) for _ in range(V)]
+    lens, parents = [], []
+    for v in range(V):
+        for _ in range(int(rng.integers(0, 41))):
+            lens.append(int(rng.choice([1, 16, 40, 96, 128, 129, 300])))
+            parents.append(v)
+    return workloads.make_pass(view_lens, lens, parents, H=16, dtype="bf16", seed=1000 + seed,
+                               lead_rows=int(rng.integers(0, 20)), mid_rows=int(rng.integers(0, 20)),
+                               tail_rows=int(rng.integers(0, 20)))
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("structure", ["one_launch", "three_launches"])
+def test_random_wide_passes_both_structures(cuda_device, seed, structure):
+    spanla.set_pass_variant(spanla.PASS_ONE_LAUNCH if structure == "one_launch" else spanla.PASS_THREE_LAUNCHES)
+    try:
+        _check_random_linear(cuda_device, _random_wide_pass(seed), seed, "bf16")
+    finally:
+        spanla.set_pass_variant(spanla.PASS_ONE_LAUNCH)
+
+
+def _check_random_linear(cuda_device, w, seed, dtype):
     q, k, v = to_device(w, cuda_device)
     out = torch.full_like(q, float("nan"))
     out, state = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, out=out)
