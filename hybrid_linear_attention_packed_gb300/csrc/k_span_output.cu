@@ -79,6 +79,7 @@ constexpr uint32_t kStateTileBytes = kHeadDim * 128;       // 64 rows x 128 B (b
 constexpr uint32_t kSOpBytes = 2 * kStateTileBytes;         // S as bf16 hi + lo
 constexpr uint32_t kOQuarterBytes = kOutStoreRows * 128;     // 32 rows of O (bf16) on their way out
 static_assert(kOutStoreRows == 32, "one TMA store per warp's rows");
+static_assert(kFirstLoads <= kStages, "the set-up loads use fresh stages");
 static_assert(4 * kOQuarterBytes <= kSOpBytes, "O staging fits in one S operand");
 constexpr int kCoordSlots = 64;                              // tile coordinates staged for the producer
 constexpr int kP1Slots = 32;                                 // phase-1 piece records staged
@@ -102,7 +103,6 @@ struct OutSmem {
                        kP1Ready = kPReady + 14, kP1Free = kPReady + 16, kP1Done = kPReady + 18,
                        kNumBars = kPReady + 19;
   static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
-  static constexpr uint32_t kN1 = kTmemSlot + 4;                  // phase-1 tiles of this CTA
   static constexpr uint32_t kCoord = kTmemSlot + 8;              // (row0, head) of the first tiles
   static constexpr uint32_t kP1 = kCoord + 8 * kCoordSlots;      // phase-1 piece records
   static constexpr uint32_t kBytes = kP1 + sizeof(SpanDesc) * kP1Slots;
@@ -112,6 +112,7 @@ static_assert(OutSmem::kRequest <= 227 * 1024, "shared memory budget");
 
 // Kernel parameters besides the tensor maps (see SpanOutputArgs).
 struct OutParams {
+  const CtaHead* heads;
   const WorkTile* work;
   const int32_t* cta_begin;
   const uint8_t* bounds;
@@ -222,6 +223,13 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   auto bar = [&](int slot) { return base + L::kBar + 8u * slot; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
+  // This CTA's set-up record: one round trip (the descriptors were uploaded
+  // before the launch, but an L2 flush may have sent them back to DRAM).
+  const int4* hd = reinterpret_cast<const int4*>(prm.heads + blockIdx.x);
+  const int4 h0 = __ldg(hd), h1 = __ldg(hd + 1);
+  const int i_begin = h0.x, n = h0.y, p1_begin = h0.z, n_p1 = h0.w;
+  const int n1 = h1.x;         // phase-1 tiles
+  const int n_first = h1.y;    // loads issued during the set-up
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(L::kFull + s), 1);
@@ -240,42 +248,41 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     mbar_init(bar(L::kP1Done), kGroupThreads);
     fence_mbar_init();
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
+    // The first loads (phase-1 K and V, then the run's Q, K and V) go out
+    // now, while the rest of the set-up completes; the stages are fresh.
+    const int4 f0 = __ldg(hd + 2), f1 = __ldg(hd + 3);
+    const int fr[2 * kFirstLoads] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+    for (int u = 0; u < kFirstLoads; ++u) {
+      if (u < n_first) {
+        const uint32_t st = base + L::kStage0 + u * kStageBytes;
+        if (u < n1) {
+          mbar_arrive_expect_tx(bar(L::kFull + u), 2 * kRowTileBytes);
+        } else {
+          mbar_arrive_expect_tx(bar(L::kFull + u), kStageBytes);
+          tma_load_3d(st + L::kQ, &tm_q, bar(L::kFull + u), 0, fr[2 * u], fr[2 * u + 1]);
+        }
+        tma_load_3d(st + L::kK, &tm_k, bar(L::kFull + u), 0, fr[2 * u], fr[2 * u + 1]);
+        tma_load_3d(st + L::kV, &tm_v, bar(L::kFull + u), 0, fr[2 * u], fr[2 * u + 1]);
+      }
+    }
     tma_prefetch_desc(&tm_o);
   }
 
-  // The schedule comes from a copy that completed before the first kernel of
-  // the pass began, and Q, K, V from before that: every role but the one that
-  // reads the start states runs ahead of the previous kernel's completion.
-  const int i_begin = prm.cta_begin[blockIdx.x];
-  const int n = prm.cta_begin[blockIdx.x + 1] - i_begin;
   const WorkTile* list = prm.work + i_begin;
-  // Phase-1 pieces of this CTA (one-launch pass only).
-  const int p1_begin = prm.fused ? prm.p1_begin[blockIdx.x] : 0;
-  const int n_p1 = prm.fused ? prm.p1_begin[blockIdx.x + 1] - p1_begin : 0;
-  const SpanDesc* p1 = prm.p1 + p1_begin;
+  const SpanDesc* p1 = prm.p1 + p1_begin;   // phase-1 pieces (one-launch pass only)
   int2* coord = reinterpret_cast<int2*>(smem + L::kCoord);
   SpanDesc* p1s = reinterpret_cast<SpanDesc*>(smem + L::kP1);
   // Warp 0 stages the producer's tile coordinates and the phase-1 pieces
   // (loads issued before the CTA-wide set-up completes, so their latency
-  // overlaps it) and counts the phase-1 tiles.
+  // overlaps it).
   if (warp == 0) {
     int2 c_lo = make_int2(0, 0), c_hi = make_int2(0, 0);
     if (lane < n) c_lo = make_int2(list[lane].row0, list[lane].head);
     if (lane + 32 < n && lane + 32 < kCoordSlots) c_hi = make_int2(list[lane + 32].row0, list[lane + 32].head);
-    int tiles1 = 0;
-    for (int j = lane; j < n_p1; j += 32) {
-      const SpanDesc sd = p1[j];
-      if (j < kP1Slots) p1s[j] = sd;
-      tiles1 += (sd.len + kTileRows - 1) / kTileRows;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tiles1 += __shfl_xor_sync(0xffffffffu, tiles1, o);
+    for (int j = lane; j < n_p1 && j < kP1Slots; j += 32) p1s[j] = p1[j];
     if (lane < n) coord[lane] = c_lo;
     if (lane + 32 < n && lane + 32 < kCoordSlots) coord[lane + 32] = c_hi;
-    if (lane == 0) *reinterpret_cast<int*>(smem + L::kN1) = tiles1;
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -285,7 +292,6 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const int n1 = *reinterpret_cast<const int*>(smem + L::kN1);   // phase-1 tiles
   auto p1_of = [&](int j) { return j < kP1Slots ? p1s[j] : p1[j]; };
 
   if (warp == 0) {
@@ -296,6 +302,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       for (int j = 0; j < n_p1 && ok; ++j) {
         const SpanDesc sd = p1_of(j);
         for (int r = 0; r < sd.len && ok; r += kTileRows, ++u) {
+          if (u < n_first) continue;   // issued during the set-up
           const int s = u % kStages;
           if (!wait_or_flag(bar(L::kEmpty + s), ((u / kStages) & 1) ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
           const uint32_t st = base + L::kStage0 + s * kStageBytes;
@@ -305,6 +312,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
       }
       for (int i = 0; i < n && ok; ++i, ++u) {
+        if (u < n_first) continue;   // issued during the set-up
         const int2 rc = i < kCoordSlots ? coord[i] : make_int2(list[i].row0, list[i].head);
         const int s = u % kStages;
         if (!wait_or_flag(bar(L::kEmpty + s), ((u / kStages) & 1) ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
@@ -831,6 +839,7 @@ cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
   cudaError_t e = set_smem_limit_once(span_output_kernel, bytes, done);
   if (e != cudaSuccess) return e;
   OutParams p{};
+  p.heads = a.heads;
   p.work = a.work;
   p.cta_begin = a.cta_begin;
   p.bounds = a.bounds;

@@ -721,7 +721,7 @@ span_la_status encode_map(CUtensorMap* map, const void* base, int64_t T, int H, 
 // need to know about it.
 struct DescBlock {
   std::vector<uint8_t> host;
-  size_t off_scan = 0, off_bounds = 0, off_a = 0, off_b = 0, off_c = 0, off_d = 0;
+  size_t off_scan = 0, off_bounds = 0, off_a = 0, off_b = 0, off_c = 0, off_d = 0, off_h = 0;
   int grid = 0;            // span_output CTAs (span mode)
   int state_grid = 0;      // span_state CTAs (span mode)
   int n_scan = 0, n_chunks = 0, n_tiles = 0;
@@ -748,6 +748,34 @@ DescBlock make_desc(const Plan& plan, int H) {
     d.off_c = put(d.host, plan.cta_begin);
     d.grid = plan.out_grid();
     d.state_grid = plan.state_grid();
+    // Output CTAs' set-up records (phase-1 pieces are per output CTA only in
+    // the one-launch pass; in three launches `spans` belong to span_state).
+    std::vector<CtaHead> heads(static_cast<size_t>(d.grid));
+    for (int c = 0; c < d.grid; ++c) {
+      CtaHead& h = heads[c];
+      h = CtaHead{};
+      h.i_begin = plan.cta_begin[c];
+      h.n = plan.cta_begin[c + 1] - plan.cta_begin[c];
+      if (plan.fused) {
+        h.p1_begin = plan.span_begin[c];
+        h.n_p1 = plan.span_begin[c + 1] - plan.span_begin[c];
+      }
+      for (int j = 0; j < h.n_p1; ++j) {
+        const SpanDesc& sd = plan.spans[h.p1_begin + j];
+        for (int32_t r = 0; r < sd.len; r += kTileRows, ++h.n1)
+          if (h.n_first < kFirstLoads) {
+            h.first[2 * h.n_first] = sd.row0 + r;
+            h.first[2 * h.n_first + 1] = sd.head;
+            ++h.n_first;
+          }
+      }
+      for (int i = 0; i < h.n && h.n_first < kFirstLoads; ++i, ++h.n_first) {
+        const WorkTile& w = plan.work[h.i_begin + i];
+        h.first[2 * h.n_first] = w.row0;
+        h.first[2 * h.n_first + 1] = w.head;
+      }
+    }
+    d.off_h = put(d.host, heads);
   } else {
     d.off_a = put(d.host, plan.chunks);
     d.off_b = put(d.host, plan.tiles);
@@ -1115,6 +1143,7 @@ span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(pass counter)");
     if (desc.n_out_tiles > 0) {
       SpanOutputArgs a;
+      a.heads = reinterpret_cast<const CtaHead*>(block + desc.off_h);
       a.work = reinterpret_cast<const WorkTile*>(block + desc.off_b);
       a.cta_begin = reinterpret_cast<const int32_t*>(block + desc.off_c);
       a.grid = desc.grid;
@@ -1169,6 +1198,7 @@ span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t
     const bool pdl = kernel_before;
     if (desc.span_mode) {
       SpanOutputArgs a;
+      a.heads = reinterpret_cast<const CtaHead*>(block + desc.off_h);
       a.work = reinterpret_cast<const WorkTile*>(block + desc.off_b);
       a.cta_begin = reinterpret_cast<const int32_t*>(block + desc.off_c);
       a.grid = desc.grid;

@@ -199,7 +199,24 @@ cudaError_t launch_span_state(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
 // slots of `ws`), then counts itself in *counter; a CTA that needs other
 // CTAs' slots waits until *counter reaches n_p1_ctas (the CTAs with phase-1
 // work).  The grid is then launched cooperatively (every CTA resident).
+// One span-output CTA's set-up record, at a fixed stride, so that the CTA
+// reads it in one round trip and its producer issues the first loads before
+// the rest of the set-up: its tile records, its phase-1 pieces, its phase-1
+// tiles (loads before the run's tiles) and the (row0, head) of its first
+// kFirstLoads loads in load order (phase-1 K/V boxes first).
+constexpr int kFirstLoads = 4;
+struct CtaHead {
+  int32_t i_begin, n;          // tile records [i_begin, i_begin + n)
+  int32_t p1_begin, n_p1;      // phase-1 pieces (one-launch pass)
+  int32_t n1;                  // phase-1 tiles
+  int32_t n_first;             // entries of `first`
+  int32_t pad[2];
+  int32_t first[2 * kFirstLoads];
+};
+static_assert(sizeof(CtaHead) == 64, "CtaHead is 64 bytes");
+
 struct SpanOutputArgs {
+  const CtaHead* heads = nullptr;
   const WorkTile* work = nullptr;
   const int32_t* cta_begin = nullptr;
   int grid = 0;
