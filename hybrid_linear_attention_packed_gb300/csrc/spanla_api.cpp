@@ -4,11 +4,15 @@
 // diagnostics (status text, profiling counters, fault injection).
 //
 // A pass ("Serving 0.88M TPS from Two RTXs and Mac Minis", section "Kernels":
-// one scan per pass in three launches) is enqueued as
-//   span state -> segmented scan -> span output (views + branch fork)
-// for bf16 inputs (chunk state -> scan -> tile output for fp32 inputs), over
-// descriptor tables built here from the host metadata, so that each kernel is
-// one launch for the whole pass however many views and branches it holds.
+// one scan per pass, the small kernels fused) is enqueued, for bf16 inputs,
+// as one cooperative launch of the span-output kernel (phase 1: the local
+// states other SMs need; a grid-wide counter; then each SM sums the start
+// states it needs and runs its output tiles, branch fork included), or, as
+// the page lays it out, as span state -> segmented scan -> span output
+// (span_la_pass_variant); for fp32 inputs as chunk state -> scan -> tile
+// output.  Every launch covers the whole pass however many views and
+// branches it holds, from descriptor tables built here from the host
+// metadata.
 // The softmax layer over the same rows is one launch (section "Softmax
 // layer" below).
 #include <algorithm>

@@ -15,12 +15,15 @@
  * (section "The Workload": branches attend to the view but not to each other).
  * The work follows the chunked form the "Kernels" section describes (each
  * chunk a few 64x64 matrix products; one scan of states covers every view of
- * the pass, in three launches): a local state K^T V per piece of rows, one
- * segmented prefix scan over every view of the pass, and the output of every
- * 128-row tile (masked Q K^T V inside the tile plus Q S_prev).  For bf16
- * inputs the output work is cut into one run of tiles per SM; a piece is the
- * part of one view (per head) inside one run, and the output kernel carries
- * the state from tile to tile on chip.  For fp32 inputs the pieces are
+ * the pass): a local state K^T V per piece of rows, the prefix of those states
+ * over every view of the pass, and the output of every 128-row tile (masked
+ * Q K^T V inside the tile plus Q S_prev).  For bf16 inputs the output work is
+ * cut into one run of tiles per SM; a piece is the part of one view (per
+ * head) inside one run, and the output kernel carries the state from tile to
+ * tile on chip.  By default the whole bf16 pass is one cooperative launch
+ * (the SMs sum the prefixes they need after a grid-wide counter); the
+ * page's three launches (local states, one segmented scan, output) are the
+ * alternative span_la_pass_variant selects.  For fp32 inputs the pieces are
  * 64-row chunks and every 128-row tile starts from its chunk's prefix.
  *
  * Conventions shared by every entry point
@@ -102,9 +105,10 @@ typedef struct {
 /*
  * span_la_pass -- one packed pass over views and branches.
  *
- * Section "Kernels" (one scan per pass in three launches; shared branch
- * passes) and section "The Workload".  Computes o for every view row and every
- * branch row and writes each view's final state to view_state_out.
+ * Section "Kernels" (one scan per pass; shared branch passes with the small
+ * kernels fused) and section "The Workload".  Computes o for every view row
+ * and every branch row and writes each view's final state to view_state_out.
+ * One cooperative launch for bf16 inputs by default (span_la_pass_variant).
  *
  *   q, k, v          device [T][H][64], dims.dtype
  *   view_cu_seqlens  host int32 [num_views + 1]
