@@ -74,7 +74,8 @@ class ClockSampler:
     """nvidia-smi samples every 200 ms while running (SM clock, throttle reasons)."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
 
     def __init__(self, gpu_id: str):
         self.lines = []
@@ -140,6 +141,25 @@ def summarize_clocks(rows, t0: float, t1: float):
             "sm_max_mhz": max(mx) if mx else None,
             "power_w_max": max(pw) if pw else None,
             "reasons": sorted(reasons), "samples": len(sel)}
+
+
+def summarize_busy_clocks(rows, min_util: float = 1.0):
+    """Median SM clock and the throttle reasons over every sample of the run in
+    which the GPU ran kernels (utilization >= min_util % over nvidia-smi's
+    sample period): a longer record than the timed region alone, which lasts
+    milliseconds."""
+    busy = []
+    for r in rows:
+        try:
+            if len(r) > 10 and float(r[10]) >= min_util:
+                busy.append(r)
+        except ValueError:
+            pass
+    if not busy:
+        return {"sm_mhz": None, "samples": 0, "reasons": []}
+    out = summarize_clocks(busy, -1e18, 1e18)
+    out["min_utilization_pct"] = min_util
+    return out
 
 
 def gpu_id_for_smi(torch, dev_index: int) -> str:
@@ -689,6 +709,7 @@ def main():
     def step():
         run_on(q, k, v, out, state)
 
+    run_sampler = ClockSampler(gpu_id_for_smi(torch, local))   # the whole GPU part of the run
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         step()
@@ -1024,6 +1045,19 @@ def main():
         for a in raw:
             fn(*a)
 
+    # Host time of one warm call through the C entry point (prepared
+    # arguments, device kept busy), beside host_enqueue_us through Python.
+    busy = torch.empty(256 << 20, dtype=torch.float32, device=dev)
+    host_c = []
+    for _ in range(50):
+        busy.zero_()
+        t_h = time.perf_counter()
+        raw_step()
+        host_c.append((time.perf_counter() - t_h) * 1e6)
+    torch.cuda.synchronize()
+    spanla.span_la_check()
+    del busy
+
     NW = 200
     w_start = torch.cuda.Event(enable_timing=True)
     w_end = torch.cuda.Event(enable_timing=True)
@@ -1067,6 +1101,7 @@ def main():
 
     h2d = 3 * (w.T - row_lo) * w.H * 64 * esize
     d2h = (w.T - row_lo) * w.H * 64 * esize + (0 if shards_mode else w.V * w.H * STATE_BYTES)
+    clocks_busy = summarize_busy_clocks(run_sampler.stop())
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not shards_mode:
@@ -1110,6 +1145,8 @@ def main():
                 "profiled_kernel_us_sum": profiled_step_us,
                 "step_ms_min": min(step_ms),
                 "host_enqueue_us": statistics.median(host_us),
+                "host_enqueue_us_c_abi": statistics.median(host_c),
+                "clocks_busy": clocks_busy,
                 "graph_us_per_step": graph_us,
                 "warm_l2_us_per_step": warm_us,
                 "cold_plan": cold,
