@@ -273,10 +273,11 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   const SpanDesc* p1 = prm.p1 + p1_begin;   // phase-1 pieces (one-launch pass only)
   int2* coord = reinterpret_cast<int2*>(smem + L::kCoord);
   SpanDesc* p1s = reinterpret_cast<SpanDesc*>(smem + L::kP1);
-  // Warp 0 stages the producer's tile coordinates and the phase-1 pieces
-  // (loads issued before the CTA-wide set-up completes, so their latency
-  // overlaps it).
-  if (warp == 0) {
+  // Warp 2 (the O issuer, idle until the set-up completes) stages the
+  // producer's tile coordinates and the phase-1 pieces, at the same time as
+  // thread 0 initialises the barriers and issues the first loads (behind
+  // those, these small loads would wait for megabytes of tile traffic).
+  if (warp == 2) {
     int2 c_lo = make_int2(0, 0), c_hi = make_int2(0, 0);
     if (lane < n) c_lo = make_int2(list[lane].row0, list[lane].head);
     if (lane + 32 < n && lane + 32 < kCoordSlots) c_hi = make_int2(list[lane + 32].row0, list[lane + 32].head);
