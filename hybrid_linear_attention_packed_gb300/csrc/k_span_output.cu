@@ -32,7 +32,11 @@
 //
 // Software pipelined over consecutive tiles t.  15 warps:
 //   warp 0     producer: phase-1 K, V tiles, then Q, K, V tiles by TMA into
-//              a four-stage ring.
+//              a four-stage ring.  When a pass's phase-1 K and V exceed what
+//              the L2 can keep for the tiles' second read, the phase-1 loads
+//              take the L2 evict-first policy (the kP1EvictFirst instance),
+//              so that they displace one another rather than dirty lines
+//              that would first have to be written back.
 //   warp 1     front issuer (one lane; the warp zeroes partial-tile K/V
 //              rows): phase 1, K^T V summed over each phase-1 piece into a
 //              TMEM region; then per tile, as soon as it has landed,
@@ -205,6 +209,8 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
+// kP1EvictFirst: phase-1 K and V loads under the L2 evict-first policy.
+template <bool kP1EvictFirst>
 __global__ void __launch_bounds__(kThreads, 1)
 span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -252,18 +258,25 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // now, while the rest of the set-up completes; the stages are fresh.
     const int4 f0 = __ldg(hd + 2), f1 = __ldg(hd + 3);
     const int fr[2 * kFirstLoads] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+    const uint64_t pol = kP1EvictFirst ? l2_evict_first_policy() : 0;
 #pragma unroll
     for (int u = 0; u < kFirstLoads; ++u) {
       if (u < n_first) {
         const uint32_t st = base + L::kStage0 + u * kStageBytes;
+        const bool hint_kv = kP1EvictFirst && u < n1;
         if (u < n1) {
           mbar_arrive_expect_tx(bar(L::kFull + u), 2 * kRowTileBytes);
         } else {
           mbar_arrive_expect_tx(bar(L::kFull + u), kStageBytes);
           tma_load_3d(st + L::kQ, &tm_q, bar(L::kFull + u), 0, fr[2 * u], fr[2 * u + 1]);
         }
-        tma_load_3d(st + L::kK, &tm_k, bar(L::kFull + u), 0, fr[2 * u], fr[2 * u + 1]);
-        tma_load_3d(st + L::kV, &tm_v, bar(L::kFull + u), 0, fr[2 * u], fr[2 * u + 1]);
+        if (hint_kv) {
+          tma_load_3d_hint(st + L::kK, &tm_k, bar(L::kFull + u), 0, fr[2 * u], fr[2 * u + 1], pol);
+          tma_load_3d_hint(st + L::kV, &tm_v, bar(L::kFull + u), 0, fr[2 * u], fr[2 * u + 1], pol);
+        } else {
+          tma_load_3d(st + L::kK, &tm_k, bar(L::kFull + u), 0, fr[2 * u], fr[2 * u + 1]);
+          tma_load_3d(st + L::kV, &tm_v, bar(L::kFull + u), 0, fr[2 * u], fr[2 * u + 1]);
+        }
       }
     }
     tma_prefetch_desc(&tm_o);
@@ -299,6 +312,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
+      const uint64_t pol = kP1EvictFirst ? l2_evict_first_policy() : 0;
       int u = 0;   // load index: phase-1 tiles, then the run's tiles
       for (int j = 0; j < n_p1 && ok; ++j) {
         const SpanDesc sd = p1_of(j);
@@ -308,8 +322,13 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           if (!wait_or_flag(bar(L::kEmpty + s), ((u / kStages) & 1) ^ 1, err, kErrTimeoutMma)) { ok = false; break; }
           const uint32_t st = base + L::kStage0 + s * kStageBytes;
           mbar_arrive_expect_tx(bar(L::kFull + s), 2 * kRowTileBytes);
-          tma_load_3d(st + L::kK, &tm_k, bar(L::kFull + s), 0, sd.row0 + r, sd.head);
-          tma_load_3d(st + L::kV, &tm_v, bar(L::kFull + s), 0, sd.row0 + r, sd.head);
+          if (kP1EvictFirst) {
+            tma_load_3d_hint(st + L::kK, &tm_k, bar(L::kFull + s), 0, sd.row0 + r, sd.head, pol);
+            tma_load_3d_hint(st + L::kV, &tm_v, bar(L::kFull + s), 0, sd.row0 + r, sd.head, pol);
+          } else {
+            tma_load_3d(st + L::kK, &tm_k, bar(L::kFull + s), 0, sd.row0 + r, sd.head);
+            tma_load_3d(st + L::kV, &tm_v, bar(L::kFull + s), 0, sd.row0 + r, sd.head);
+          }
         }
       }
       for (int i = 0; i < n && ok; ++i, ++u) {
@@ -837,7 +856,9 @@ cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
   if (a.grid <= 0) return cudaSuccess;
   const uint32_t bytes = OutSmem::kRequest;
   static std::atomic<uint64_t> done{0};
-  cudaError_t e = set_smem_limit_once(span_output_kernel, bytes, done);
+  auto kernel = a.p1_evict_first ? span_output_kernel<true> : span_output_kernel<false>;
+  static std::atomic<uint64_t> done_hint{0};
+  cudaError_t e = set_smem_limit_once(kernel, bytes, a.p1_evict_first ? done_hint : done);
   if (e != cudaSuccess) return e;
   OutParams p{};
   p.heads = a.heads;
@@ -872,7 +893,7 @@ cudaError_t launch_span_output(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
   }
   cfg.attrs = attr;
   cfg.numAttrs = (a.fused || a.pdl) ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, span_output_kernel, tm_q[0], tm_k[0], tm_v[0], *tm_o, p);
+  return cudaLaunchKernelEx(&cfg, kernel, tm_q[0], tm_k[0], tm_v[0], *tm_o, p);
 }
 
 }  // namespace spanla

@@ -293,6 +293,7 @@ struct Plan {
   // one-launch pass: spans / span_begin are the phase-1 pieces per output CTA
   bool fused = false;
   int n_p1_ctas = 0;                 // CTAs with phase-1 pieces
+  bool p1_evict_first = false;       // phase-1 loads under the L2 evict-first policy
   std::vector<int32_t> empty_views;  // views without rows (their final state is zero)
 
   int state_slots(int H) const {
@@ -617,7 +618,12 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
     }
     plan.spans.resize(pieces.size());
     std::vector<int32_t> fill(plan.span_begin.begin(), plan.span_begin.end() - 1);
-    for (size_t u = 0; u < pieces.size(); ++u) plan.spans[fill[piece_cta[u]]++] = pieces[u];
+    int64_t p1_bytes = 0;
+    for (size_t u = 0; u < pieces.size(); ++u) {
+      plan.spans[fill[piece_cta[u]]++] = pieces[u];
+      p1_bytes += static_cast<int64_t>(pieces[u].len) * 2 * kHeadDim * 2;
+    }
+    plan.p1_evict_first = p1_bytes > kP1EvictFirstBytes;
     plan.fused = true;
     return plan;
   }
@@ -735,6 +741,7 @@ struct DescBlock {
   bool span_mode = true;
   bool fused = false;      // one-launch pass (span mode)
   int n_p1_ctas = 0;
+  bool p1_evict_first = false;
   std::vector<int32_t> empty_views;
 };
 
@@ -792,6 +799,7 @@ DescBlock make_desc(const Plan& plan, int H) {
   d.block_bytes = d.host.size();
   d.fused = plan.fused;
   d.n_p1_ctas = plan.n_p1_ctas;
+  d.p1_evict_first = plan.p1_evict_first;
   d.empty_views = plan.empty_views;
   return d;
 }
@@ -1164,6 +1172,7 @@ span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t
       a.p1_begin = reinterpret_cast<const int32_t*>(block + desc.off_d);
       a.counter = counter;
       a.n_p1_ctas = desc.n_p1_ctas;
+      a.p1_evict_first = desc.p1_evict_first;
       e = counted_launch(kKernelSpanOutput, stream, [&] {
         return launch_span_output(tile_ops.q, tile_ops.k, tile_ops.v, &tm_o, a, stream);
       });

@@ -205,6 +205,13 @@ cudaError_t launch_span_state(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
 // tiles (loads before the run's tiles) and the (row0, head) of its first
 // kFirstLoads loads in load order (phase-1 K/V boxes first).
 constexpr int kFirstLoads = 4;
+// Phase-1 K and V bytes of a one-launch pass above which its phase-1 loads
+// take the L2 evict-first policy.  Below it, the tiles' second read of K and
+// V finds them in the 129 MB L2, and the policy would make it miss; above it
+// that read misses anyway, and the policy spares the write-back of dirty
+// lines that phase 1 would otherwise displace.
+constexpr int64_t kP1EvictFirstBytes = 96ll << 20;
+
 struct CtaHead {
   int32_t i_begin, n;          // tile records [i_begin, i_begin + n)
   int32_t p1_begin, n_p1;      // phase-1 pieces (one-launch pass)
@@ -234,6 +241,7 @@ struct SpanOutputArgs {
   const int32_t* p1_begin = nullptr;
   unsigned* counter = nullptr;
   int n_p1_ctas = 0;
+  bool p1_evict_first = false;     // phase-1 K, V loads under the L2 evict-first policy
 };
 // tm_q/k/v: 128-row boxes of one head; tm_o: the output array, 32-row boxes
 // of one head (a warp's rows, stored with one TMA store when all lie in the
