@@ -46,8 +46,8 @@
 //              region t & 1.
 //   warp 2     O issuer (one lane): once the P conversion has turned P(t)
 //              into bf16 in place,  O(t) = P(t) V  (M128 N64 K128, P read
-//              from tensor memory), then, with S(t) staged,  O(t) += Q S_hi +
-//              Q S_lo  (M128 N64 K64), so that an O buffer is held only from
+//              from tensor memory), then, with S(t) staged,  O(t) += Q S
+//              (M128 N64 K64, S rounded to bf16), so that an O buffer is held only from
 //              the end of the conversion until the tile's output is read.
 //   warps 3-10 P conversion, two warps per TMEM lane quarter, one per
 //              64-column half: each thread owns one tile row (TMEM lane) and
@@ -59,8 +59,8 @@
 //              piece states out of TMEM into the workspace.  Then they hold
 //              the running fp32 state in registers (a 32-column half of one
 //              state row per thread); per step t they add dS(t) to it (or load
-//              the next piece's start state), stage S(t+1) as bf16 high / low
-//              parts for Q S, and then store O(t).
+//              the next piece's start state), stage S(t+1) rounded to bf16
+//              for Q S, and then store O(t).
 // K^T V runs with M = 128 and the K tile as both 64-wide M atoms, so TMEM
 // lanes 64..127 hold a copy of rows 0..63: the lower copy is read for
 // columns 0..31, the upper for 32..63.
@@ -80,7 +80,9 @@ constexpr int kStages = 4;
 constexpr uint32_t kRowTileBytes = kTileRows * 128;        // 128 rows x 128 B
 constexpr uint32_t kStageBytes = 3 * kRowTileBytes;       // Q K V
 constexpr uint32_t kStateTileBytes = kHeadDim * 128;       // 64 rows x 128 B (bf16)
-constexpr uint32_t kSOpBytes = 2 * kStateTileBytes;         // S as bf16 hi + lo
+// An S operand: S in bf16 (8 KB); the whole 16 KB also serves as the fp32
+// buffer of the start-state sums and holds O on its way out.
+constexpr uint32_t kSOpBytes = 2 * kStateTileBytes;
 constexpr uint32_t kOQuarterBytes = kOutStoreRows * 128;     // 32 rows of O (bf16) on their way out
 static_assert(kOutStoreRows == 32, "one TMA store per warp's rows");
 static_assert(kFirstLoads <= kStages, "the set-up loads use fresh stages");
@@ -176,23 +178,17 @@ __device__ __forceinline__ int inline_bound(const uint4& v, int q) {
   return static_cast<int>((w >> (8 * (q & 3))) & 0xffu);
 }
 
-// Write 32 state values (columns 32*half ..) of row d as bf16 high / low parts
-// into the MN-major S operand ([d][64 e], 128-byte swizzle).
+// Write 32 state values (columns 32*half ..) of row d, rounded to bf16,
+// into the MN-major S operand ([d][64 e], 128-byte swizzle).  (The state
+// itself stays fp32; only its product with Q takes the rounded copy, whose
+// entries are off by less than 2^-9 of their value, as q, k and v are.)
 __device__ __forceinline__ void stage_state_half_row(uint8_t* s_op, int d, int half, const float* x) {
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    uint32_t hi[4], lo[4];
+    uint32_t b[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float h0, l0, h1, l1;
-      split_bf16(x[8 * g + 2 * u], h0, l0);
-      split_bf16(x[8 * g + 2 * u + 1], h1, l1);
-      hi[u] = pack_bf16x2(h0, h1);
-      lo[u] = pack_bf16x2(l0, l1);
-    }
-    const uint32_t off = sw128_offset(d, 32 * half + 8 * g);
-    *reinterpret_cast<uint4*>(s_op + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(s_op + kStateTileBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    for (int u = 0; u < 4; ++u) b[u] = pack_bf16x2(x[8 * g + 2 * u], x[8 * g + 2 * u + 1]);
+    *reinterpret_cast<uint4*>(s_op + sw128_offset(d, 32 * half + 8 * g)) = make_uint4(b[0], b[1], b[2], b[3]);
   }
 }
 
@@ -463,7 +459,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                           id_n64_b_mn, kk > 0 ? 1u : 0u);
       }
       __syncwarp();
-      // S(i) staged: O(i) += Q S_hi + Q S_lo; release the stage.
+      // S(i) staged: O(i) += Q S; release the stage.
       if (!__all_sync(0xffffffffu, wait_or_flag(bar(L::kSSmem + b), (i >> 1) & 1, err, kErrTimeoutMma)))
         break;
       tc_fence_after_sync();
@@ -471,10 +467,8 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (has_state) {
           const uint32_t sop = base + L::kS + b * kSOpBytes;
           for (int kk = 0; kk < kHeadDim / 16; ++kk)
-            for (int part = 0; part < 2; ++part)
-              mma_bf16(tmem + colO, smem_desc_sw128(st + L::kQ + kk * 32, 16, 1024),
-                       smem_desc_sw128(sop + part * kStateTileBytes + kk * 2048, kStateTileBytes, 1024),
-                       id_n64_b_mn, 1u);
+            mma_bf16(tmem + colO, smem_desc_sw128(st + L::kQ + kk * 32, 16, 1024),
+                     smem_desc_sw128(sop + kk * 2048, kStateTileBytes, 1024), id_n64_b_mn, 1u);
         }
         mma_commit(bar(L::kOReady + b));
         mma_commit(bar(L::kEmpty + s));

@@ -10,8 +10,8 @@
 //   qk    4 x M128 N128 K16, A and B K-major           (P = Q K^T of a tile)
 //   kv    8 x M128 N64  K16, A and B MN-major          (dS = [K|K]^T V)
 //   pv    8 x M128 N64  K16, A from tensor memory      (O = P V)
-//   qs    8 x M128 N64  K16, B MN-major                (O += Q S_hi + Q S_lo)
-//   tile  the 28 of one output tile: qk + kv + pv + qs
+//   qs    4 x M128 N64  K16, B MN-major                (O += Q S, S in bf16)
+//   tile  the 24 of one output tile: qk + kv + pv + qs
 //
 // Usage: tc_rate <mode> [grid (0: one per SM)] [iters]; prints one line:
 //   mode grid iters ns_per_group mhz tflops_per_sm tflops_total err
@@ -85,9 +85,7 @@ tc_rate_kernel(int mode, int iters, unsigned long long* out, unsigned* err) {
                           i_n64, kk > 0);
       if (mode == kQS || mode == kTile)
         for (int kk = 0; kk < 4; ++kk)
-          for (int part = 0; part < 2; ++part)
-            mma_bf16(tmem + colO, d_kmajor(q, kk), d_mn(s + part * 8192, kk, 8192), i_n64,
-                     (mode == kTile || kk > 0 || part > 0) ? 1u : 0u);
+          mma_bf16(tmem + colO, d_kmajor(q, kk), d_mn(s, kk, 8192), i_n64, (mode == kTile || kk > 0) ? 1u : 0u);
     }
     mma_commit(bar);
     if (!mbar_wait_bounded(bar, 0, 2000000000ull)) atomicOr(err, 1u);
@@ -107,7 +105,7 @@ tc_rate_kernel(int mode, int iters, unsigned long long* out, unsigned* err) {
 int main(int argc, char** argv) {
   const char* names[] = {"qk", "kv", "pv", "qs", "tile"};
   const double flop[] = {4 * 2.0 * 128 * 128 * 16, 8 * 2.0 * 128 * 64 * 16, 8 * 2.0 * 128 * 64 * 16,
-                         8 * 2.0 * 128 * 64 * 16, 0};
+                         4 * 2.0 * 128 * 64 * 16, 0};
   int mode = -1;
   for (int m = 0; m < 5; ++m)
     if (argc > 1 && std::strcmp(argv[1], names[m]) == 0) mode = m;
