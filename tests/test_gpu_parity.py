@@ -3,7 +3,10 @@ same seeded inputs, element by element.
 
 Tolerance (written here, applied per call): max|o_gpu - o_ref| / max|o_ref|
 <= 1e-3 for fp32 inputs and <= 1e-2 for bf16 inputs; the same bound holds for
-the view states against max|S_ref|.
+the view states against max|S_ref|.  On the benchmark configurations of bf16
+inputs the output must also stay within 5e-3 (BF16_STATE_TOL): the bf16 pass
+multiplies q by the running state rounded to bf16, and half the bf16 bound is
+the limit that choice was held to.
 """
 import numpy as np
 import pytest
@@ -15,6 +18,8 @@ from hybrid_linear_attention_packed_gb300 import (span_la_branches_from_state, s
 from oracle import oracle_branches_from_state, oracle_pass
 
 pytestmark = pytest.mark.gpu
+
+BF16_STATE_TOL = 5e-3
 
 
 def _run_gpu(w, dev, poison=True):
@@ -29,7 +34,7 @@ def _oracle(w):
     return oracle_pass(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu, w.branch_parent)
 
 
-def _check_full(w, dev):
+def _check_full(w, dev, out_tol=None):
     out, state = _run_gpu(w, dev)
     ref, ref_state = _oracle(w)
     got = f64(out)
@@ -46,6 +51,8 @@ def _check_full(w, dev):
     print("%s: out %.2e (views %.2e, branches %.2e) state %.2e"
           % (w.name, e_all, e_view, e_br, e_state))
     assert e_all <= tol and e_state <= tol
+    if out_tol is not None:
+        assert e_all <= out_tol
     return out, state
 
 
@@ -55,16 +62,16 @@ def test_tiny_oracle_case(cuda_device):
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_single_request_7400(cuda_device, seed):
-    _check_full(workloads.single_request(seed), cuda_device)
+    _check_full(workloads.single_request(seed), cuda_device, BF16_STATE_TOL)
 
 
 def test_packed_four_requests(cuda_device):
-    _check_full(workloads.packed_four(0), cuda_device)
+    _check_full(workloads.packed_four(0), cuda_device, BF16_STATE_TOL)
 
 
 @pytest.mark.parametrize("n_views", [1, 4])
 def test_sweep_small(cuda_device, n_views):
-    _check_full(workloads.sweep(n_views, 0), cuda_device)
+    _check_full(workloads.sweep(n_views, 0), cuda_device, BF16_STATE_TOL)
 
 
 @pytest.mark.parametrize("n_views", [16, 32])
