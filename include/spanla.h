@@ -58,10 +58,12 @@
  *   workspace allocations in the graph.  The descriptor bytes of a recorded
  *   call are kept by the library for the life of the process.
  * Precision.  bf16 or fp32 inputs; the state and every accumulation are fp32.
- *   fp32 operands (and the fp32 state and P tiles fed to the tensor cores) are
- *   split into two bf16 parts whose cross products are summed.  Outputs are
- *   rounded to the input type (round to nearest even).  Results are
- *   deterministic run to run (no floating-point atomics).
+ *   With fp32 inputs, fp32 operands (q, k, v, and the state and P tiles fed
+ *   to the tensor cores) are split into two bf16 parts whose cross products
+ *   are summed.  With bf16 inputs, P and the state enter their products with
+ *   q rounded to bf16, like q, k and v themselves (the state itself stays
+ *   fp32).  Outputs are rounded to the input type (round to nearest even).
+ *   Results are deterministic run to run (no floating-point atomics).
  * Errors.  Metadata, shape, pointer and alignment problems are detected on the
  *   host before anything is enqueued; the call then returns an error code and
  *   writes nothing.  Device-side waits are bounded: a wait that runs out sets
