@@ -60,8 +60,8 @@
  * Precision.  bf16 or fp32 inputs; the state and every accumulation are fp32.
  *   With fp32 inputs, fp32 operands (q, k, v, and the state and P tiles fed
  *   to the tensor cores) are split into two bf16 parts whose cross products
- *   are summed.  With bf16 inputs, P and the state enter their products with
- *   q rounded to bf16, like q, k and v themselves (the state itself stays
+ *   are summed.  With bf16 inputs, P enters P v and the state enters q S
+ *   rounded to bf16, like q, k and v themselves (the state itself stays
  *   fp32).  Outputs are rounded to the input type (round to nearest even).
  *   Results are deterministic run to run (no floating-point atomics).
  * Errors.  Metadata, shape, pointer and alignment problems are detected on the
