@@ -156,16 +156,38 @@ def _iptr(a: np.ndarray):
     """Address of an int32 array for a ``const int32_t*`` argument (None when empty)."""
     if a.size == 0:
         return None
+    if a.flags.writeable:   # (cheaper than numpy's .ctypes helper object)
+        return ctypes.addressof(ctypes.c_int32.from_buffer(a))
     return a.ctypes.data
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_raw_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream_handle(stream) -> int:
+    """The CUDA stream handle for a call: ``stream``'s, or the current device's
+    current stream."""
     if stream is None:
+        if _raw_stream is not None and _raw_device is not None:
+            return int(_raw_stream(_raw_device()))
         stream = torch.cuda.current_stream()
     return int(stream.cuda_stream)
 
 
 def _dims_of(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> Dims:
+    # The usual case in one expression; anything else goes through the
+    # checks below, which name the problem.
+    sh, dt = q.shape, q.dtype
+    if (len(sh) == 3 and sh[2] == 64 and k.shape == sh and v.shape == sh and k.dtype == dt
+            and v.dtype == dt and (dt == torch.bfloat16 or dt == torch.float32)
+            and q.is_cuda and k.is_cuda and v.is_cuda
+            and q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        return Dims(sh[0], sh[1], 64, SPAN_LA_BF16 if dt == torch.bfloat16 else SPAN_LA_F32)
+    return _dims_checked(q, k, v)
+
+
+def _dims_checked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> Dims:
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda:
             raise ValueError("%s must be a CUDA tensor" % name)
