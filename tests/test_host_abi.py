@@ -103,6 +103,22 @@ def test_empty_call_is_a_no_op(lib):
     assert st == 0
 
 
+def test_metadata_addresses(lib):
+    """The binding passes int32 metadata by address: writable arrays through a
+    ctypes view of their buffer, read-only ones through numpy's helper, empty
+    ones as NULL; the address is the array's own data either way, and
+    non-int32 or strided input is first copied to a contiguous int32 array."""
+    a = np.arange(7, dtype=np.int32)
+    b = np.arange(7, dtype=np.int32)
+    b.flags.writeable = False
+    assert spanla._iptr(a) == a.__array_interface__["data"][0]
+    assert spanla._iptr(b) == b.__array_interface__["data"][0]
+    assert spanla._iptr(np.zeros(0, dtype=np.int32)) is None
+    c = spanla._i32(np.arange(14, dtype=np.int64)[::2])
+    assert c.dtype == np.int32 and c.flags.c_contiguous and list(c) == list(range(0, 14, 2))
+    assert spanla._i32(a) is a
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not found"):
         spanla.load_library(str(tmp_path / "nope.so"))
