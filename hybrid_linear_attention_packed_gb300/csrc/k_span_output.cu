@@ -80,13 +80,15 @@ constexpr int kStages = 4;
 constexpr uint32_t kRowTileBytes = kTileRows * 128;        // 128 rows x 128 B
 constexpr uint32_t kStageBytes = 3 * kRowTileBytes;       // Q K V
 constexpr uint32_t kStateTileBytes = kHeadDim * 128;       // 64 rows x 128 B (bf16)
-// An S operand: S in bf16 (8 KB); the whole 16 KB also serves as the fp32
-// buffer of the start-state sums and holds O on its way out.
+// An S operand: S in bf16 in its first 8 KB.  Its second 8 KB holds O of
+// two lane quarters on its way out (quarters 0, 1 in operand 0; 2, 3 in
+// operand 1), and the whole 16 KB also serves as the fp32 buffer of the
+// start-state sums.
 constexpr uint32_t kSOpBytes = 2 * kStateTileBytes;
 constexpr uint32_t kOQuarterBytes = kOutStoreRows * 128;     // 32 rows of O (bf16) on their way out
 static_assert(kOutStoreRows == 32, "one TMA store per warp's rows");
 static_assert(kFirstLoads <= kStages, "the set-up loads use fresh stages");
-static_assert(4 * kOQuarterBytes <= kSOpBytes, "O staging fits in one S operand");
+static_assert(2 * kOQuarterBytes == kStateTileBytes, "two quarters of O staging per S operand");
 constexpr int kCoordSlots = 64;                              // tile coordinates staged for the producer
 constexpr int kP1Slots = 32;                                 // phase-1 piece records staged
 constexpr uint32_t kTmemCols = 512;
@@ -97,7 +99,7 @@ constexpr uint32_t kNamedStateBar = 1;                       // bar.sync id of t
 struct OutSmem {
   static constexpr uint32_t kStage0 = 0;
   static constexpr uint32_t kQ = 0, kK = kRowTileBytes, kV = 2 * kRowTileBytes;
-  static constexpr uint32_t kS = kStages * kStageBytes;          // two S operands (hi, lo)
+  static constexpr uint32_t kS = kStages * kStageBytes;          // two S operands (S, O staging)
   static constexpr uint32_t kBar = kS + 2 * kSOpBytes;
   // barrier slots (8 bytes each); the pairs are used by alternate tiles (or
   // phase-1 pieces).  Empty takes two arrivals per use: the front issuer's
@@ -649,6 +651,10 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       }
       float4* buf = reinterpret_cast<float4*>(smem + L::kS + (t & 1) * kSOpBytes);
       if (t & 1) tag_op1 = -1; else tag_op0 = -1;
+      // The buffer holds two warps' O staging: their TMA stores must have
+      // read it.
+      if (lane == 0) bulk_wait_read_all();
+      named_barrier_sync(kNamedStateBar, kGroupThreads);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const int f = g + 128 * c, hr = f >> 3;
@@ -709,15 +715,9 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_arrive(bar(L::kSSmem + (t & 1)));
     };
 
-    // O(i) -> global (rows of the tile only).
-    // Tiles whose O goes out through S operand i & 1 (TMA stores): not a
-    // one-tile piece with a start state (that piece keeps its start state in
-    // the operand for the next one-tile piece: packed branches of one parent,
-    // stored row by row), and at least one whole 32-row group.
-    auto o_through_smem = [&](const TileState& r) {
-      return (r.flags & (kTileFirst | kTileLast | kTileHasInit)) != (kTileFirst | kTileLast | kTileHasInit) &&
-             r.nrows >= 32;
-    };
+    // O(i) -> global (rows of the tile only), through this warp's O staging
+    // when its 32 rows all lie in the tile (one TMA store), else row by row.
+    bool o_pending = false;   // this warp's last TMA store may still read its staging
     auto o_work = [&](int i, const TileState& r, bool live) -> bool {
       const int b = i & 1;
       if (!live || !__all_sync(0xffffffffu, wait_or_flag(bar(L::kOReady + b), (i >> 1) & 1, err, kErrTimeoutMma)))
@@ -725,11 +725,15 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tc_fence_after_sync();
       const uint32_t colO = b ? kColO1 : kColO0;
       // A warp whose 32 rows all lie in the tile writes them, 128-byte
-      // swizzled, into its quarter of S operand b (free: Q S of tile i has
-      // completed) and stores them with one TMA store; otherwise each thread
-      // stores its own row if it lies in the tile.
-      const bool whole = o_through_smem(r) && (quarter + 1) * 32 <= r.nrows;
-      uint8_t* ob = smem + L::kS + b * kSOpBytes + quarter * kOQuarterBytes;
+      // swizzled, into its O staging (once its previous store has read it)
+      // and stores them with one TMA store; otherwise each thread stores its
+      // own row if it lies in the tile.
+      const bool whole = (quarter + 1) * 32 <= r.nrows;
+      uint8_t* ob = smem + L::kS + (quarter >> 1) * kSOpBytes + kStateTileBytes + (quarter & 1) * kOQuarterBytes;
+      if (whole && o_pending) {
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
       uint4* dst = reinterpret_cast<uint4*>(
           prm.out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim);
       const bool store = row < r.nrows;
@@ -761,6 +765,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tma_store_3d(&tm_o, smem_addr(ob), 0, r.row0 + quarter * 32, r.head);
           bulk_commit_group();
         }
+        o_pending = true;
       }
       return true;
     };
@@ -810,24 +815,14 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       TileState nxt = n > 1 ? load_state(list + 1) : TileState{};
       start_piece(0, cur);
       stage(0, cur);
-      bool prev_smem = false;   // O(i-1) went out through S operand (i+1) & 1
       for (int i = 0; i < n; ++i) {
         // S(i+1) first: the O issuer needs it right after P V of tile i+1.
         if (i + 1 < n || (cur.flags & kTileFinalOut)) ok = take_ds(i, cur, ok);
         if (i + 1 < n) {
-          if (prev_smem) {
-            // The TMA stores of O(i-1) have left S operand (i+1) & 1.
-            if (lane == 0) bulk_wait_read_all();
-            ok = named_barrier_and(kNamedStateBar, kGroupThreads, ok);
-          }
           if (cur.flags & kTileLast) start_piece(i + 1, nxt);
           stage(i + 1, nxt);
         }
         ok = o_work(i, cur, ok);
-        prev_smem = o_through_smem(cur);
-        if (prev_smem) {   // S operand i & 1 no longer holds a start state
-          if (i & 1) tag_op1 = -1; else tag_op0 = -1;
-        }
         cur = nxt;
         if (i + 2 < n) nxt = load_state(list + i + 2);
       }
