@@ -70,8 +70,8 @@
 namespace spanla {
 namespace {
 
-constexpr int kThreads = 480;
-constexpr int kGroupWarps = 4;                           // state and output
+constexpr int kThreads = 32 * (3 + 8 + 8);
+constexpr int kGroupWarps = 8;                           // state and output
 constexpr int kGroupThreads = 32 * kGroupWarps;
 constexpr int kConvWarps = 8;                            // P conversion
 constexpr int kConvThreads = 32 * kConvWarps;
@@ -180,25 +180,25 @@ __device__ __forceinline__ int inline_bound(const uint4& v, int q) {
   return static_cast<int>((w >> (8 * (q & 3))) & 0xffu);
 }
 
-// Write 32 state values (columns 32*half ..) of row d, rounded to bf16,
-// into the MN-major S operand ([d][64 e], 128-byte swizzle).  (The state
-// itself stays fp32; only its product with Q takes the rounded copy, whose
-// entries are off by less than 2^-9 of their value, as q, k and v are.)
-__device__ __forceinline__ void stage_state_half_row(uint8_t* s_op, int d, int half, const float* x) {
+// Write 16 state values (columns col0 ..) of row d, rounded to bf16, into
+// the MN-major S operand ([d][64 e], 128-byte swizzle).  (The state itself
+// stays fp32; only its product with Q takes the rounded copy, whose entries
+// are off by less than 2^-9 of their value, as q, k and v are.)
+__device__ __forceinline__ void stage_state_slice(uint8_t* s_op, int d, int col0, const float* x) {
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
+  for (int g = 0; g < 2; ++g) {
     uint32_t b[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) b[u] = pack_bf16x2(x[8 * g + 2 * u], x[8 * g + 2 * u + 1]);
-    *reinterpret_cast<uint4*>(s_op + sw128_offset(d, 32 * half + 8 * g)) = make_uint4(b[0], b[1], b[2], b[3]);
+    *reinterpret_cast<uint4*>(s_op + sw128_offset(d, col0 + 8 * g)) = make_uint4(b[0], b[1], b[2], b[3]);
   }
 }
 
-// 32 fp32 values (one half-row of a state) to global memory.
-__device__ __forceinline__ void store_half_row(float* dst, const float* x) {
+// 16 fp32 values (one thread's slice of a state row) to global memory.
+__device__ __forceinline__ void store_slice(float* dst, const float* x) {
   float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-  for (int c = 0; c < 8; ++c) d4[c] = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+  for (int c = 0; c < 4; ++c) d4[c] = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
 }
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
@@ -509,30 +509,33 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         break;
       tc_fence_after_sync();
       const uint32_t colP = (b ? kColP1 : kColP0) + c0;
-      uint32_t pk[32];
-      if (all_zero) {
+      // Two 32-column chunks in turn; chunk q's bf16 pairs go to columns
+      // 16q .. 16q + 15 of the half, over scores already read (chunk 1's land
+      // over columns 16 .. 31 of chunk 0).
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = 0u;
-      } else {
-        uint32_t r0[32], r1[32];
-        tmem_ld_32cols(tmem + lane_base + colP, r0);
-        tmem_ld_32cols(tmem + lane_base + colP + 32, r1);
-        tmem_ld_wait();
+      for (int q = 0; q < 2; ++q) {
+        uint32_t pk[16];
+        if (all_zero) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int jj = c0 + 2 * c;
-          float p0 = __uint_as_float(c < 16 ? r0[2 * c] : r1[2 * c - 32]);
-          float p1v = __uint_as_float(c < 16 ? r0[2 * c + 1] : r1[2 * c - 31]);
-          if (!all_kept) {
-            p0 = (jj >= seg_start && jj <= hi_col) ? p0 : 0.f;
-            p1v = (jj + 1 >= seg_start && jj + 1 <= hi_col) ? p1v : 0.f;
+          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+        } else {
+          uint32_t r0[32];
+          tmem_ld_32cols(tmem + lane_base + colP + 32 * q, r0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int jj = c0 + 32 * q + 2 * c;
+            float p0 = __uint_as_float(r0[2 * c]);
+            float p1v = __uint_as_float(r0[2 * c + 1]);
+            if (!all_kept) {
+              p0 = (jj >= seg_start && jj <= hi_col) ? p0 : 0.f;
+              p1v = (jj + 1 >= seg_start && jj + 1 <= hi_col) ? p1v : 0.f;
+            }
+            pk[c] = pack_bf16x2(p0, p1v);
           }
-          pk[c] = pack_bf16x2(p0, p1v);
         }
+        tmem_st_16cols(tmem + lane_base + colP + 16 * q, pk);
       }
-      // bf16 pairs of this half's 64 columns go to its first 32 columns, all
-      // of them read before any is overwritten.
-      tmem_st_32cols(tmem + lane_base + colP, pk);
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(L::kPDone + b));
@@ -540,12 +543,15 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   } else {
     // ------------------------------------------------------------ state and output
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
+    const int pi = (warp - kStateWarp0) >> 2;     // which of the quarter's two warps
     const int row = quarter * 32 + lane;          // tile row = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     // State work: lanes 0..63 and their copy in lanes 64..127 hold state rows
-    // d = row & 63; the lower copy handles columns 0..31, the upper 32..63.
+    // d = row & 63; the lower copy handles columns 0..31, the upper 32..63,
+    // and the quarter's two warps take 16 of those each.
     const int d = row & 63, sh = row >> 6;
-    const int64_t half_row = static_cast<int64_t>(d) * kHeadDim + sh * 32;   // offset in a state
+    const int col0 = 32 * sh + 16 * pi;           // this thread's state columns col0 .. col0 + 15
+    const int64_t slice = static_cast<int64_t>(d) * kHeadDim + col0;   // offset in a state
     bool ok = true;
 
     // Phase 1: each piece's K^T V out of TMEM into its workspace slot; then
@@ -556,13 +562,13 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       ok = __all_sync(0xffffffffu, wait_or_flag(bar(L::kP1Ready + b), (j >> 1) & 1, err, kErrTimeoutMma));
       if (!ok) break;
       tc_fence_after_sync();
-      uint32_t r0[32];
-      tmem_ld_32cols(tmem + lane_base + (b ? kColD1 : kColD0) + 32 * sh, r0);
+      uint32_t r0[16];
+      tmem_ld_16cols(tmem + lane_base + (b ? kColD1 : kColD0) + col0, r0);
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(L::kP1Free + b));
-      store_half_row(prm.ws + static_cast<int64_t>(sd.slot) * kStateFloats + half_row,
-                     reinterpret_cast<const float*>(r0));
+      store_slice(prm.ws + static_cast<int64_t>(sd.slot) * kStateFloats + slice,
+                  reinterpret_cast<const float*>(r0));
     }
     if (n_p1 > 0) {
       mbar_arrive(bar(L::kP1Done));
@@ -589,13 +595,13 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       named_barrier_sync(kNamedStateBar, kGroupThreads);
     };
 
-    // The running state (row d, columns 32*sh ..) in fp32.  tag_run names the
+    // The running state (row d, columns col0 ..) in fp32.  tag_run names the
     // start state it holds while it is one (after the first tile of a
     // one-tile piece, or a view's final state); -1 once tiles have been added
     // to it.  A run of pieces with the same start state (the packed branch
     // tiles of one parent) loads it once, and each S operand remembers the
     // start state it holds, so that it is staged once per operand.
-    float s_run[32];
+    float s_run[16];
     int64_t tag_run = -1, tag_op0 = -1, tag_op1 = -1;
     auto carry_tag = [&](int view, int head) -> int64_t {
       return (static_cast<int64_t>(1) << 62) | (static_cast<int64_t>(view) << 16) | head;
@@ -609,9 +615,9 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     };
     // Sum, in order, of the states of term A (a_n states a_rows heads apart)
     // and term B (b_n workspace slots) into s_run.  The group reads each
-    // state coalesced (thread g of the group takes float4 number g + 128 c),
+    // state coalesced (thread g of the group takes float4 number g + 256 c),
     // the sum goes through S operand t & 1 (free: its last reader was Q S of
-    // tile t - 2), and each thread takes its half-row back from there.  The
+    // tile t - 2), and each thread takes its slice back from there.  The
     // buffer index is XOR-swizzled on the half-row so that both sides are
     // free of bank conflicts.
     auto sum_start = [&](int t, const TileState& r) {
@@ -626,28 +632,28 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       auto src = [&](int k) -> const float4* {
         return reinterpret_cast<const float4*>(k < na ? pa + k * sa : pb + static_cast<int64_t>(k - na) * kStateFloats) + g;
       };
-      float4 acc[8];
+      float4 acc[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
       auto add4 = [](float4& x, const float4 y) { x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w; };
       int k = 0;
       for (; k + 2 <= total; k += 2) {
         const float4* p0 = src(k);
         const float4* p1 = src(k + 1);
-        float4 x[8], y[8];
+        float4 x[4], y[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) x[c] = __ldcg(p0 + 128 * c);
+        for (int c = 0; c < 4; ++c) x[c] = __ldcg(p0 + kGroupThreads * c);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) y[c] = __ldcg(p1 + 128 * c);
+        for (int c = 0; c < 4; ++c) y[c] = __ldcg(p1 + kGroupThreads * c);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) add4(acc[c], x[c]);
+        for (int c = 0; c < 4; ++c) add4(acc[c], x[c]);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) add4(acc[c], y[c]);
+        for (int c = 0; c < 4; ++c) add4(acc[c], y[c]);
       }
       if (k < total) {
         const float4* p0 = src(k);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) add4(acc[c], __ldcg(p0 + 128 * c));
+        for (int c = 0; c < 4; ++c) add4(acc[c], __ldcg(p0 + kGroupThreads * c));
       }
       float4* buf = reinterpret_cast<float4*>(smem + L::kS + (t & 1) * kSOpBytes);
       if (t & 1) tag_op1 = -1; else tag_op0 = -1;
@@ -656,15 +662,15 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (lane == 0) bulk_wait_read_all();
       named_barrier_sync(kNamedStateBar, kGroupThreads);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int f = g + 128 * c, hr = f >> 3;
+      for (int c = 0; c < 4; ++c) {
+        const int f = g + kGroupThreads * c, hr = f >> 3;
         buf[hr * 8 + ((f & 7) ^ ((hr >> 1) & 7))] = acc[c];
       }
       named_barrier_sync(kNamedStateBar, kGroupThreads);
       const int hr = 2 * d + sh;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 v4 = buf[hr * 8 + (c ^ ((hr >> 1) & 7))];
+      for (int c = 0; c < 4; ++c) {
+        const float4 v4 = buf[hr * 8 + ((4 * pi + c) ^ ((hr >> 1) & 7))];
         s_run[4 * c] = v4.x; s_run[4 * c + 1] = v4.y; s_run[4 * c + 2] = v4.z; s_run[4 * c + 3] = v4.w;
       }
       named_barrier_sync(kNamedStateBar, kGroupThreads);
@@ -676,7 +682,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     auto start_piece = [&](int t, const TileState& r) {
       if (!(r.flags & kTileHasInit)) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s_run[e] = 0.f;
+        for (int e = 0; e < 16; ++e) s_run[e] = 0.f;
         tag_run = -1;
         return;
       }
@@ -685,12 +691,12 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tag_run = tag;
       if (r.flags & kTileCarry) {
         // The running state has moved on since the view's last tile (a long
-        // branch ran in between): this thread's own half-row of the final
+        // branch ran in between): this thread's own slice of the final
         // state, as it wrote it.
         const float4* p4 = reinterpret_cast<const float4*>(
-            prm.final_out + (static_cast<int64_t>(r.final_idx) * H + r.head) * kStateFloats + half_row);
+            prm.final_out + (static_cast<int64_t>(r.final_idx) * H + r.head) * kStateFloats + slice);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
           const float4 v4 = __ldcg(p4 + c);
           s_run[4 * c] = v4.x; s_run[4 * c + 1] = v4.y; s_run[4 * c + 2] = v4.z; s_run[4 * c + 3] = v4.w;
         }
@@ -708,7 +714,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const bool uses = !(r.flags & kTileFirst) || (r.flags & kTileHasInit);
       const int64_t held = (t & 1) ? tag_op1 : tag_op0;
       if (uses && !(tag >= 0 && tag == held)) {
-        stage_state_half_row(smem + L::kS + (t & 1) * kSOpBytes, d, sh, s_run);
+        stage_state_slice(smem + L::kS + (t & 1) * kSOpBytes, d, col0, s_run);
         if (t & 1) tag_op1 = tag; else tag_op0 = tag;
       }
       fence_proxy_async_smem();
@@ -724,45 +730,42 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         return false;
       tc_fence_after_sync();
       const uint32_t colO = b ? kColO1 : kColO0;
-      // A warp whose 32 rows all lie in the tile writes them, 128-byte
-      // swizzled, into its O staging (once its previous store has read it)
-      // and stores them with one TMA store; otherwise each thread stores its
-      // own row if it lies in the tile.
+      // The quarter's two warps take 32 of the 64 output columns each.  A
+      // warp whose 32 rows all lie in the tile writes its 32 x 32 block,
+      // 64-byte swizzled, into its O staging (once its previous store has
+      // read it) and stores it with one TMA store; otherwise each thread
+      // stores its own row if it lies in the tile.
       const bool whole = (quarter + 1) * 32 <= r.nrows;
-      uint8_t* ob = smem + L::kS + (quarter >> 1) * kSOpBytes + kStateTileBytes + (quarter & 1) * kOQuarterBytes;
+      uint8_t* ob = smem + L::kS + (quarter >> 1) * kSOpBytes + kStateTileBytes + (quarter & 1) * kOQuarterBytes +
+                    pi * (kOQuarterBytes / 2);
       if (whole && o_pending) {
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
       }
       uint4* dst = reinterpret_cast<uint4*>(
-          prm.out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim);
+          prm.out + ((static_cast<int64_t>(r.row0) + row) * H + r.head) * kHeadDim + 32 * pi);
       const bool store = row < r.nrows;
+      uint32_t r0[32];
+      tmem_ld_32cols(tmem + lane_base + colO + 32 * pi, r0);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kOFree + b));
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t r0[32];
-        tmem_ld_32cols(tmem + lane_base + colO + 32 * h, r0);
-        tmem_ld_wait();
-        if (h == 1) {
-          tc_fence_before_sync();
-          mbar_arrive(bar(L::kOFree + b));
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v4 = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c]), __uint_as_float(r0[8 * c + 1])),
-                                      pack_bf16x2(__uint_as_float(r0[8 * c + 2]), __uint_as_float(r0[8 * c + 3])),
-                                      pack_bf16x2(__uint_as_float(r0[8 * c + 4]), __uint_as_float(r0[8 * c + 5])),
-                                      pack_bf16x2(__uint_as_float(r0[8 * c + 6]), __uint_as_float(r0[8 * c + 7])));
-          if (whole)
-            *reinterpret_cast<uint4*>(ob + lane * 128 + (((4 * h + c) ^ (lane & 7)) << 4)) = v4;
-          else if (store)
-            dst[4 * h + c] = v4;
-        }
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v4 = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c]), __uint_as_float(r0[8 * c + 1])),
+                                    pack_bf16x2(__uint_as_float(r0[8 * c + 2]), __uint_as_float(r0[8 * c + 3])),
+                                    pack_bf16x2(__uint_as_float(r0[8 * c + 4]), __uint_as_float(r0[8 * c + 5])),
+                                    pack_bf16x2(__uint_as_float(r0[8 * c + 6]), __uint_as_float(r0[8 * c + 7])));
+        if (whole)
+          *reinterpret_cast<uint4*>(ob + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = v4;
+        else if (store)
+          dst[c] = v4;
       }
       if (whole) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&tm_o, smem_addr(ob), 0, r.row0 + quarter * 32, r.head);
+          tma_store_3d(&tm_o, smem_addr(ob), 32 * pi, r.row0 + quarter * 32, r.head);
           bulk_commit_group();
         }
         o_pending = true;
@@ -783,11 +786,11 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (good) tc_fence_after_sync();
       if (!(r.flags & kTileLast) || (r.flags & kTileFinalOut)) {
         if (good) {
-          uint32_t r0[32];
-          tmem_ld_32cols(tmem + lane_base + (b ? kColD1 : kColD0) + 32 * sh, r0);
+          uint32_t r0[16];
+          tmem_ld_16cols(tmem + lane_base + (b ? kColD1 : kColD0) + col0, r0);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) s_run[e] += __uint_as_float(r0[e]);
+          for (int e = 0; e < 16; ++e) s_run[e] += __uint_as_float(r0[e]);
         }
         tag_run = -1;
       }
@@ -797,8 +800,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       }
       if (r.flags & kTileFinalOut) {
         if (good)
-          store_half_row(
-              prm.final_out + (static_cast<int64_t>(r.final_idx) * H + r.head) * kStateFloats + half_row, s_run);
+          store_slice(prm.final_out + (static_cast<int64_t>(r.final_idx) * H + r.head) * kStateFloats + slice, s_run);
         tag_run = carry_tag(r.final_idx, r.head);
       }
       return good;

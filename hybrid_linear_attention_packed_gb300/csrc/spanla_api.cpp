@@ -710,18 +710,20 @@ size_t put(std::vector<uint8_t>& host, const std::vector<T>& v) {
 template <typename T>
 size_t bytes_of(const std::vector<T>& v) { return align256(v.size() * sizeof(T)); }
 
-// 3-D view (d, token, head) of a [T][H][64] bf16 array; box = {64, rows, heads}.
+// 3-D view (d, token, head) of a [T][H][64] bf16 array; box = {box_cols,
+// rows, heads} (128-byte swizzle for 64 columns, 64-byte for 32).
 span_la_status encode_map(CUtensorMap* map, const void* base, int64_t T, int H, int box_rows,
-                          int box_heads) {
+                          int box_heads, int box_cols = kHeadDim) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(T),
                               static_cast<cuuint64_t>(H)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(H) * kHeadDim * 2, kHeadDim * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(box_rows),
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows),
                              static_cast<cuuint32_t>(box_heads)};
   const cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        box_cols == kHeadDim ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SPAN_LA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return SPAN_LA_OK;
@@ -1116,14 +1118,15 @@ span_la_status enqueue_pass(const DescBlock& desc, const uint8_t* block, uint8_t
     }
   }
   if (st != SPAN_LA_OK) return st;
-  // The span-output kernel stores whole 32-row groups of O with TMA.
+  // The span-output kernel stores whole 32-row x 32-column blocks of O with
+  // TMA (one per warp).
   CUtensorMap tm_o{};
   const bool span_out = desc.span_mode && desc.n_out_tiles > 0;
   if (span_out) {
     if (mc != nullptr && mc->valid && map_hit && mc->o == out) {
       tm_o = mc->tm_o;
     } else {
-      st = encode_map(&tm_o, out, T, H, kOutStoreRows, 1);
+      st = encode_map(&tm_o, out, T, H, kOutStoreRows, 1, 32);
       if (st != SPAN_LA_OK) return st;
     }
   }
