@@ -30,7 +30,7 @@
 // on chip (K^T V of that tile added to the running state), writes it out and
 // starts that view's following branch tiles in its run from it directly.
 //
-// Software pipelined over consecutive tiles t.  15 warps:
+// Software pipelined over consecutive tiles t.  19 warps:
 //   warp 0     producer: phase-1 K, V tiles, then Q, K, V tiles by TMA into
 //              a four-stage ring.  When a pass's phase-1 K and V exceed what
 //              the L2 can keep for the tiles' second read, the phase-1 loads
@@ -47,20 +47,22 @@
 //   warp 2     O issuer (one lane): once the P conversion has turned P(t)
 //              into bf16 in place,  O(t) = P(t) V  (M128 N64 K128, P read
 //              from tensor memory), then, with S(t) staged,  O(t) += Q S
-//              (M128 N64 K64, S rounded to bf16), so that an O buffer is held only from
-//              the end of the conversion until the tile's output is read.
+//              (M128 N64 K64, S rounded to bf16), so that an O buffer is
+//              held only from the end of the conversion until the tile's
+//              output is read.
 //   warps 3-10 P conversion, two warps per TMEM lane quarter, one per
 //              64-column half: each thread owns one tile row (TMEM lane) and
 //              turns its half of P(t) into the masked bf16 A operand in place
-//              in tensor memory -- 64 fp32 columns become 64 bf16 in the half's
-//              first 32 columns (P V reads keys 0..63 from columns 0..31 and
-//              keys 64..127 from columns 64..95).
-//   warps 11-14 state and output, one warp per lane quarter.  Phase 1: the
+//              in tensor memory, 32 columns at a time -- 64 fp32 columns
+//              become 64 bf16 in the half's first 32 columns (P V reads keys
+//              0..63 from columns 0..31 and keys 64..127 from columns 64..95).
+//   warps 11-18 state and output, two warps per lane quarter.  Phase 1: the
 //              piece states out of TMEM into the workspace.  Then they hold
-//              the running fp32 state in registers (a 32-column half of one
-//              state row per thread); per step t they add dS(t) to it (or load
-//              the next piece's start state), stage S(t+1) rounded to bf16
-//              for Q S, and then store O(t).
+//              the running fp32 state in registers (16 columns of one state
+//              row per thread); per step t they add dS(t) to it (or load the
+//              next piece's start state), stage S(t+1) rounded to bf16 for
+//              Q S, and then store O(t), 32 of its 64 columns per warp (one
+//              32 x 32 TMA store when the warp's rows all lie in the tile).
 // K^T V runs with M = 128 and the K tile as both 64-wide M atoms, so TMEM
 // lanes 64..127 hold a copy of rows 0..63: the lower copy is read for
 // columns 0..31, the upper for 32..63.
