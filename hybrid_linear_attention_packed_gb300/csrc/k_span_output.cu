@@ -46,10 +46,11 @@
 //              region t & 1.
 //   warp 2     O issuer (one lane): once the P conversion has turned P(t)
 //              into bf16 in place,  O(t) = P(t) V  (M128 N64 K128, P read
-//              from tensor memory), then, with S(t) staged,  O(t) += Q S
-//              (M128 N64 K64, S rounded to bf16), so that an O buffer is
-//              held only from the end of the conversion until the tile's
-//              output is read.
+//              from tensor memory), which hands P buffer t & 1 back to the
+//              front issuer as soon as it completes, then, with S(t) staged,
+//              O(t) += Q S  (M128 N64 K64, S rounded to bf16), so that an O
+//              buffer is held only from the end of the conversion until the
+//              tile's output is read.
 //   warps 3-10 P conversion, two warps per TMEM lane quarter, one per
 //              64-column half: each thread owns one tile row (TMEM lane) and
 //              turns its half of P(t) into the masked bf16 A operand in place
@@ -106,12 +107,14 @@ struct OutSmem {
   // barrier slots (8 bytes each); the pairs are used by alternate tiles (or
   // phase-1 pieces).  Empty takes two arrivals per use: the front issuer's
   // and the O issuer's MMAs both read a tile's stage (the front issuer
-  // arrives twice on a phase-1 stage).
+  // arrives twice on a phase-1 stage).  PFree (P V done: the P buffer may be
+  // overwritten) is apart from OReady (P V and Q S done), so that the next
+  // Q K^T into a P buffer does not wait for the state staging Q S waits for.
   static constexpr int kFull = 0, kEmpty = kStages, kPReady = 2 * kStages,
                        kPDone = kPReady + 2, kOReady = kPReady + 4, kOFree = kPReady + 6,
                        kSSmem = kPReady + 8, kDReady = kPReady + 10, kDFree = kPReady + 12,
                        kP1Ready = kPReady + 14, kP1Free = kPReady + 16, kP1Done = kPReady + 18,
-                       kNumBars = kPReady + 19;
+                       kPFree = kPReady + 19, kNumBars = kPReady + 21;
   static constexpr uint32_t kTmemSlot = kBar + 8 * kNumBars;
   static constexpr uint32_t kCoord = kTmemSlot + 8;              // (row0, head) of the first tiles
   static constexpr uint32_t kP1 = kCoord + 8 * kCoordSlots;      // phase-1 piece records
@@ -245,6 +248,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_init(bar(L::kPReady + b), 1);
       mbar_init(bar(L::kPDone + b), kConvThreads);
       mbar_init(bar(L::kOReady + b), 1);
+      mbar_init(bar(L::kPFree + b), 1);
       mbar_init(bar(L::kOFree + b), kGroupThreads);
       mbar_init(bar(L::kSSmem + b), kGroupThreads);
       mbar_init(bar(L::kDReady + b), 1);
@@ -408,7 +412,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       __syncwarp();
       // P buffer b is free once P V of tile i-2 (which read it) has completed.
       bool ok2 = true;
-      if (i >= 2) ok2 = wait_or_flag(bar(L::kOReady + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
+      if (i >= 2) ok2 = wait_or_flag(bar(L::kPFree + b), ((i - 2) >> 1) & 1, err, kErrTimeoutMma);
       if (!__all_sync(0xffffffffu, ok2)) break;
       tc_fence_after_sync();
       if (lane == 0) {
@@ -461,6 +465,7 @@ span_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           mma_bf16_tmem_a(tmem + colO, tmem + colP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
                           smem_desc_sw128(st + L::kV + kk * 2048, kRowTileBytes, 1024),
                           id_n64_b_mn, kk > 0 ? 1u : 0u);
+        mma_commit(bar(L::kPFree + b));
       }
       __syncwarp();
       // S(i) staged: O(i) += Q S; release the stage.
