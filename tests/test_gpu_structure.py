@@ -32,6 +32,70 @@ def test_run_to_run_bit_identical(cuda_device):
     assert torch.equal(s1, s2)
 
 
+
+@pytest.mark.parametrize("variant", ["one_launch", "three_launches"])
+def test_repeated_passes_bit_identical(cuda_device, variant):
+    """Thirty passes of the 7,400-token request, with the L2 written over, a
+    side stream and back-to-back launches between them, all equal to the
+    first bit for bit: the hand-offs between the kernel's warps (tensor
+    memory, shared-memory operands and staging) leave no timing-dependent
+    result, whichever order the roles happen to run in."""
+    spanla.set_pass_variant(spanla.PASS_ONE_LAUNCH if variant == "one_launch" else spanla.PASS_THREE_LAUNCHES)
+    try:
+        w = workloads.single_request(3)
+        q, k, v = to_device(w, cuda_device)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=cuda_device)
+        side = torch.cuda.Stream(cuda_device)
+        ref, ref_state = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+        span_la_check()
+        outs = []
+        for rep in range(30):
+            if rep % 3 == 0:
+                flush.fill_(rep & 0xFF)      # L2 full of dirty lines
+            if rep % 3 == 1:
+                side.wait_stream(torch.cuda.current_stream(cuda_device))
+                with torch.cuda.stream(side):
+                    o, s = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, stream=side)
+                torch.cuda.current_stream(cuda_device).wait_stream(side)
+            else:
+                o, s = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent)
+            outs.append((o, s))
+        torch.cuda.synchronize(cuda_device)
+        span_la_check()
+        span_la_check(side)
+        seg = torch.zeros(w.T, dtype=torch.bool)
+        seg[: w.branch_cu[-1]] = True
+        seg = seg.to(cuda_device)
+        for o, s in outs:
+            assert torch.equal(o[seg], ref[seg])
+            assert torch.equal(s, ref_state)
+    finally:
+        spanla.set_pass_variant(spanla.PASS_ONE_LAUNCH)
+
+
+def test_repeated_softmax_passes_bit_identical(cuda_device):
+    """The softmax layer: twenty calls over the 7,400-token request, the L2
+    written over between some of them, all equal to the first bit for bit
+    (the two softmax warps of a row quarter hand the running maximum to each
+    other, so their relative timing must not change a result)."""
+    w = workloads.single_request(4)
+    q, k, v = to_device(w, cuda_device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=cuda_device)
+    lse0 = torch.empty((w.T, w.H), dtype=torch.float32, device=cuda_device)
+    ref = spanla.span_la_softmax_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, lse=lse0)
+    span_la_check()
+    seg = torch.zeros(w.T, dtype=torch.bool)
+    seg[: w.branch_cu[-1]] = True
+    seg = seg.to(cuda_device)
+    for rep in range(20):
+        if rep % 2 == 0:
+            flush.fill_(rep & 0xFF)
+        lse = torch.empty_like(lse0)
+        o = spanla.span_la_softmax_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent, lse=lse)
+        span_la_check()
+        assert torch.equal(o[seg], ref[seg])
+        assert torch.equal(lse[seg], lse0[seg])
+
 def _pack(view_len, branches, H, seed):
     """A view plus the given list of (name, rows) branches, each row drawn from
     the same per-branch seeded stream so a branch is identical wherever it sits."""
