@@ -894,9 +894,31 @@ def main():
                 assert st_c == 0
             torch.cuda.synchronize()
             spanla.span_la_check()
+        # The same new plans built ahead by span_la_plan_prepare (as a server
+        # would while the pass's inputs are copied in): the host time of the
+        # prepare call, and of the pass that then finds its plan cached.
+        prep_host, chost_p = None, None
+        if not shards_mode:
+            prep_host, chost_p = [], []
+            dt_c = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+            for i in range(2 * NV):
+                bcu_j, par_j = variants[(i + 1) % NV]
+                torch.cuda.synchronize()
+                cbusy.zero_()
+                t_h = time.perf_counter()
+                spanla.span_la_plan_prepare(w.view_cu, bcu_j, par_j, q.shape[0], q.shape[1], dtype=dt_c)
+                prep_host.append((time.perf_counter() - t_h) * 1e6)
+                t_h = time.perf_counter()
+                st_c = lib_c.span_la_pass(*raw_c[(i + 1) % NV])
+                chost_p.append((time.perf_counter() - t_h) * 1e6)
+                assert st_c == 0
+            torch.cuda.synchronize()
+            spanla.span_la_check()
         del cbusy
         cold = {"cold_plan_ms_per_step": cms, "cold_plan_host_us": statistics.median(chost),
                 "cold_plan_host_us_c_abi": statistics.median(chost_c) if chost_c else None,
+                "prepare_host_us": statistics.median(prep_host) if prep_host else None,
+                "prepared_pass_host_us_c_abi": statistics.median(chost_p) if chost_p else None,
                 "cold_plan_value": rows_per_step / (cms / 1e3), "variants": NV, "steps": KC,
                 "mode": "branch lengths permuted within each parent's run of branches: a new "
                         "plan (host build + descriptor upload) in every step"}

@@ -14,6 +14,7 @@ from .spanla import (  # noqa: F401
     span_la_check,
     span_la_pass,
     span_la_pass_noalloc,
+    span_la_plan_prepare,
     span_la_softmax_branches_from_kv,
     span_la_softmax_pass,
 )

@@ -999,6 +999,15 @@ std::vector<int32_t> plan_key(int device, int dtype, int H, int from_state, int 
   return key;
 }
 
+// Cache key of a span_la_pass plan.  span_la_plan_prepare uses the same key,
+// so that a pass finds the plan prepared for its metadata.
+std::vector<int32_t> pass_key(int device, const span_la_dims& dims, int num_sms, bool fused,
+                              const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
+                              int32_t B, const int32_t* parent) {
+  return plan_key(device, dims.dtype, dims.num_heads, fused ? 4 : 0, num_sms, view_cu, V, branch_cu, B,
+                  parent);
+}
+
 // The device block for `key` (built by `build` on a miss), usable on `stream`.
 // The caller holds g_cache_mu until its launches are enqueued and recorded
 // with note_reader on `*entry`, so that no other call evicts the block (or
@@ -1472,14 +1481,51 @@ span_la_status span_la_pass(const void* q, const void* k, const void* v, span_la
   int device = 0;
   cudaGetDevice(&device);
   const bool fused = one_launch();
-  const std::vector<int32_t> key = plan_key(device, dims.dtype, dims.num_heads, fused ? 4 : 0, dev->num_sms,
-                                            view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
-                                            branch_parent);
+  const std::vector<int32_t> key = pass_key(device, dims, dev->num_sms, fused, view_cu_seqlens, num_views,
+                                            branch_cu_seqlens, num_branches, branch_parent);
   auto build = [&] {
     return make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches, branch_parent,
                      dims.num_heads, dims.dtype == SPAN_LA_BF16, dev->num_sms, fused);
   };
   return run_plan(key, build, q, k, v, dims, view_state_out, view_state_out, out, stream, dev, device);
+}
+
+span_la_status span_la_plan_prepare(span_la_dims dims, const int32_t* view_cu_seqlens, int32_t num_views,
+                                    const int32_t* branch_cu_seqlens, int32_t num_branches,
+                                    const int32_t* branch_parent, cudaStream_t stream) {
+  g_detail.clear();
+  span_la_status st = check_dims(dims);
+  if (st != SPAN_LA_OK) return st;
+  std::vector<Segment> segs;
+  if ((st = check_cu(view_cu_seqlens, num_views, dims.total_rows, "view_cu_seqlens", &segs, true)) != SPAN_LA_OK) return st;
+  if ((st = check_cu(branch_cu_seqlens, num_branches, dims.total_rows, "branch_cu_seqlens", &segs, false)) != SPAN_LA_OK) return st;
+  if ((st = check_overlap(segs)) != SPAN_LA_OK) return st;
+  if ((st = check_parents(branch_parent, num_branches, num_views)) != SPAN_LA_OK) return st;
+  if (num_views == 0 && num_branches == 0) return SPAN_LA_OK;
+
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != SPAN_LA_OK) return st;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(SPAN_LA_ERR_UNSUPPORTED, "span_la_plan_prepare: the stream is being captured (captured "
+                                     "passes do not use the plan cache)");
+  int device = 0;
+  cudaGetDevice(&device);
+  const bool fused = one_launch();
+  const std::vector<int32_t> key = pass_key(device, dims, dev->num_sms, fused, view_cu_seqlens, num_views,
+                                            branch_cu_seqlens, num_branches, branch_parent);
+  auto build = [&] {
+    return make_desc(make_plan(view_cu_seqlens, num_views, branch_cu_seqlens, num_branches, branch_parent,
+                               dims.num_heads, dims.dtype == SPAN_LA_BF16, dev->num_sms, fused),
+                     dims.num_heads);
+  };
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  const DescBlock* desc = nullptr;
+  const uint8_t* block = nullptr;
+  CacheEntry* entry = nullptr;
+  return cached_block(key, device, stream, build, &desc, &block, &entry);
 }
 
 span_la_status span_la_softmax_pass(const void* q, const void* k, const void* v, span_la_dims dims,

@@ -34,7 +34,8 @@ EXPORTED = ("span_la_pass", "span_la_branches_from_state", "span_la_check",
             "span_la_cache_put", "span_la_cache_contains", "span_la_cache_branches",
             "span_la_cache_stats", "span_la_softmax_pass", "span_la_softmax_branches_from_kv",
             "span_la_fault_inject", "span_la_softmax_plan_stats",
-            "span_la_selftest_wait_timeout_noalloc", "span_la_pass_variant")
+            "span_la_selftest_wait_timeout_noalloc", "span_la_pass_variant",
+            "span_la_plan_prepare")
 NUM_KERNELS = 7
 
 
@@ -112,6 +113,8 @@ def load_library(path: Optional[str] = None):
         lib.span_la_softmax_plan_stats.restype = ctypes.c_int
         lib.span_la_pass_variant.argtypes = [ctypes.c_int32]
         lib.span_la_pass_variant.restype = ctypes.c_int
+        lib.span_la_plan_prepare.argtypes = [Dims, i32p, ctypes.c_int32, i32p, ctypes.c_int32, i32p, vp]
+        lib.span_la_plan_prepare.restype = ctypes.c_int
         lib.span_la_fault_inject.argtypes = [ctypes.c_int32, ctypes.c_int32]
         lib.span_la_fault_inject.restype = ctypes.c_int
         lib.span_la_softmax_branches_from_kv.argtypes = [vp, vp, ctypes.c_int64, i32p, ctypes.c_int32,
@@ -239,6 +242,28 @@ def span_la_pass(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                               out.data_ptr(), view_state_out.data_ptr(), _stream_handle(stream))
     _raise(lib, st, _entry)
     return out, view_state_out
+
+
+def span_la_plan_prepare(view_cu_seqlens: Sequence[int], branch_cu_seqlens: Optional[Sequence[int]],
+                         branch_parent: Optional[Sequence[int]], total_rows: int, num_heads: int,
+                         dtype: torch.dtype = torch.bfloat16,
+                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Build and upload the plan of a later :func:`span_la_pass` with this
+    metadata on the current device (``span_la_plan_prepare`` in
+    ``include/spanla.h``), so that the pass finds it in the plan cache."""
+    lib = load_library()
+    if dtype == torch.bfloat16:
+        dt = SPAN_LA_BF16
+    elif dtype == torch.float32:
+        dt = SPAN_LA_F32
+    else:
+        raise ValueError("dtype %s not supported (bf16 or fp32)" % dtype)
+    vcu, bcu, par = _i32(view_cu_seqlens), _i32(branch_cu_seqlens), _i32(branch_parent)
+    V = max(len(vcu) - 1, 0)
+    B = max(len(bcu) - 1, 0)
+    st = lib.span_la_plan_prepare(Dims(int(total_rows), int(num_heads), 64, dt), _iptr(vcu), V,
+                                  _iptr(bcu), B, _iptr(par), _stream_handle(stream))
+    _raise(lib, st, "span_la_plan_prepare")
 
 
 def span_la_pass_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -130,6 +130,45 @@ span_la_status span_la_pass(const void *q, const void *k, const void *v,
                             cudaStream_t stream);
 
 /*
+ * span_la_plan_prepare -- build and upload the launch plan of a later
+ * span_la_pass, ahead of that call.
+ *
+ * Section "Batching in the Router": the router packs a pass from the
+ * requests it has gathered, so the pass's metadata is known before its rows
+ * reach the GPU.  Section "Kernels": a pass is launched from descriptors
+ * built on the host from that metadata.  span_la_pass builds them on its first
+ * call with new metadata (tens of microseconds of host time) and keeps them
+ * in the per-device plan cache; this call does the same work earlier, for
+ * example while the pass's q, k and v are still being copied in, so that the
+ * pass itself finds the plan in the cache.  It computes nothing and touches
+ * no q, k, v or output buffer.
+ *
+ *   dims             as the pass's dims (total_rows bounds the metadata;
+ *                    num_heads and dtype select the plan)
+ *   view_cu_seqlens, num_views, branch_cu_seqlens, num_branches,
+ *   branch_parent    as for span_la_pass (host arrays, read during the call)
+ *   stream           the descriptor upload is enqueued here (pinned staging,
+ *                    stream ordered); a pass on another stream waits for it
+ *                    through an event
+ *   match            a span_la_pass on the same device with the same
+ *                    metadata, num_heads, dtype and pass structure
+ *                    (span_la_pass_variant) uses the prepared plan.  The
+ *                    cache holds 16 plans per device, least recently used
+ *                    evicted: a plan is lost if 16 others are used or
+ *                    prepared after it and before its pass.  Preparing a
+ *                    plan that is already cached only marks it as used
+ *   errors           metadata problems as for span_la_pass, nothing
+ *                    enqueued; SPAN_LA_ERR_UNSUPPORTED while `stream` is
+ *                    being captured (captured passes do not use the cache);
+ *                    SPAN_LA_ERR_NOMEM if the descriptor block cannot be
+ *                    allocated (stream ordered, on `stream`)
+ */
+span_la_status span_la_plan_prepare(span_la_dims dims,
+                                    const int32_t *view_cu_seqlens, int32_t num_views,
+                                    const int32_t *branch_cu_seqlens, int32_t num_branches,
+                                    const int32_t *branch_parent, cudaStream_t stream);
+
+/*
  * span_la_branches_from_state -- branches only, each forking from a cached
  * view state.
  *

@@ -248,6 +248,44 @@ def test_plan_reused_across_calls_and_streams(cuda_device):
         assert rel_err(f64(state), ref_state) <= TOL["bf16"]
 
 
+def test_prepared_plan_is_used_by_the_pass(cuda_device):
+    """span_la_plan_prepare puts a pass's plan in the cache before the pass:
+    preparing it again allocates nothing (a pending forced allocation failure
+    is not reached), and the pass that follows on another stream gives the
+    bits of a pass that builds its own plan (the no-allocation entry point
+    plans every call) and the oracle's results.  A capturing stream is
+    refused."""
+    from helpers import TOL, f64, rel_err, segment_rows
+    from oracle import oracle_pass
+    w = workloads.make_pass([1300, 250], [40, 90, 33, 200, 7], [0, 0, 1, 1, 1], H=4, dtype="bf16",
+                            seed=60)
+    side = torch.cuda.Stream(device=cuda_device)
+    spanla.span_la_plan_prepare(w.view_cu, w.branch_cu, w.branch_parent, w.T, w.H, stream=side)
+    spanla.fault_inject(spanla.FAULT_ALLOC, 1)
+    try:
+        spanla.span_la_plan_prepare(w.view_cu, w.branch_cu, w.branch_parent, w.T, w.H, stream=side)
+    finally:
+        spanla.fault_inject(spanla.FAULT_ALLOC, 0)
+    q, k, v = to_device(w, cuda_device)
+    out, state = span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
+                              out=torch.full_like(q, float("nan")))
+    out_own, state_own = spanla.span_la_pass_noalloc(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
+                                                     out=torch.full_like(q, float("nan")))
+    torch.cuda.synchronize()
+    span_la_check()
+    seg = segment_rows(w)
+    segt = torch.from_numpy(seg)
+    assert torch.equal(out.cpu()[segt], out_own.cpu()[segt]) and torch.equal(state, state_own)
+    ref, ref_state = oracle_pass(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu, w.branch_parent)
+    assert rel_err(f64(out)[seg], ref[seg]) <= TOL["bf16"]
+    assert rel_err(f64(state), ref_state) <= TOL["bf16"]
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(SpanLAError) as exc:
+        with torch.cuda.graph(g):
+            spanla.span_la_plan_prepare(w.view_cu, w.branch_cu, w.branch_parent, w.T, w.H)
+    assert exc.value.status == 2
+
+
 def test_plan_cache_eviction_is_stream_ordered(cuda_device):
     """More distinct layouts than the plan cache keeps per device (16): each
     further one evicts the least recently used descriptor block, freed in

@@ -75,6 +75,32 @@ def test_bad_metadata_is_rejected_before_any_launch(lib, vcu, bcu, par, what):
     assert st == 1 and what in detail
 
 
+def _prepare(lib, vcu, bcu, par, dims=None):
+    dims = dims or _dims()
+    (va, vp), (ba, bp), (pa, pp) = _arr(vcu), _arr(bcu), _arr(par)
+    V, B = max(len(va) - 1, 0), max(len(ba) - 1, 0)
+    st = lib.span_la_plan_prepare(dims, vp if V else None, V, bp if B else None, B,
+                                  pp if B else None, None)
+    return st, lib.span_la_last_error_detail().decode()
+
+
+@pytest.mark.parametrize("vcu,bcu,par,what", [
+    ([0, 50, 40], [], [], "non-decreasing"),
+    ([0, 101], [], [], "non-decreasing"),
+    ([0, 50], [40, 60], [0], "overlap"),
+    ([0, 50], [50, 60], [1], "branch_parent"),
+])
+def test_plan_prepare_rejects_what_the_pass_rejects(lib, vcu, bcu, par, what):
+    """span_la_plan_prepare runs the pass's metadata checks before any device
+    work: the same metadata gets the same status and detail."""
+    st, detail = _prepare(lib, vcu, bcu, par)
+    assert st == 1 and what in detail
+    assert (st, detail) == _pass(lib, vcu, bcu, par)
+    st, detail = _prepare(lib, [0, 10], [], [], dims=_dims(D=128))
+    assert st == 2 and "head_dim" in detail
+    assert _prepare(lib, [0], [], [])[0] == 0   # nothing to plan: no device work
+
+
 def test_unsupported_shapes_and_pointers(lib):
     st, detail = _pass(lib, [0, 10], [], [], dims=_dims(D=128))
     assert st == 2 and "head_dim" in detail
