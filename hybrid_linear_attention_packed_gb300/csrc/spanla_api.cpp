@@ -407,26 +407,26 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
     int64_t row0, len;
     int ntiles;
   };
+  // The blocks of head 0 first; the other heads repeat them.
   std::vector<Block> blocks;
   blocks.reserve(static_cast<size_t>(H) * (V + groups.size()));
-  int64_t W = 0;
-  for (int h = 0; h < H; ++h) {
-    for (size_t r = 0; r < requests.size(); ++r) {
-      const int p = requests[r];
-      if (p < V) {
-        const int64_t len = view_cu[p + 1] - view_cu[p];
-        const int nt = static_cast<int>((len + kTileRows - 1) / kTileRows);
-        blocks.push_back({0, p, h, view_cu[p], len, nt});
-        W += nt;
-      }
-      for (int g : by_parent_idx[r]) {
-        const BranchGroup& bg = groups[g];
-        const int nt = bg.is_long ? static_cast<int>((bg.len + kTileRows - 1) / kTileRows) : 1;
-        blocks.push_back({bg.is_long ? 1 : 2, g, h, bg.row0, bg.len, nt});
-        W += nt;
-      }
+  int64_t W0 = 0;
+  for (size_t r = 0; r < requests.size(); ++r) {
+    const int p = requests[r];
+    if (p < V) {
+      const int64_t len = view_cu[p + 1] - view_cu[p];
+      const int nt = static_cast<int>((len + kTileRows - 1) / kTileRows);
+      blocks.push_back({0, p, 0, view_cu[p], len, nt});
+      W0 += nt;
+    }
+    for (int g : by_parent_idx[r]) {
+      const BranchGroup& bg = groups[g];
+      const int nt = bg.is_long ? static_cast<int>((bg.len + kTileRows - 1) / kTileRows) : 1;
+      blocks.push_back({bg.is_long ? 1 : 2, g, 0, bg.row0, bg.len, nt});
+      W0 += nt;
     }
   }
+  const int64_t W = W0 * H;
 
   // Runs.  Every head has the same sequence of tiles, so when the SMs can
   // be split evenly over the heads, each head's sequence is cut into R equal
@@ -440,6 +440,19 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
   const bool aligned = R >= 1 && per_head > 0 && static_cast<int64_t>(R) * H * 100 >= static_cast<int64_t>(sms) * 85;
   const int Rh = aligned ? static_cast<int>(std::min<int64_t>(R, per_head)) : 0;
   const int grid = aligned ? Rh * H : static_cast<int>(std::min<int64_t>(W, sms));
+  // With runs aligned to heads, run (p, h) is run (p, 0) with the head (and
+  // the slots) shifted: passes 1 and 2 below plan head 0 only, and its
+  // records are repeated for the other heads afterwards.  Otherwise every
+  // head's blocks are planned.
+  const bool per_head_copy = aligned && H > 1;
+  if (!per_head_copy) {
+    const size_t n0 = blocks.size();
+    for (int h = 1; h < H; ++h)
+      for (size_t i = 0; i < n0; ++i) {
+        blocks.push_back(blocks[i]);
+        blocks.back().head = h;
+      }
+  }
   // start of CTA c's run in the head-major sequence, and its length
   auto run_start = [&](int c) -> int64_t {
     if (!aligned) return grid > 0 ? static_cast<int64_t>(c) * W / grid : 0;
@@ -607,6 +620,43 @@ Plan make_span_plan(const int32_t* view_cu, int32_t V, const int32_t* branch_cu,
       }
     }
     g0 += bk.ntiles;
+  }
+  if (per_head_copy) {
+    // Head h: the pieces, slots and scan entries of head 0 shifted by h
+    // heads (slots are numbered head after head, S0 per head), and run
+    // (p, h) a copy of run (p, 0) in CTA p H + h.
+    const int32_t S0 = static_cast<int32_t>(pieces.size());
+    const size_t n_scan0 = plan.scan.size();
+    for (int h = 1; h < H; ++h) {
+      for (int32_t u = 0; u < S0; ++u) {
+        SpanDesc sd = pieces[u];
+        sd.head = h;
+        sd.slot += h * S0;
+        pieces.push_back(sd);
+        piece_cta.push_back(piece_cta[u] + h);
+      }
+      for (size_t e = 0; e < n_scan0; ++e) {
+        ScanDesc sc = plan.scan[e];
+        if (sc.nslots > 0) sc.slot0 += h * S0;
+        sc.head = h;
+        plan.scan.push_back(sc);
+      }
+    }
+    for (int p = 0; p < Rh; ++p) {
+      const WorkTile* src = plan.work.data() + plan.cta_begin[p * H];
+      const int32_t n = plan.cta_begin[p * H + 1] - plan.cta_begin[p * H];
+      for (int h = 1; h < H; ++h) {
+        WorkTile* dst = plan.work.data() + plan.cta_begin[p * H + h];
+        std::memcpy(dst, src, static_cast<size_t>(n) * sizeof(WorkTile));
+        for (int32_t i = 0; i < n; ++i) {
+          dst[i].head = h;
+          // the parent's final state (three launches, or a carry) is not a slot
+          if (fused && dst[i].stateA >= 0) dst[i].stateA += h * S0;
+          if (dst[i].stateB >= 0) dst[i].stateB += h * S0;
+        }
+      }
+    }
+    plan.n_pieces *= H;
   }
   if (fused) {
     // phase-1 pieces listed per output CTA (index = the CTA of the run)
