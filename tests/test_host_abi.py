@@ -191,6 +191,29 @@ def test_plan_covers_every_row_once(lib, dtype, name, variant):
         assert st["scan_segments"] == 0
 
 
+@pytest.mark.parametrize("variant", [spanla.PASS_ONE_LAUNCH, spanla.PASS_THREE_LAUNCHES])
+@pytest.mark.parametrize("H,sms", [(16, 152), (8, 152), (3, 152), (48, 152), (4, 20)])
+def test_head_aligned_plan_is_heads_times_one_head(lib, variant, H, sms):
+    """When the runs line up with the heads (R = SMs // H runs per head), the
+    planner plans one head and copies it to the others; every count summed
+    over heads must then be H times that of the one-head plan on R SMs,
+    which the planner builds directly."""
+    from hybrid_linear_attention_packed_gb300 import workloads
+    R = sms // H
+    assert R * H * 100 >= sms * 85   # the aligned case
+    spanla.set_pass_variant(variant)
+    try:
+        for w in (workloads.single_request(0), workloads.packed_four(2)):
+            many = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, H, num_sms=sms)
+            one = spanla.plan_stats(w.view_cu, w.branch_cu, w.branch_parent, 1, num_sms=R)
+            for f in ("state_slots", "state_rows", "scan_segments", "final_states", "tiles",
+                      "tile_rows", "start_state_reads", "out_items"):
+                assert many[f] == H * one[f], (f, many[f], one[f])
+            assert many["run_tiles"] == one["run_tiles"]
+    finally:
+        spanla.set_pass_variant(spanla.PASS_ONE_LAUNCH)
+
+
 def test_one_launch_plan_of_a_pass_that_fits_one_run_per_request(lib):
     """Requests small next to a run: in the one-launch pass a view whose
     branches all lie in the run that holds its last tile publishes nothing
