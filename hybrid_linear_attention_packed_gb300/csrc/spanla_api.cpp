@@ -912,7 +912,9 @@ cudaError_t upload_pinned(void* dst, const std::vector<uint8_t>& bytes, int devi
   for (auto& b : g_pin) {
     if (b.device != device) continue;
     ++mine;
-    if (b.cap >= n && pinned_free(b) && (pick == nullptr || b.cap < pick->cap)) pick = &b;
+    // the smallest free buffer that fits; an event is queried only for a
+    // buffer that would be a better pick (each query costs host time)
+    if (b.cap >= n && (pick == nullptr || b.cap < pick->cap) && pinned_free(b)) pick = &b;
   }
   cudaError_t e = cudaSuccess;
   if (pick == nullptr) {
@@ -972,6 +974,25 @@ struct CacheEntry {
   uint64_t last_use = 0;
 };
 
+// Events of the plan cache (upload and reader events), kept for reuse per
+// device instead of being destroyed and created on every miss (guarded by
+// g_cache_mu, like the cache).
+std::vector<cudaEvent_t> g_cache_events[kMaxDevices];
+
+cudaError_t take_cache_event(int device, cudaEvent_t* ev) {
+  std::vector<cudaEvent_t>& spare = g_cache_events[device & (kMaxDevices - 1)];
+  if (!spare.empty()) {
+    *ev = spare.back();
+    spare.pop_back();
+    return cudaSuccess;
+  }
+  return cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+}
+
+void give_cache_event(int device, cudaEvent_t ev) {
+  if (ev != nullptr) g_cache_events[device & (kMaxDevices - 1)].push_back(ev);
+}
+
 // Records on `stream` that the launches just enqueued there read `en`'s
 // block.  A new stream beyond kMaxReaders takes over the oldest reader: it
 // first waits for that reader's event, so its own event covers both.
@@ -988,11 +1009,11 @@ cudaError_t note_reader(CacheEntry& en, cudaStream_t stream) {
     return e;
   }
   cudaEvent_t ev = nullptr;
-  cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  cudaError_t e = take_cache_event(en.device, &ev);
   if (e != cudaSuccess) return e;
   e = cudaEventRecord(ev, stream);
   if (e != cudaSuccess) {
-    cudaEventDestroy(ev);
+    give_cache_event(en.device, ev);
     return e;
   }
   en.readers.emplace_back(stream, ev);
@@ -1006,14 +1027,15 @@ cudaError_t release_entry(CacheEntry& en, cudaStream_t stream) {
   if (en.sync_on_evict) {
     e = cudaDeviceSynchronize();
   } else {
-    e = cudaStreamWaitEvent(stream, en.uploaded, 0);
+    // work already on `stream` is ordered before the free without a wait
+    if (en.upload_stream != stream) e = cudaStreamWaitEvent(stream, en.uploaded, 0);
     for (const auto& r : en.readers)
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, r.second, 0);
+      if (e == cudaSuccess && r.first != stream) e = cudaStreamWaitEvent(stream, r.second, 0);
   }
   if (e == cudaSuccess) e = cudaFreeAsync(en.d_block, stream);
   if (e != cudaSuccess) return e;
-  for (const auto& r : en.readers) cudaEventDestroy(r.second);
-  cudaEventDestroy(en.uploaded);
+  for (const auto& r : en.readers) give_cache_event(en.device, r.second);
+  give_cache_event(en.device, en.uploaded);
   return cudaSuccess;
 }
 
@@ -1102,10 +1124,10 @@ span_la_status cached_block(const std::vector<int32_t>& key, int device, cudaStr
   if (e != cudaSuccess)
     return fail(SPAN_LA_ERR_NOMEM, "cudaMallocAsync(descriptors, %zu): %s", bytes, cudaGetErrorString(e));
   e = upload_pinned(en.d_block, en.desc.host, device, stream);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&en.uploaded, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = take_cache_event(device, &en.uploaded);
   if (e == cudaSuccess) e = cudaEventRecord(en.uploaded, stream);
   if (e != cudaSuccess) {
-    if (en.uploaded != nullptr) cudaEventDestroy(en.uploaded);
+    give_cache_event(device, en.uploaded);
     cudaFreeAsync(en.d_block, stream);
     return cuda_fail(e, "descriptor upload");
   }
