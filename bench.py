@@ -857,6 +857,24 @@ def main():
         torch.cuda.synchronize()
         spanla.span_la_check()
         cms = statistics.mean(a.elapsed_time(b) for a, b in zip(cs, ce))
+        # The same fresh plans, each prepared on a side stream while the L2
+        # flush before its step runs (a server preparing the next pass while
+        # the device is busy): the pass waits for the upload through an event.
+        cms_p = None
+        if not shards_mode:
+            side = torch.cuda.Stream(device=dev)
+            dt_p = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+            for i in range(KC):
+                bcu_j, par_j = variants[i % NV]
+                spanla.span_la_plan_prepare(w.view_cu, bcu_j, par_j, q.shape[0], q.shape[1], dtype=dt_p,
+                                            stream=side)
+                flush.zero_()
+                cs[i].record(stream)
+                cold_call(i % NV)
+                ce[i].record(stream)
+            torch.cuda.synchronize()
+            spanla.span_la_check()
+            cms_p = statistics.mean(a.elapsed_time(b) for a, b in zip(cs, ce))
         # Host time of one call that builds a new plan, with the device busy
         # on earlier work (as in a serving loop) but no backlog of calls
         # ahead of it: the loop above runs ahead of the device, so its host
@@ -917,6 +935,7 @@ def main():
         del cbusy
         cold = {"cold_plan_ms_per_step": cms, "cold_plan_host_us": statistics.median(chost),
                 "cold_plan_host_us_c_abi": statistics.median(chost_c) if chost_c else None,
+                "prepared_ms_per_step": cms_p,
                 "prepare_host_us": statistics.median(prep_host) if prep_host else None,
                 "prepared_pass_host_us_c_abi": statistics.median(chost_p) if chost_p else None,
                 "cold_plan_value": rows_per_step / (cms / 1e3), "variants": NV, "steps": KC,
