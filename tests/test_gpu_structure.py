@@ -335,6 +335,37 @@ def test_plan_cache_eviction_is_stream_ordered(cuda_device):
         check(i, res)
 
 
+def test_prepared_plans_across_evictions_and_streams(cuda_device):
+    """Forty layouts, each prepared on a side stream held back by device work
+    and then passed on the current stream without a host synchronisation:
+    every pass waits for its plan's upload, evictions (more layouts than the
+    cache's 16) hand their events on to later plans, and every result matches
+    the oracle."""
+    from helpers import TOL, f64, rel_err, segment_rows
+    from oracle import oracle_pass
+
+    ws = [workloads.make_pass([200 + 13 * i, 140], [25, 70, 9], [0, 1, 1], H=2, dtype="bf16", seed=300 + i)
+          for i in range(40)]
+    ins = [to_device(w, cuda_device) for w in ws]
+    side = torch.cuda.Stream(device=cuda_device)
+    torch.cuda.synchronize()
+    results = []
+    for i, w in enumerate(ws):
+        with torch.cuda.stream(side):
+            torch.cuda._sleep(1_000_000)          # the upload lands after the pass is enqueued
+        spanla.span_la_plan_prepare(w.view_cu, w.branch_cu, w.branch_parent, w.T, w.H, stream=side)
+        q, k, v = ins[i]
+        results.append(span_la_pass(q, k, v, w.view_cu, w.branch_cu, w.branch_parent,
+                                    out=torch.full_like(q, float("nan"))))
+    torch.cuda.synchronize()
+    span_la_check()
+    for w, (out, state) in zip(ws, results):
+        ref, ref_state = oracle_pass(f64(w.q), f64(w.k), f64(w.v), w.view_cu, w.branch_cu, w.branch_parent)
+        seg = segment_rows(w)
+        assert rel_err(f64(out)[seg], ref[seg]) <= TOL["bf16"]
+        assert rel_err(f64(state), ref_state) <= TOL["bf16"]
+
+
 def _graph_replay_equals_eager(dev, record, w_a, w_b):
     """Record `record(q, k, v, outs)` into a CUDA graph on inputs A, replay it
     after copying inputs B into the same buffers, and compare with an eager
