@@ -51,7 +51,10 @@
  *   pass, branch and softmax calls do not synchronise the device: the
  *   per-device cache of launch plans (16 per device, keyed on the metadata,
  *   least recently used evicted) frees an evicted plan in stream order
- *   behind the calls that read it.
+ *   behind the calls that read it.  The cached plans, their events and the
+ *   pinned staging buffers belong to the device's primary context and live
+ *   until the process exits: do not call the library on a device after a
+ *   cudaDeviceReset of that device.
  * Graphs.  The pass, branch and softmax calls may be recorded while `stream`
  *   is being captured into a CUDA graph: the recorded work replays on the
  *   buffers of the recorded call (their current contents), with its own
